@@ -1,0 +1,240 @@
+/*
+ * tv.h: C ABI of the GB300 tree-verify library (one shared object,
+ * libtreeverify.so).  One call per step of a speculative-decoding verify
+ * round of a hybrid Gated DeltaNet + attention mixer stack, never one per
+ * operator; activations stay on the device.
+ *
+ * Sources (page title, section):
+ *  [TOUR]  "One request, end to end", 2.6 "The decode loop": the target
+ *          verifies the whole draft tree in one forward pass through every
+ *          layer, walks it with its own tokens, keeps the longest agreeing
+ *          path plus one token of its own, and commits that path's KV rows
+ *          and recurrent state.
+ *  [LEAF]  "How ignis serves a request", "The shape of the process": the
+ *          kernel leaf sits behind a flat C ABI named after its step
+ *          granularity; nothing it computes crosses the ABI as a host pointer.
+ *  [MODEL] "Adding a model", step 4 (hot verbs forward_tree, commit_tree,
+ *          rollback_to): every verified row must equal the decode step's row
+ *          bit for bit; "What is still specific to Qwen3.8": Gated DeltaNet
+ *          heads of 128 by 128 and attention layers.
+ *  [STATE] "Adding a model", "The model layer": per-sequence cache state is
+ *          the recurrent state (copied whole) plus K and V views with a token
+ *          axis sliced by length.
+ *  [PAR]   "Parallel requests", "Joint verify": several sequences' trees in
+ *          one pass, the mixers running per sequence.
+ *
+ * Conventions shared by every call
+ *  - Ownership: the caller allocates and owns every buffer (device memory
+ *    unless marked host).  The library allocates nothing in these calls and
+ *    keeps no pointer after a call returns.  Verify inputs (k_t, v_t, k, v,
+ *    alpha, beta) must stay alive until tv_commit_path has run on the stream.
+ *  - Streams: every call only enqueues work on `stream` (a cudaStream_t; NULL
+ *    is the legacy default stream) and never synchronises, so a whole round
+ *    can be captured in a CUDA graph.
+ *  - Errors: argument errors that the host can see return a tv_status
+ *    immediately and enqueue nothing.  Errors only the device can see (a
+ *    malformed tree, a cache that would overflow, a bounded wait that
+ *    expired) write their tv_status code into the caller's device status word
+ *    (first error wins) and make every later call that is given the same
+ *    word a no-op.  Nothing traps.
+ *  - Node-indexed arrays concatenate the sequences' trees: sequence s owns
+ *    global nodes node_off[s] .. node_off[s+1]-1, whose local index 0 is the
+ *    root.  The root is the last committed token: it is not yet in the cache
+ *    or in the state, and it is always accepted.
+ *  - Rows: a tree node at depth d (root depth 0) sees the L committed cache
+ *    rows plus its ancestors-or-self at logical positions L .. L+d, exactly
+ *    where decoding them one by one would have put them.
+ *  - Alignment: every device pointer 16-byte aligned.
+ */
+#ifndef TV_H
+#define TV_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef struct CUstream_st* tv_stream; /* same type as cudaStream_t */
+
+#define TV_MAX_SEQ 8    /* sequences in one launch */
+#define TV_MAX_NODES 64 /* nodes in one sequence's tree */
+#define TV_MAX_PATH 16  /* nodes on a root path, root included */
+
+typedef enum {
+  TV_OK = 0,
+  TV_ERR_ARG = 1,       /* null pointer, bad count or length bound */
+  TV_ERR_SHAPE = 2,     /* unsupported head count / head dim combination */
+  TV_ERR_DTYPE = 3,     /* unsupported element type */
+  TV_ERR_ALIGN = 4,     /* pointer not 16-byte aligned */
+  TV_ERR_TREE = 5,      /* device: malformed parent array or node offsets */
+  TV_ERR_CAPACITY = 6,  /* device: a write past a cache's `cap` rows */
+  TV_ERR_CUDA = 7,      /* a CUDA runtime call failed (launch, attribute) */
+  TV_ERR_WORKSPACE = 8, /* workspace smaller than the *_workspace_bytes bound */
+  TV_ERR_TIMEOUT = 9,   /* device: a bounded wait inside a kernel expired */
+  TV_ERR_LEN = 10       /* device: a sequence length above the host bound max_len */
+} tv_status;
+
+typedef enum { TV_F32 = 0, TV_BF16 = 1 } tv_dtype;
+
+/* Human-readable name of a status code (static string). */
+const char* tv_status_string(tv_status s);
+/* Library version string (static). */
+const char* tv_version(void);
+
+/* ------------------------------------------------------------------------
+ * Draft trees
+ * ------------------------------------------------------------------------
+ * [TOUR] (the block drafter's chain merged with the lookup drafter's
+ * branches into one tree).  A tree is a parent-index array in topological
+ * order: parent[0] = -1 and 0 <= parent[i] < i (sequence-local indices),
+ * 1..TV_MAX_NODES nodes, at most TV_MAX_PATH nodes on any root path.
+ */
+typedef struct {
+  int32_t n_seq;           /* sequences, 1..TV_MAX_SEQ (host) */
+  int32_t n_total;         /* nodes over all sequences (host) */
+  int32_t n_max;           /* host bound on any one tree's size, 1..TV_MAX_NODES */
+  const int32_t* node_off; /* device [n_seq+1], node_off[0] = 0, node_off[n_seq] = n_total */
+  const int32_t* parent;   /* device [n_total], sequence-local parent, -1 at the root */
+  void* meta;              /* device, tv_tree_meta_bytes() bytes: derived tables (private layout) */
+  int32_t* status;         /* device [1] error word, 0 = ok; shared by the calls of a round */
+} tv_tree;
+
+/* Bytes of the `meta` buffer for a launch of n_total nodes. */
+size_t tv_tree_meta_bytes(int32_t n_seq, int32_t n_total);
+
+/* Validate the trees and derive, into tree->meta, each node's depth,
+ * ancestor-or-self bitmask, ancestor at every depth, and the traversal order
+ * the recurrent layers use.  Must run (stream-ordered) before any call that
+ * takes the tree.  A malformed tree sets TV_ERR_TREE in *tree->status. */
+tv_status tv_tree_prepare(const tv_tree* tree, tv_stream stream);
+
+/* ------------------------------------------------------------------------
+ * Attention: tree-masked grouped-query attention over the KV cache
+ * ------------------------------------------------------------------------
+ * [TOUR], [MODEL].  For every node i and query head h (KV head
+ * g = h / (Hq/Hkv)):
+ *     out[i,h] = sum_p softmax_p(scale * q[i,h] . key_p) value_p
+ * over the L context rows of the cache and the ancestors-or-self of i.
+ */
+typedef struct {
+  tv_dtype dtype; /* element type of cache, q, k_t, v_t and out: TV_BF16 (tensor-core
+                     path, D in {64,128,256}) or TV_F32 (CUDA-core path, D in {64,128,256}) */
+  int32_t Hq, Hkv, D; /* Hq % Hkv == 0, Hq/Hkv <= 128 */
+  int32_t cap;        /* rows per KV head of every cache */
+  void* const* K;     /* host array [n_seq] of device pointers, each [Hkv][cap][D] */
+  void* const* V;     /* same layout as K */
+} tv_attn_layer;
+
+/* Fixed per model and shared by verify and decode: the positions of one KV
+ * split (a multiple of 64).  The split structure is part of the row function,
+ * so verify rows equal decode rows bit for bit only under the same plan. */
+typedef struct {
+  int32_t split;
+} tv_plan;
+
+/* Device scratch bytes needed by tv_attn_tree_verify / tv_decode_step for
+ * this layer shape, n_seq sequences of at most n_max nodes and contexts of at
+ * most max_len rows.  0 for the TV_F32 path. */
+size_t tv_attn_workspace_bytes(const tv_plan* plan, const tv_attn_layer* layer, int32_t n_seq,
+                               int32_t n_max, int32_t max_len);
+
+/* Verify every tree node of every sequence for one attention layer.
+ *  len       device [n_seq]: committed rows L_s (read only)
+ *  max_len   host bound, >= every L_s (sizes the launch; a larger L_s sets TV_ERR_LEN)
+ *  q         [n_total][Hq][D]; k_t, v_t [n_total][Hkv][D]: the nodes' own rows
+ *  out       [n_total][Hq][D]
+ *  scale     score scale (D^-1/2 for standard attention)
+ *  workspace device scratch of at least tv_attn_workspace_bytes() bytes
+ * The cache is read only; the tree rows enter it only through tv_commit_path,
+ * so rolling back a rejected tree costs nothing. */
+tv_status tv_attn_tree_verify(const tv_plan* plan, const tv_attn_layer* layer, const tv_tree* tree,
+                              const int32_t* len, int32_t max_len, const void* q, const void* k_t,
+                              const void* v_t, void* out, float scale, void* workspace,
+                              size_t workspace_bytes, tv_stream stream);
+
+/* ------------------------------------------------------------------------
+ * Gated DeltaNet: the gated delta rule along every node's ancestor path
+ * ------------------------------------------------------------------------
+ * [MODEL].  For value head h (key head g = h / (Hv/Hk)) and node i, with
+ * S_{par(root)} = S (the committed state):
+ *     S_i = alpha_i S_{par(i)} (I - beta_i k_i k_i^T) + beta_i v_i k_i^T
+ *     out[i,h] = scale * S_i q_i
+ * No per-node state is written to memory.
+ */
+typedef struct {
+  tv_dtype dtype;         /* element type of q, k, v and out (TV_BF16 or TV_F32) */
+  int32_t Hk, Hv, dk, dv; /* Hv % Hk == 0, dk in {64,128}, dv <= 256 */
+  float* const* S;        /* host array [n_seq] of device pointers, each fp32 [Hv][dv][dk] */
+} tv_gdn_layer;
+
+/*  q, k  [n_total][Hk][dk]; v [n_total][Hv][dv]; alpha, beta fp32 [n_total][Hv]
+ *  out   [n_total][Hv][dv]
+ *  scale output scale (dk^-1/2 by default).  The state is read only. */
+tv_status tv_gdn_tree_verify(const tv_gdn_layer* layer, const tv_tree* tree, const void* q,
+                             const void* k, const void* v, const float* alpha, const float* beta,
+                             void* out, float scale, tv_stream stream);
+
+/* ------------------------------------------------------------------------
+ * Accept walk: longest agreeing path plus one token
+ * ------------------------------------------------------------------------
+ * [TOUR].  A node agrees when every node on its root path below the root
+ * carries the token the target chose greedily at that node's parent.  The
+ * accepted path is the root path of the deepest agreeing node (lowest local
+ * index among equally deep ones); the bonus token is the target's greedy
+ * token at the path's last node (it becomes the next round's root).
+ *  tok, greedy device [n_total] int32: each node's draft token / the target's argmax after it
+ *  path        device [n_seq][TV_MAX_PATH] out: local node indices, root first, -1 padded
+ *  acc_len     device [n_seq] out: accepted path length a (1..TV_MAX_PATH, root included)
+ *  bonus       device [n_seq] out */
+tv_status tv_accept_path(const tv_tree* tree, const int32_t* tok, const int32_t* greedy,
+                         int32_t* path, int32_t* acc_len, int32_t* bonus, tv_stream stream);
+
+/* ------------------------------------------------------------------------
+ * Commit the accepted path into every layer's cache state
+ * ------------------------------------------------------------------------
+ * [TOUR], [MODEL] commit_tree, [STATE].  For every sequence s with
+ * a = acc_len[s] and L = len[s]:
+ *   attention layer l: rows L..L+a-1 of K_l[s], V_l[s] <- k_t[l], v_t[l] rows of
+ *     the path's nodes (bit copies);
+ *   GDN layer l: S_l[s] <- S_l[s] advanced along the path with the same step
+ *     function tv_gdn_tree_verify and tv_decode_step use;
+ *   then len[s] += a.
+ * k_t, v_t, k, v, alpha, beta are host arrays (one device pointer per layer)
+ * of the same buffers that layer's verify call read.  A sequence with
+ * L + a > cap sets TV_ERR_CAPACITY and commits nothing. */
+tv_status tv_commit_path(const tv_tree* tree, const int32_t* path, const int32_t* acc_len,
+                         int32_t n_attn, const tv_attn_layer* attn, const void* const* k_t,
+                         const void* const* v_t, int32_t n_gdn, const tv_gdn_layer* gdn,
+                         const void* const* k, const void* const* v, const float* const* alpha,
+                         const float* const* beta, int32_t* len, tv_stream stream);
+
+/* ------------------------------------------------------------------------
+ * Single-token decode (the row every verified row must equal)
+ * ------------------------------------------------------------------------
+ * [MODEL] step 4 and its load-time self-check.  One token per sequence for
+ * exactly one layer (attn XOR gdn non-NULL), run through the same tiles,
+ * splits and step function as verify:
+ *   attention: writes the token's k, v at row len[s] of the cache and attends
+ *     over rows 0..len[s]; q [n_seq][Hq][D], k, v [n_seq][Hkv][D];
+ *     workspace as for tv_attn_tree_verify with n_max = 1.
+ *   GDN: S <- step(S) in place and out = scale * S q; q, k [n_seq][Hk][dk],
+ *     v [n_seq][Hv][dv], alpha, beta [n_seq][Hv].
+ * len is not advanced here: after the last layer of a token call
+ * tv_len_advance.  status: device error word (as in tv_tree). */
+tv_status tv_decode_step(const tv_plan* plan, const tv_attn_layer* attn, const tv_gdn_layer* gdn,
+                         int32_t n_seq, const int32_t* len, int32_t max_len, const void* q,
+                         const void* k, const void* v, const float* alpha, const float* beta,
+                         void* out, float scale, void* workspace, size_t workspace_bytes,
+                         int32_t* status, tv_stream stream);
+
+/* len[s] += by[s] (device [n_seq]) if `by` is non-NULL, else len[s] += inc. */
+tv_status tv_len_advance(int32_t* len, const int32_t* by, int32_t inc, int32_t n_seq,
+                         tv_stream stream);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* TV_H */

@@ -104,16 +104,19 @@ def attn_tree_verify(K, V, L, q, k_t, v_t, parent, scale):
         ctx_v = V[g, :L]
         heads = list(range(g * G, (g + 1) * G))
         # scores against the context, every node and head of this group at once
-        s_ctx = np.einsum("nhd,pd->nhp", q[:, heads], ctx_k) * scale
+        s_ctx = (q[:, heads] @ ctx_k.T) * scale  # [N, G, L]
+        w_ctx = np.empty_like(s_ctx)
         for i in range(N):
             path = root_path(parent, i)
             tree_k = k_t[path, g]  # [d+1, D]
             tree_v = v_t[path, g]
-            for hi, h in enumerate(heads):
-                s = np.concatenate([s_ctx[i, hi], (tree_k @ q[i, h]) * scale])
-                w = np.exp(s - s.max())
-                w /= w.sum()
-                o[i, h] = w[:L] @ ctx_v + w[L:] @ tree_v
+            s = np.concatenate([s_ctx[i], (q[i, heads] @ tree_k.T) * scale], axis=1)  # [G, L+d+1]
+            w = np.exp(s - s.max(axis=1, keepdims=True))
+            w /= w.sum(axis=1, keepdims=True)
+            w_ctx[i] = w[:, :L]
+            o[i, heads] = w[:, L:] @ tree_v
+        # the context part of every weighted sum, as one matrix product
+        o[:, heads] += w_ctx @ ctx_v
     return o
 
 

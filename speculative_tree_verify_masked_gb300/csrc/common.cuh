@@ -1,0 +1,94 @@
+// Internal definitions shared by the library's translation units: the layout
+// of the derived tree tables, device status helpers and small numeric helpers.
+#pragma once
+#include <cstddef>
+#include <cstdint>
+#include <cuda_runtime.h>
+#include <cuda_bf16.h>
+
+#include "tv.h"
+
+namespace tv {
+
+// A bounded wait gives up after this many SM clocks (about a second).
+constexpr long long kWaitCycles = 1LL << 31;
+
+// ----------------------------------------------------------------------------
+// derived tree tables (written by tv_tree_prepare, read by the other calls)
+// ----------------------------------------------------------------------------
+struct SeqInfo {
+  int32_t n;          // nodes of this sequence's tree (0 = invalid tree)
+  int32_t off;        // first global node index
+  int32_t max_depth;  // deepest node
+  int32_t max_slot;   // saved-state slots the recurrent traversal needs
+};
+
+struct MetaView {
+  SeqInfo* seq;     // [TV_MAX_SEQ]
+  uint64_t* anc;    // [n_total] ancestor-or-self bitmask (sequence-local bits)
+  int32_t* depth;   // [n_total]
+  int32_t* sched;   // [n_total] recurrent traversal, per sequence at off..off+n-1
+  int8_t* anc_at;   // [n_total][TV_MAX_PATH] local index of the ancestor at each depth
+};
+
+__host__ __device__ inline size_t align16(size_t x) { return (x + 15) & ~static_cast<size_t>(15); }
+
+__host__ __device__ inline size_t meta_bytes(int n_total) {
+  const size_t n = static_cast<size_t>(n_total);
+  return align16(sizeof(SeqInfo) * TV_MAX_SEQ) + align16(8 * n) + 2 * align16(4 * n) +
+         align16(TV_MAX_PATH * n);
+}
+
+__host__ __device__ inline MetaView meta_view(void* base, int n_total) {
+  const size_t n = static_cast<size_t>(n_total);
+  char* p = static_cast<char*>(base);
+  MetaView m;
+  m.seq = reinterpret_cast<SeqInfo*>(p);
+  p += align16(sizeof(SeqInfo) * TV_MAX_SEQ);
+  m.anc = reinterpret_cast<uint64_t*>(p);
+  p += align16(8 * n);
+  m.depth = reinterpret_cast<int32_t*>(p);
+  p += align16(4 * n);
+  m.sched = reinterpret_cast<int32_t*>(p);
+  p += align16(4 * n);
+  m.anc_at = reinterpret_cast<int8_t*>(p);
+  return m;
+}
+
+// Recurrent traversal step: [0,8) local node, [8,16) source of the parent
+// state (0 = the state already in registers, 1+k = saved slot k),
+// [16,24) save after the step (0 = no, 1+k = slot k), bit 24 = node has children.
+constexpr int kMaxSlots = 5;  // a tree of <= 64 nodes never needs more (see tree.cu)
+__host__ __device__ inline int32_t sched_encode(int node, int src, int save, int has_children) {
+  return node | (src << 8) | (save << 16) | (has_children << 24);
+}
+
+// ----------------------------------------------------------------------------
+// device status word: the first error code wins; later calls become no-ops
+// ----------------------------------------------------------------------------
+__device__ __forceinline__ void set_status(int32_t* st, int code) {
+  if (st) atomicCAS(st, 0, code);
+}
+__device__ __forceinline__ bool status_bad(const int32_t* st) {
+  return st != nullptr && *reinterpret_cast<const volatile int32_t*>(st) != 0;
+}
+
+// ----------------------------------------------------------------------------
+// element conversion
+// ----------------------------------------------------------------------------
+__device__ __forceinline__ float to_f32(float x) { return x; }
+__device__ __forceinline__ float to_f32(__nv_bfloat16 x) { return __bfloat162float(x); }
+template <typename T>
+__device__ __forceinline__ T from_f32(float x);
+template <>
+__device__ __forceinline__ float from_f32<float>(float x) { return x; }
+template <>
+__device__ __forceinline__ __nv_bfloat16 from_f32<__nv_bfloat16>(float x) {
+  return __float2bfloat16_rn(x);
+}
+
+// bf16 halves of a packed word, exactly
+__device__ __forceinline__ float bf16_lo(uint32_t w) { return __uint_as_float(w << 16); }
+__device__ __forceinline__ float bf16_hi(uint32_t w) { return __uint_as_float(w & 0xFFFF0000u); }
+
+}  // namespace tv

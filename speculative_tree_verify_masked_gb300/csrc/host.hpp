@@ -1,0 +1,37 @@
+// Host-side helpers shared by the C-ABI entry points.
+#pragma once
+#include <cstdint>
+#include <cuda_runtime.h>
+
+#include "tv.h"
+
+namespace tv {
+
+inline bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+// Status of the launches just enqueued.  Clears a sticky-free launch error
+// so that the next call starts clean.
+inline tv_status launch_status() {
+  const cudaError_t e = cudaGetLastError();
+  return e == cudaSuccess ? TV_OK : TV_ERR_CUDA;
+}
+
+// Streaming multiprocessors of the current device.
+inline int num_sms() {
+  static int cached = 0;
+  if (cached > 0) return cached;
+  int dev = 0, n = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess) return 1;
+  if (cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess) return 1;
+  cached = n > 0 ? n : 1;
+  return cached;
+}
+
+inline bool tree_ok(const tv_tree* t) {
+  return t && t->n_seq >= 1 && t->n_seq <= TV_MAX_SEQ && t->n_max >= 1 && t->n_max <= TV_MAX_NODES &&
+         t->n_total >= t->n_seq && t->n_total <= t->n_seq * t->n_max && t->node_off && t->parent &&
+         t->meta && t->status && aligned16(t->node_off) && aligned16(t->parent) && aligned16(t->meta) &&
+         aligned16(t->status);
+}
+
+}  // namespace tv

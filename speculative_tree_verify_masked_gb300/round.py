@@ -1,0 +1,124 @@
+"""One speculative verify round over a mixer stack, driven through the C ABI.
+
+A round is: tv_tree_prepare, one tv_gdn_tree_verify / tv_attn_tree_verify per
+layer (in layer order), tv_accept_path, tv_commit_path.  This module owns the
+device buffers of a synthetic workload (caches, states, per-layer node
+inputs and outputs, tree tables, workspace) and issues those calls on one
+stream; it can also capture the round in a CUDA graph.
+"""
+from __future__ import annotations
+
+import math
+
+import torch
+
+from . import binding as B
+from . import synth
+
+DEFAULT_SPLIT = 4096  # positions per KV split (multiple of 64)
+
+
+class VerifyRound:
+    def __init__(self, cfg: synth.Workload, device="cuda", split: int = DEFAULT_SPLIT, layers=None,
+                 cap_extra: int = 64, seed_layers=None):
+        self.cfg = cfg
+        self.device = device
+        s = cfg.shapes
+        self.layers = list(range(cfg.n_layers)) if layers is None else list(layers)
+        self.trees = [synth.tree_and_tokens(cfg, q) for q in range(cfg.n_seq)]
+        self.parents = [t[0] for t in self.trees]
+        self.n_nodes = [len(p) for p in self.parents]
+        self.tree = B.Tree(self.parents, device=device)
+        self.tok = torch.tensor([x for t in self.trees for x in t[1]], dtype=torch.int32, device=device)
+        self.greedy = torch.tensor([x for t in self.trees for x in t[2]], dtype=torch.int32, device=device)
+        self.expected_paths = [t[3] for t in self.trees]
+        self.len0 = torch.tensor(cfg.ctx_lens, dtype=torch.int32, device=device)
+        self.len = self.len0.clone()
+        self.max_len = max(cfg.ctx_lens)
+        self.cap = self.max_len + cap_extra
+        self.plan = B.plan(split)
+        self.attn_scale = 1.0 / math.sqrt(s.D)
+        self.gdn_scale = 1.0 / math.sqrt(s.dk)
+        self.attn, self.gdn = {}, {}
+        for li in self.layers:
+            if cfg.is_attn(li):
+                per = [synth.attn_layer_inputs(cfg, li, q, self.n_nodes[q], self.cap, device) for q in range(cfg.n_seq)]
+                layer = B.AttnLayer([x["K"] for x in per], [x["V"] for x in per], s.Hq)
+                q_ = torch.cat([x["q"] for x in per]).contiguous()
+                k_t = torch.cat([x["k_t"] for x in per]).contiguous()
+                v_t = torch.cat([x["v_t"] for x in per]).contiguous()
+                out = torch.empty_like(q_)
+                self.attn[li] = dict(layer=layer, q=q_, k_t=k_t, v_t=v_t, out=out)
+            else:
+                per = [synth.gdn_layer_inputs(cfg, li, q, self.n_nodes[q], device) for q in range(cfg.n_seq)]
+                layer = B.GdnLayer([x["S0"] for x in per], s.Hk, s.kv_dtype)
+                d = {k: torch.cat([x[k] for x in per]).contiguous() for k in ("q", "k", "v", "alpha", "beta")}
+                d["out"] = torch.empty((d["v"].shape[0], s.Hv, s.dv), dtype=s.kv_dtype, device=device)
+                d["layer"] = layer
+                self.gdn[li] = d
+        ws_bytes = 0
+        if self.attn:
+            first = next(iter(self.attn.values()))["layer"]
+            ws_bytes = B.tv_attn_workspace_bytes(self.plan, first, cfg.n_seq, self.tree.n_max, self.max_len)
+        self.ws = torch.empty(max(16, ws_bytes) // 4 + 4, dtype=torch.float32, device=device) if ws_bytes else None
+        self.path = torch.full((cfg.n_seq, B.TV_MAX_PATH), -1, dtype=torch.int32, device=device)
+        self.acc_len = torch.zeros(cfg.n_seq, dtype=torch.int32, device=device)
+        self.bonus = torch.zeros(cfg.n_seq, dtype=torch.int32, device=device)
+        al = [li for li in self.layers if li in self.attn]
+        gl = [li for li in self.layers if li in self.gdn]
+        self.commit_args = B.CommitArgs(
+            [self.attn[li]["layer"] for li in al], [self.attn[li]["k_t"] for li in al],
+            [self.attn[li]["v_t"] for li in al], [self.gdn[li]["layer"] for li in gl],
+            [self.gdn[li]["k"] for li in gl], [self.gdn[li]["v"] for li in gl],
+            [self.gdn[li]["alpha"] for li in gl], [self.gdn[li]["beta"] for li in gl])
+
+    # -- steps of the round -------------------------------------------------
+    def prepare(self, stream=None):
+        B.tv_tree_prepare(self.tree, stream)
+
+    def verify_layer(self, li, stream=None):
+        if li in self.attn:
+            a = self.attn[li]
+            B.tv_attn_tree_verify(self.plan, a["layer"], self.tree, self.len, self.max_len, a["q"], a["k_t"],
+                                  a["v_t"], a["out"], self.attn_scale, self.ws, stream)
+        else:
+            g = self.gdn[li]
+            B.tv_gdn_tree_verify(g["layer"], self.tree, g["q"], g["k"], g["v"], g["alpha"], g["beta"], g["out"],
+                                 self.gdn_scale, stream)
+
+    def verify(self, stream=None):
+        self.prepare(stream)
+        for li in self.layers:
+            self.verify_layer(li, stream)
+
+    def accept(self, stream=None):
+        B.tv_accept_path(self.tree, self.tok, self.greedy, self.path, self.acc_len, self.bonus, stream)
+
+    def commit(self, stream=None):
+        B.tv_commit_path(self.tree, self.path, self.acc_len, self.commit_args, self.len, stream)
+
+    def run(self, stream=None, reset_len: bool = True):
+        """One round.  With reset_len the context length is first restored so
+        repeated rounds do the same work (the caches' rows past it and the
+        states are overwritten by each commit)."""
+        if reset_len:
+            self.len.copy_(self.len0)
+        self.verify(stream)
+        self.accept(stream)
+        self.commit(stream)
+
+    def status(self) -> int:
+        return self.tree.status_code()
+
+    def capture(self):
+        """Capture run() in a CUDA graph on a side stream; returns the graph."""
+        g = torch.cuda.CUDAGraph()
+        s = torch.cuda.Stream()
+        s.wait_stream(torch.cuda.current_stream())
+        with torch.cuda.stream(s):
+            self.run()  # warm (attribute setup outside capture)
+        torch.cuda.current_stream().wait_stream(s)
+        torch.cuda.synchronize()
+        with torch.cuda.graph(g):
+            self.run()
+        return g
