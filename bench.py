@@ -371,7 +371,7 @@ def run_ours(args, rank, world, local_rank):
                    "ctx_lens": cfg.ctx_lens, "tree_nodes": n_nodes, "accepted": acc_lens,
                    "Hq_Hkv_D": [cfg.shapes.Hq, cfg.shapes.Hkv, cfg.shapes.D],
                    "Hk_Hv_dk_dv": [cfg.shapes.Hk, cfg.shapes.Hv, cfg.shapes.dk, cfg.shapes.dv],
-                   "split": args.split, "timing": "CUDA-graph replay of whole rounds, CUDA events",
+                   "split": r.split, "timing": "CUDA-graph replay of whole rounds, CUDA events",
                    "l2": "no flush: every round streams inputs far larger than L2 (KV context per round)",
                    "parallelism": f"replicas x{world}"},
         "us_per_round": round(ms * 1e3, 2),
@@ -435,7 +435,8 @@ def main():
     ap.add_argument("--steps", type=int, default=600)
     ap.add_argument("--warmup", type=int, default=20)
     ap.add_argument("--config", type=int, default=3, choices=[0, 1, 2, 3, 4])
-    ap.add_argument("--split", type=int, default=4096, help="positions per KV split (multiple of 64)")
+    ap.add_argument("--split", type=int, default=None,
+                    help="positions per KV split (multiple of 64); default: the plan chosen for the workload")
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--traffic", type=float, default=None, help="ncu DRAM bytes per attention launch, if measured")
     ap.add_argument("--no-e2e", action="store_true")

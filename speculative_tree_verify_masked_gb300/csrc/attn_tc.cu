@@ -6,13 +6,14 @@
 // L cache rows, then its ancestors-or-self at L .. L+d.  Positions are cut
 // into tiles of 64 and splits of plan.split positions, both aligned at
 // absolute position 0.  Within a split the tiles run in order through one
-// online softmax: S = Q K^T on the tensor core (fp32), the scaled tile max,
-// p = 2^(s*c - m) rounded to bf16, l += sum of the rounded p, O = O*alpha +
-// P V on the tensor core.  Splits are merged in split order.  The running
-// state (m, l, O) is carried between kernels as exact fp32, and every tile
-// update runs the same code, so the result depends only on the row's query
-// and key sequence: a node verified in a tree and the same token decoded
-// after its ancestors were committed produce the same bits.
+// online softmax: S = Q K^T on the tensor core (fp32); the tile's 64 slots are
+// handled as two halves of 32 that share the scaled tile max; p = 2^(s*c - m)
+// rounded to bf16; each half keeps its own running sum of the rounded p;
+// O = O * alpha + P V on the tensor core.  Splits are merged in split order.
+// The running state (m, l_A, l_B, O) is carried between kernels as exact
+// fp32 and every tile update runs the same code, so the result depends only
+// on the row's query and key sequence: a node verified in a tree and the same
+// token decoded after its ancestors were committed produce the same bits.
 //
 // Kernels.
 //  split kernel (persistent, one CTA per SM): the tiles that every node of a
@@ -20,17 +21,19 @@
 //    128 query rows (node x head of one KV head) at once.  Warp 0 streams K/V
 //    tiles with TMA (128B-swizzled boxes) through a ring of stages; warp 1
 //    issues the tcgen05 MMAs (Q and P live in TMEM, K and V in shared memory,
-//    S and O accumulate in TMEM); warps 2-5 run the softmax, one TMEM lane
-//    (query row) per thread.  S is double-buffered so QK^T of tile t+1 runs on
-//    the tensor core while the softmax of tile t runs.  Each split's (m, l, O)
-//    goes to the workspace.
+//    S and O accumulate in TMEM); warps 2-5 and 6-9 run the softmax, one TMEM
+//    lane (query row) and one half tile per thread.  S is double-buffered so
+//    QK^T of tile t+1 runs on the tensor core while the softmax of tile t runs.
+//    Each split's state goes to the workspace.
 //  tail kernel (one CTA per node and KV head): the node's own tiles (cache
 //    rows past the last shared tile plus its ancestors at their logical
-//    slots, built in shared memory), continuing the split state left by the
-//    split kernel, then the in-order merge of all splits and the bf16 output.
+//    slots, gathered into shared memory with cp.async), continuing the split
+//    state the split kernel left, then the in-order merge of all splits and
+//    the bf16 output.
 //  Decode runs the same two kernels with a one-node tree per sequence and
 //  appends its own K/V row.
 #include <cmath>
+#include <cstring>
 #include <cudaTypedefs.h>
 
 #include "common.cuh"
@@ -40,24 +43,30 @@
 
 namespace tv {
 
-constexpr int kTile = 64;         // KV positions per tile
-constexpr int kBox = 64 * 128;    // one [64 rows x 128 B] 128B-swizzled box
+constexpr int kTile = 64;       // KV positions per tile
+constexpr int kHalf = 32;       // positions per softmax half
+constexpr int kBox = 64 * 128;  // one [64 rows x 128 B] 128B-swizzled box
+constexpr int kMaxGroup = 64;   // query heads per KV head on this path
 
 template <int D>
 struct Tc {
-  static constexpr int KB = D / 64;                 // 64-column boxes per row
-  static constexpr int TILE = kTile * D * 2;        // bytes of one K or V tile
-  static constexpr int NS = (D == 256) ? 3 : 6;     // pipeline stages
-  static constexpr int STAGE = 2 * TILE;
-  static constexpr int T_O = 0;                     // TMEM columns: O [D]
-  static constexpr int T_S = D;                     //   S/P [2 x 64]
-  static constexpr int T_Q = D + 2 * kTile;         //   Q [D/2] (bf16 pairs)
+  static constexpr int KB = D / 64;           // 64-column boxes per row
+  static constexpr int TILE = kTile * D * 2;  // bytes of one K or V tile
+  // K and V tiles stream through separate rings: a K slot frees as soon as
+  // QK^T of its tile completes, a V slot after PV, so K loads run further ahead.
+  static constexpr int NK = (D == 256) ? 4 : 6;
+  static constexpr int NV = (D == 256) ? 2 : 6;
+  static constexpr int T_O = 0;              // TMEM columns: O [D]
+  static constexpr int T_S = D;              //   S/P [2 x 64]
+  static constexpr int T_Q = D + 2 * kTile;  //   Q [D/2] (bf16 pairs)
   static constexpr int COLS = (D + 2 * kTile + D / 2) <= 256 ? 256 : 512;
   static constexpr uint32_t IDESC_QK = idesc_bf16_f32(128, kTile, false, false);
   static constexpr uint32_t IDESC_PV = idesc_bf16_f32(128, D, false, true);
-  static constexpr int NBAR = 2 * NS + 7;
-  static constexpr int SMEM_SPLIT = 1024 + NS * STAGE + NBAR * 8 + 16;
+  static constexpr int RING = (NK + NV) * TILE;
+  static constexpr int NBAR = 2 * (NK + NV) + 10;
+  static constexpr int SMEM_SPLIT = 1024 + RING + NBAR * 8 + 16;
   static constexpr int SMEM_TAIL = 1024 + 2 * TILE + 16 + 16;
+  static constexpr int REC = D + 4;  // workspace record: O[D], m, l_A, l_B, pad
 };
 
 struct TcParams {
@@ -103,90 +112,91 @@ __device__ __forceinline__ void issue_pv(uint32_t tO, uint32_t tP, uint32_t vtil
     tc_mma_ts(tO, tP + kk * 8, desc_v(vtile, kk), Tc<D>::IDESC_PV, (acc || kk > 0) ? 1u : 0u);
 }
 
-// Online-softmax update for one tile of one row.  s: raw scores of the tile's
-// 64 slots, slots >= nvalid masked.  m is the running max in the exp2 domain
-// (scaled by c), l the running sum of the bf16-rounded probabilities.
-// Writes the tile's probabilities as packed bf16 pairs and the factor alpha
-// that the running O must be multiplied by (exactly 1 when m is unchanged).
-__device__ __forceinline__ void softmax_tile(const float (&s)[kTile], int nvalid, float c, float& m, float& l,
-                                             uint32_t (&P)[kTile / 2], float& alpha) {
-  float mx = -INFINITY;
+// Max of the valid slots of one half tile (exact; any order gives the same).
+__device__ __forceinline__ float half_max(const float (&s)[kHalf], int nvalid) {
+  float v[kHalf];
 #pragma unroll
-  for (int j = 0; j < kTile; j++) mx = fmaxf(mx, j < nvalid ? s[j] : -INFINITY);
-  const float m_new = fmaxf(m, __fmul_rn(mx, c));
-  alpha = (m_new == m) ? 1.f : ex2_approx(__fsub_rn(m, m_new));
+  for (int j = 0; j < kHalf; j++) v[j] = j < nvalid ? s[j] : -INFINITY;
+#pragma unroll
+  for (int w = kHalf / 2; w >= 1; w >>= 1)
+#pragma unroll
+    for (int j = 0; j < w; j++) v[j] = fmaxf(v[j], v[j + w]);
+  return v[0];
+}
+
+// Probabilities of one half tile as packed bf16 pairs and the sum of the
+// rounded values (fixed order).  m_new: the running max in the exp2 domain.
+__device__ __forceinline__ float half_probs(const float (&s)[kHalf], int nvalid, float c, float m_new,
+                                            uint32_t (&P)[kHalf / 2]) {
   const float neg = -m_new;
   float acc[4] = {0.f, 0.f, 0.f, 0.f};
 #pragma unroll
-  for (int j = 0; j < kTile; j += 2) {
+  for (int j = 0; j < kHalf; j += 2) {
     const float p0 = j < nvalid ? ex2_approx(__fmaf_rn(s[j], c, neg)) : 0.f;
     const float p1 = j + 1 < nvalid ? ex2_approx(__fmaf_rn(s[j + 1], c, neg)) : 0.f;
     const uint32_t w = pack_bf16x2(p0, p1);
     P[j / 2] = w;
     acc[(j / 2) & 3] = __fadd_rn(acc[(j / 2) & 3], __fadd_rn(bf16_lo(w), bf16_hi(w)));
   }
-  const float rs = __fadd_rn(__fadd_rn(acc[0], acc[1]), __fadd_rn(acc[2], acc[3]));
-  l = __fmaf_rn(l, alpha, rs);
-  m = m_new;
+  return __fadd_rn(__fadd_rn(acc[0], acc[1]), __fadd_rn(acc[2], acc[3]));
 }
 
-__device__ __forceinline__ void tmem_ld64f(uint32_t taddr, float (&s)[kTile]) {
-  uint32_t r0[32], r1[32];
-  tmem_ld32(taddr, r0);
-  tmem_ld32(taddr + 32, r1);
-#pragma unroll
-  for (int i = 0; i < 32; i++) {
-    s[i] = __uint_as_float(r0[i]);
-    s[32 + i] = __uint_as_float(r1[i]);
+// Reference max for the exponentials.  It moves only when the tile's scaled
+// max exceeds it by more than kRescale (in log2 units), so most tiles keep it
+// and skip rescaling O; probabilities then stay below 2^kRescale, well inside
+// bf16 and fp32 range.  alpha is the factor for the running O and sums:
+// exactly 1 when the reference is kept, 0 on the first tile.
+constexpr float kRescale = 8.f;
+__device__ __forceinline__ float next_max(float m, float mx_raw, float c, float& alpha) {
+  const float mt = __fmul_rn(mx_raw, c);
+  if (mt > __fadd_rn(m, kRescale) || m == -INFINITY) {
+    alpha = ex2_approx(__fsub_rn(m, mt));
+    return mt;
   }
+  alpha = 1.f;
+  return m;
 }
 
-template <int D>
-__device__ __forceinline__ void rescale_o(uint32_t tO, float alpha) {
+__device__ __forceinline__ void tmem_ld32f(uint32_t taddr, float (&s)[kHalf]) {
+  uint32_t r[32];
+  tmem_ld32(taddr, r);
+#pragma unroll
+  for (int i = 0; i < 32; i++) s[i] = __uint_as_float(r[i]);
+}
+
+__device__ __forceinline__ void tmem_st16(uint32_t taddr, const uint32_t (&r)[16]) {
+  asm volatile(
+      "tcgen05.st.sync.aligned.32x32b.x16.b32 [%0], "
+      "{%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,%16};" ::"r"(taddr),
+      "r"(r[0]), "r"(r[1]), "r"(r[2]), "r"(r[3]), "r"(r[4]), "r"(r[5]), "r"(r[6]), "r"(r[7]), "r"(r[8]),
+      "r"(r[9]), "r"(r[10]), "r"(r[11]), "r"(r[12]), "r"(r[13]), "r"(r[14]), "r"(r[15])
+      : "memory");
+}
+
+// O columns [c0, c1) of this thread's lane times alpha.
+__device__ __forceinline__ void rescale_o(uint32_t tO, int c0, int c1, float alpha) {
 #pragma unroll 1
-  for (int c0 = 0; c0 < D; c0 += 32) {
+  for (int c = c0; c < c1; c += 32) {
     uint32_t r[32];
-    tmem_ld32(tO + c0, r);
+    tmem_ld32(tO + c, r);
 #pragma unroll
     for (int i = 0; i < 32; i++) r[i] = __float_as_uint(__fmul_rn(__uint_as_float(r[i]), alpha));
-    tmem_st32(tO + c0, r);
+    tmem_st32(tO + c, r);
   }
 }
 
-// Q row (D bf16) into this thread's TMEM lane, zeros when q == nullptr.
-template <int D>
-__device__ __forceinline__ void load_q_tmem(uint32_t tQ, const __nv_bfloat16* q) {
-#pragma unroll 1
-  for (int c0 = 0; c0 < D / 2; c0 += 32) {
-    uint32_t r[32];
-    if (q) {
-      const uint4* s4 = reinterpret_cast<const uint4*>(q) + c0 / 4;
-#pragma unroll
-      for (int i = 0; i < 8; i++) {
-        const uint4 v = s4[i];
-        r[4 * i] = v.x;
-        r[4 * i + 1] = v.y;
-        r[4 * i + 2] = v.z;
-        r[4 * i + 3] = v.w;
-      }
-    } else {
-#pragma unroll
-      for (int i = 0; i < 32; i++) r[i] = 0u;
-    }
-    tmem_st32(tQ + c0, r);
-  }
-}
-
-// Workspace record of (split, row): O[D], m, l, 2 pad floats.
+// Workspace record of (sequence, KV head, split, row).
 __device__ __forceinline__ float* ws_rec(const TcParams& p, int s, int g, int split, int row, int D) {
   return p.ws + ((((static_cast<size_t>(s) * p.Hkv + g) * p.max_splits + split) * p.rows_max + row) *
                  static_cast<size_t>(D + 4));
 }
 
+// This half's O columns (TMEM) to the record; half 0 also writes m and l_A,
+// half 1 writes l_B.
 template <int D>
-__device__ __forceinline__ void store_state(uint32_t tO, float* rec, float m, float l) {
+__device__ __forceinline__ void store_state(uint32_t tO, float* rec, int hf, float m, float lh) {
 #pragma unroll 1
-  for (int c0 = 0; c0 < D; c0 += 32) {
+  for (int c0 = hf * (D / 2); c0 < (hf + 1) * (D / 2); c0 += 32) {
     uint32_t r[32];
     tmem_ld32(tO + c0, r);
     if (rec) {
@@ -198,8 +208,12 @@ __device__ __forceinline__ void store_state(uint32_t tO, float* rec, float m, fl
     }
   }
   if (rec) {
-    rec[D] = m;
-    rec[D + 1] = l;
+    if (hf == 0) {
+      rec[D] = m;
+      rec[D + 1] = lh;
+    } else {
+      rec[D + 2] = lh;
+    }
   }
 }
 
@@ -263,34 +277,53 @@ __device__ __forceinline__ bool wait_role(uint32_t bar, uint32_t parity, volatil
 }
 
 template <int D>
-__global__ void __launch_bounds__(192, 1) attn_split_kernel(const __grid_constant__ TcParams p) {
+__global__ void __launch_bounds__(352, 1) attn_split_kernel(const __grid_constant__ TcParams p) {
   using C = Tc<D>;
   extern __shared__ uint8_t smem_raw[];
   __shared__ ItemSpace is;
   __shared__ int skip;
+  __shared__ float xmax[2][2][128];  // [tile parity][half][row]: half-tile maxima
   const uint32_t raw = smem_u32(smem_raw);
   const uint32_t sb = (raw + 1023u) & ~1023u;
   uint8_t* gb = smem_raw + (sb - raw);
-  const uint32_t bars = sb + C::NS * C::STAGE;
-  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(gb + C::NS * C::STAGE + C::NBAR * 8);
+  const uint32_t bars = sb + C::RING;
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(gb + C::RING + C::NBAR * 8);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
-  const uint32_t SFULL0 = bars + 8u * (2 * C::NS), PFULL0 = bars + 8u * (2 * C::NS + 2);
-  const uint32_t ODONE = bars + 8u * (2 * C::NS + 4), QREADY = bars + 8u * (2 * C::NS + 5);
-  const uint32_t DRAIN = bars + 8u * (2 * C::NS + 6);
+  // ring barriers: KFULL[NK], KEMPTY[NK], VFULL[NV], VEMPTY[NV]
+  const uint32_t KFULL0 = bars, KEMPTY0 = bars + 8u * C::NK;
+  const uint32_t VFULL0 = bars + 16u * C::NK, VEMPTY0 = VFULL0 + 8u * C::NV;
+  const int nb = 2 * (C::NK + C::NV);
+  const uint32_t SFULL0 = bars + 8u * nb, PFULL0 = bars + 8u * (nb + 2);
+  // PV completion, one barrier per tile parity: the softmax of tile t waits for
+  // PV(t-1) only when it must rescale O.  When it waits, PV(t-2) is already
+  // complete (QK(t) was issued after it), so the barrier is at most one phase
+  // behind and its parity identifies the phase.
+  const uint32_t ODONE0 = bars + 8u * (nb + 4);
+  const uint32_t QREADY = bars + 8u * (nb + 6);
+  const uint32_t DRAIN = bars + 8u * (nb + 7);
+  const uint32_t XBAR0 = bars + 8u * (nb + 8);  // [2] half-max exchange, by tile parity
+  const uint32_t kring = sb, vring = sb + C::NK * C::TILE;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
 
   if (threadIdx.x == 0) {
-    for (int i = 0; i < C::NS; i++) {
-      mbar_init(bars + 8u * i, 1);
-      mbar_init(bars + 8u * (C::NS + i), 1);
+    for (int i = 0; i < C::NK; i++) {
+      mbar_init(KFULL0 + 8u * i, 1);
+      mbar_init(KEMPTY0 + 8u * i, 1);
+    }
+    for (int i = 0; i < C::NV; i++) {
+      mbar_init(VFULL0 + 8u * i, 1);
+      mbar_init(VEMPTY0 + 8u * i, 1);
     }
     for (int b = 0; b < 2; b++) {
       mbar_init(SFULL0 + 8u * b, 1);
-      mbar_init(PFULL0 + 8u * b, 128);
+      mbar_init(PFULL0 + 8u * b, 256);
     }
-    mbar_init(ODONE, 1);
-    mbar_init(QREADY, 128);
+    mbar_init(ODONE0, 1);
+    mbar_init(ODONE0 + 8u, 1);
+    mbar_init(QREADY, 256);
     mbar_init(DRAIN, 1);
+    mbar_init(XBAR0, 256);
+    mbar_init(XBAR0 + 8u, 256);
     *abort_flag = 0;
     fence_mbar_init();
     skip = status_bad(p.status) ? 1 : 0;
@@ -306,39 +339,41 @@ __global__ void __launch_bounds__(192, 1) attn_split_kernel(const __grid_constan
   const uint32_t tbase = *tmem_slot;
   const int total = is.cum[p.n_seq];
 
-  if (!skip && warp == 0 && lane == 0) {
-    // ---------------- TMA producer ----------------
+  if (!skip && (warp == 0 || warp == 10) && lane == 0) {
+    // ---------------- TMA producers: warp 0 streams K tiles, warp 10 V tiles ----------------
+    const bool is_k = warp == 0;
+    const int nslot = is_k ? C::NK : C::NV;
+    const uint32_t full0 = is_k ? KFULL0 : VFULL0, empty0 = is_k ? KEMPTY0 : VEMPTY0;
+    const uint32_t ring = is_k ? kring : vring;
+    const CUtensorMap* maps = is_k ? p.tmK : p.tmV;
     uint32_t it = 0;
     bool ok = true;
     for (int w = blockIdx.x; w < total && ok; w += gridDim.x) {
       const Item I = item_at(is, p, w);
       for (int t = I.t0; t < I.t1; t++) {
-        const int st = it % C::NS;
-        if (!wait_role(bars + 8u * (C::NS + st), ((it / C::NS) & 1) ^ 1, abort_flag)) {
+        const int st = it % nslot;
+        if (!wait_role(empty0 + 8u * st, ((it / nslot) & 1) ^ 1, abort_flag)) {
           ok = false;
           break;
         }
-        const uint32_t full = bars + 8u * st;
-        mbar_arrive_expect_tx(full, C::STAGE);
-        const uint32_t kd = sb + st * C::STAGE, vd = kd + C::TILE;
+        const uint32_t full = full0 + 8u * st;
+        mbar_arrive_expect_tx(full, C::TILE);
+        const uint32_t dst = ring + st * C::TILE;
         const int y = I.g * p.cap + t * kTile;
 #pragma unroll
-        for (int kb = 0; kb < C::KB; kb++) {
-          tma_load_2d(kd + kb * kBox, &p.tmK[I.s], full, kb * 64, y);
-          tma_load_2d(vd + kb * kBox, &p.tmV[I.s], full, kb * 64, y);
-        }
+        for (int kb = 0; kb < C::KB; kb++) tma_load_2d(dst + kb * kBox, &maps[I.s], full, kb * 64, y);
         it++;
       }
     }
     if (!ok) {
       set_status(p.status, TV_ERR_TIMEOUT);
       // let every issued copy land before the CTA's shared memory is released
-      for (uint32_t i = it > (uint32_t)C::NS ? it - C::NS : 0; i < it; i++)
-        mbar_wait(bars + 8u * (i % C::NS), (i / C::NS) & 1, kWaitCycles);
+      for (uint32_t i = it > (uint32_t)nslot ? it - nslot : 0; i < it; i++)
+        mbar_wait(full0 + 8u * (i % nslot), (i / nslot) & 1, kWaitCycles);
     }
   } else if (!skip && warp == 1 && lane == 0) {
     // ---------------- MMA issuer ----------------
-    uint32_t it = 0, sbuf = 0, q_ph = 0, pf_ph[2] = {0u, 0u};
+    uint32_t it = 0, sbuf = 0, q_ph = 0, pf_ph0 = 0, pf_ph1 = 0;
     bool ok = true;
     for (int w = blockIdx.x; w < total && ok; w += gridDim.x) {
       const Item I = item_at(is, p, w);
@@ -350,92 +385,128 @@ __global__ void __launch_bounds__(192, 1) attn_split_kernel(const __grid_constan
       q_ph ^= 1;
       tc_fence_after();
       for (int k = 0; k < n; k++) {
-        const int st = it % C::NS;
-        if (!wait_role(bars + 8u * st, (it / C::NS) & 1, abort_flag)) {
+        const int ks = it % C::NK;
+        if (!wait_role(KFULL0 + 8u * ks, (it / C::NK) & 1, abort_flag)) {
           ok = false;
           break;
         }
         tc_fence_after();
         const int b = sbuf & 1;
-        issue_qk<D>(tbase + C::T_S + b * kTile, tbase + C::T_Q, sb + st * C::STAGE);
+        issue_qk<D>(tbase + C::T_S + b * kTile, tbase + C::T_Q, kring + ks * C::TILE);
         tc_commit(SFULL0 + 8u * b);
+        tc_commit(KEMPTY0 + 8u * ks);
         if (k > 0) {
           const int pb = b ^ 1;
-          if (!wait_role(PFULL0 + 8u * pb, pf_ph[pb], abort_flag)) {
+          const uint32_t pt = it - 1;
+          const int vs = pt % C::NV;
+          if (!wait_role(PFULL0 + 8u * pb, pb ? pf_ph1 : pf_ph0, abort_flag) ||
+              !wait_role(VFULL0 + 8u * vs, (pt / C::NV) & 1, abort_flag)) {
             ok = false;
             break;
           }
-          pf_ph[pb] ^= 1;
+          if (pb) pf_ph1 ^= 1; else pf_ph0 ^= 1;
           tc_fence_after();
-          const int pst = (it - 1) % C::NS;
-          issue_pv<D>(tbase + C::T_O, tbase + C::T_S + pb * kTile, sb + pst * C::STAGE + C::TILE, k - 1 > 0);
-          tc_commit(bars + 8u * (C::NS + pst));
-          tc_commit(ODONE);
+          issue_pv<D>(tbase + C::T_O, tbase + C::T_S + pb * kTile, vring + vs * C::TILE, k - 1 > 0);
+          tc_commit(VEMPTY0 + 8u * vs);
+          tc_commit(ODONE0 + 8u * (pt & 1));
         }
         it++;
         sbuf++;
       }
       if (!ok) break;
       const int pb = (sbuf - 1) & 1;
-      if (!wait_role(PFULL0 + 8u * pb, pf_ph[pb], abort_flag)) {
+      const uint32_t pt = it - 1;
+      const int vs = pt % C::NV;
+      if (!wait_role(PFULL0 + 8u * pb, pb ? pf_ph1 : pf_ph0, abort_flag) ||
+          !wait_role(VFULL0 + 8u * vs, (pt / C::NV) & 1, abort_flag)) {
         ok = false;
         break;
       }
-      pf_ph[pb] ^= 1;
+      if (pb) pf_ph1 ^= 1; else pf_ph0 ^= 1;
       tc_fence_after();
-      const int pst = (it - 1) % C::NS;
-      issue_pv<D>(tbase + C::T_O, tbase + C::T_S + pb * kTile, sb + pst * C::STAGE + C::TILE, n - 1 > 0);
-      tc_commit(bars + 8u * (C::NS + pst));
-      tc_commit(ODONE);
+      issue_pv<D>(tbase + C::T_O, tbase + C::T_S + pb * kTile, vring + vs * C::TILE, n - 1 > 0);
+      tc_commit(VEMPTY0 + 8u * vs);
+      tc_commit(ODONE0 + 8u * (pt & 1));
     }
     // every MMA issued by this thread completes before TMEM is released
     tc_commit(DRAIN);
     mbar_wait(DRAIN, 0, kWaitCycles);
     if (!ok) set_status(p.status, TV_ERR_TIMEOUT);
-  } else if (!skip && warp >= 2) {
-    // ---------------- softmax / epilogue warpgroup ----------------
+  } else if (!skip && warp >= 2 && warp <= 9) {
+    // ---------------- softmax / epilogue: warps 2-9, two warpgroups, one half tile each ----------------
+    const int hf = (warp - 2) >> 2;  // 0: slots 0-31, 1: slots 32-63
     const int quad = warp & 3;
     const int lrow = quad * 32 + lane;
     const uint32_t tl = tbase + (static_cast<uint32_t>(quad * 32) << 16);
-    uint32_t sbuf = 0, sf_ph[2] = {0u, 0u}, od_ph = 0;
+    uint32_t sbuf = 0, sf_ph0 = 0, sf_ph1 = 0, x_ph0 = 0, x_ph1 = 0;
     bool ok = true;
     for (int w = blockIdx.x; w < total && ok; w += gridDim.x) {
       const Item I = item_at(is, p, w);
       const int n = I.t1 - I.t0;
       const int row = I.rb * 128 + lrow;
       const bool valid = row < is.rows[I.s];
-      const __nv_bfloat16* qrow = nullptr;
-      if (valid) {
-        const int node = row / p.G, jh = row % p.G;
-        qrow = p.q + (static_cast<size_t>(is.off[I.s] + node) * p.Hq + I.g * p.G + jh) * D;
+      // this half's Q columns (bf16 pairs) into TMEM
+      {
+        const uint4* q4 = nullptr;
+        if (valid) {
+          const int node = row / p.G, jh = row % p.G;
+          q4 = reinterpret_cast<const uint4*>(p.q + (static_cast<size_t>(is.off[I.s] + node) * p.Hq + I.g * p.G + jh) * D);
+        }
+#pragma unroll 1
+        for (int c0 = hf * (D / 4); c0 < (hf + 1) * (D / 4); c0 += 32) {
+          uint32_t r[32];
+#pragma unroll
+          for (int i = 0; i < 8; i++) {
+            const uint4 v = q4 ? q4[c0 / 4 + i] : make_uint4(0u, 0u, 0u, 0u);
+            r[4 * i] = v.x;
+            r[4 * i + 1] = v.y;
+            r[4 * i + 2] = v.z;
+            r[4 * i + 3] = v.w;
+          }
+          tmem_st32(tl + C::T_Q + c0, r);
+        }
       }
-      load_q_tmem<D>(tl + C::T_Q, qrow);
       tmem_st_wait();
       tc_fence_before();
       mbar_arrive(QREADY);
-      float m = -INFINITY, l = 0.f;
+      float m = -INFINITY, lh = 0.f;
       for (int k = 0; k < n; k++) {
         const int b = sbuf & 1;
-        if (!wait_role(SFULL0 + 8u * b, sf_ph[b], abort_flag)) {
+        if (!wait_role(SFULL0 + 8u * b, b ? sf_ph1 : sf_ph0, abort_flag)) {
           ok = false;
           break;
         }
-        sf_ph[b] ^= 1;
+        if (b) sf_ph1 ^= 1; else sf_ph0 ^= 1;
         tc_fence_after();
-        float sv[kTile];
-        tmem_ld64f(tl + C::T_S + b * kTile, sv);
-        uint32_t P[kTile / 2];
+        float sv[kHalf];
+        tmem_ld32f(tl + C::T_S + b * kTile + hf * kHalf, sv);
+        const float mh = half_max(sv, kHalf);
+        const int xb = sbuf & 1;
+        xmax[xb][hf][lrow] = mh;
+        tc_fence_before();
+        mbar_arrive(XBAR0 + 8u * xb);
+        if (!wait_role(XBAR0 + 8u * xb, xb ? x_ph1 : x_ph0, abort_flag)) {
+          ok = false;
+          break;
+        }
+        if (xb) x_ph1 ^= 1; else x_ph0 ^= 1;
+        tc_fence_after();
+        const float mo = xmax[xb][hf ^ 1][lrow];
         float alpha;
-        softmax_tile(sv, kTile, p.c, m, l, P, alpha);
-        tmem_st32(tl + C::T_S + b * kTile, P);
-        if (k > 0) {
-          if (!wait_role(ODONE, od_ph, abort_flag)) {
+        const float m_new = next_max(m, fmaxf(mh, mo), p.c, alpha);
+        uint32_t P[kHalf / 2];
+        const float rs = half_probs(sv, kHalf, p.c, m_new, P);
+        lh = __fmaf_rn(lh, alpha, rs);
+        m = m_new;
+        tmem_st16(tl + C::T_S + b * kTile + hf * (kHalf / 2), P);
+        if (k > 0 && __any_sync(0xffffffffu, alpha != 1.f)) {
+          const uint32_t t = sbuf - 1;  // PV of the previous tile must be complete
+          if (!wait_role(ODONE0 + 8u * (t & 1), (t >> 1) & 1, abort_flag)) {
             ok = false;
             break;
           }
-          od_ph ^= 1;
           tc_fence_after();
-          if (__any_sync(0xffffffffu, alpha != 1.f)) rescale_o<D>(tl + C::T_O, alpha);
+          rescale_o(tl + C::T_O, hf * (D / 2), (hf + 1) * (D / 2), alpha);
         }
         tmem_st_wait();
         tc_fence_before();
@@ -443,13 +514,17 @@ __global__ void __launch_bounds__(192, 1) attn_split_kernel(const __grid_constan
         sbuf++;
       }
       if (!ok) break;
-      if (!wait_role(ODONE, od_ph, abort_flag)) {
-        ok = false;
-        break;
+      {
+        const uint32_t t = sbuf - 1;  // the item's last PV
+        if (!wait_role(ODONE0 + 8u * (t & 1), (t >> 1) & 1, abort_flag)) {
+          ok = false;
+          break;
+        }
       }
-      od_ph ^= 1;
       tc_fence_after();
-      store_state<D>(tl + C::T_O, valid ? ws_rec(p, I.s, I.g, I.split, row, D) : nullptr, m, l);
+      // the next item's first PV waits for QREADY, which every thread signals
+      // only after this read of O
+      store_state<D>(tl + C::T_O, valid ? ws_rec(p, I.s, I.g, I.split, row, D) : nullptr, hf, m, lh);
     }
     if (!ok) set_status(p.status, TV_ERR_TIMEOUT);
   }
@@ -462,18 +537,27 @@ __global__ void __launch_bounds__(192, 1) attn_split_kernel(const __grid_constan
 // ---------------------------------------------------------------------------
 // tail kernel: the node's own tiles, then the split merge
 // ---------------------------------------------------------------------------
+__device__ __forceinline__ void cp_async16(uint32_t dst, const void* src, bool valid) {
+  asm volatile("cp.async.cg.shared.global [%0], [%1], 16, %2;" ::"r"(dst), "l"(src), "r"(valid ? 16 : 0)
+               : "memory");
+}
+__device__ __forceinline__ void cp_async_wait_all() { asm volatile("cp.async.wait_all;" ::: "memory"); }
+
 template <int D>
-__global__ void __launch_bounds__(128, 1) attn_tail_kernel(const __grid_constant__ TcParams p) {
+__global__ void __launch_bounds__(256, 1) attn_tail_kernel(const __grid_constant__ TcParams p) {
   using C = Tc<D>;
   extern __shared__ uint8_t smem_raw[];
   __shared__ int skip;
+  __shared__ float xmax[2][128];
+  __shared__ int anc_s[TV_MAX_PATH];  // global node of the ancestor at each depth
   const uint32_t raw = smem_u32(smem_raw);
   const uint32_t sb = (raw + 1023u) & ~1023u;
   uint8_t* gb = smem_raw + (sb - raw);
   const uint32_t BAR = sb + 2 * C::TILE, DRAIN = BAR + 8;
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(gb + 2 * C::TILE + 16);
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const int lrow = warp * 32 + lane;
+  const int hf = warp >> 2;  // softmax half of this thread
+  const int lrow = (warp & 3) * 32 + lane;
   const int item = blockIdx.x;
   const int g = item % p.Hkv;
   const int node_g = item / p.Hkv;  // global node (verify) or sequence (decode)
@@ -491,6 +575,10 @@ __global__ void __launch_bounds__(128, 1) attn_tail_kernel(const __grid_constant
   }
   const int local = node_g - off;
   const int L = p.len[s];
+  if (threadIdx.x < TV_MAX_PATH) {
+    const int a = p.decode ? -1 : anc[threadIdx.x];  // the ancestor row, read whole
+    anc_s[threadIdx.x] = (p.decode || threadIdx.x > depth) ? node_g : off + a;
+  }
   if (threadIdx.x == 0) {
     mbar_init(BAR, 1);
     mbar_init(DRAIN, 1);
@@ -514,77 +602,115 @@ __global__ void __launch_bounds__(128, 1) attn_tail_kernel(const __grid_constant
   __syncthreads();
   tc_fence_after();
   const uint32_t tbase = *tmem_slot;
-  const uint32_t tl = tbase + (static_cast<uint32_t>(warp * 32) << 16);
+  const uint32_t tl = tbase + (static_cast<uint32_t>((warp & 3) * 32) << 16);
 
   if (!skip) {
+    const int G = p.G;
     const int P = L + depth + 1;
     const int tsh = L / kTile, tlast = (L + depth) / kTile;
     const int ST = p.split_tiles;
-    const bool vrow = lrow < p.G;
-    const int row_seq = local * p.G + lrow;
-    const int qh = g * p.G + lrow;
-    load_q_tmem<D>(tl + C::T_Q, vrow ? p.q + (static_cast<size_t>(node_g) * p.Hq + qh) * D : nullptr);
-    float m = -INFINITY, l = 0.f;
-    bool fresh = true;
+    const bool vrow = lrow < G;
+    const int row_seq = local * G + lrow;
     int cur = tsh / ST;
-    if (tsh % ST != 0) {
-      // continue the split the split kernel started for this row
-      const float* rec = vrow ? ws_rec(p, s, g, cur, row_seq, D) : nullptr;
+    const bool cont = (tsh % ST) != 0;  // the split kernel started this split
+
+    // stage this node's G query rows (V tile area) and, when continuing, the
+    // carried state records (K tile area) with cp.async
+    const uint32_t qstage = sb + C::TILE, ostage = sb;
+    const bool ostaged = G * C::REC * 4 <= C::TILE;
+    {
+      const __nv_bfloat16* qsrc = p.q + (static_cast<size_t>(node_g) * p.Hq + g * G) * D;
+      for (int idx = threadIdx.x; idx < G * D / 8; idx += blockDim.x)
+        cp_async16(qstage + idx * 16, qsrc + idx * 8, true);
+      if (cont && ostaged) {
+        for (int idx = threadIdx.x; idx < G * C::REC / 4; idx += blockDim.x) {
+          const int r = idx / (C::REC / 4), cc = idx % (C::REC / 4);
+          cp_async16(ostage + idx * 16, ws_rec(p, s, g, cur, local * G + r, D) + cc * 4, true);
+        }
+      }
+      cp_async_wait_all();
+      __syncthreads();
+    }
+    // Q and the carried O into TMEM (each half its own columns)
+    {
+      const uint4* qs = reinterpret_cast<const uint4*>(gb + C::TILE) + lrow * (D / 8);
 #pragma unroll 1
-      for (int c0 = 0; c0 < D; c0 += 32) {
+      for (int c0 = hf * (D / 4); c0 < (hf + 1) * (D / 4); c0 += 32) {
         uint32_t r[32];
-        if (rec) {
-          const uint4* s4 = reinterpret_cast<const uint4*>(rec + c0);
 #pragma unroll
-          for (int i = 0; i < 8; i++) {
-            const uint4 v = s4[i];
-            r[4 * i] = v.x;
-            r[4 * i + 1] = v.y;
-            r[4 * i + 2] = v.z;
-            r[4 * i + 3] = v.w;
-          }
-        } else {
+        for (int i = 0; i < 8; i++) {
+          const uint4 v = vrow ? qs[c0 / 4 + i] : make_uint4(0u, 0u, 0u, 0u);
+          r[4 * i] = v.x;
+          r[4 * i + 1] = v.y;
+          r[4 * i + 2] = v.z;
+          r[4 * i + 3] = v.w;
+        }
+        tmem_st32(tl + C::T_Q + c0, r);
+      }
+    }
+    float m = -INFINITY, lh = 0.f;
+    bool fresh = true;
+    if (cont) {
+      const float* rec = vrow ? (ostaged ? reinterpret_cast<const float*>(gb) + lrow * C::REC
+                                         : ws_rec(p, s, g, cur, row_seq, D))
+                              : nullptr;
+#pragma unroll 1
+      for (int c0 = hf * (D / 2); c0 < (hf + 1) * (D / 2); c0 += 32) {
+        uint32_t r[32];
 #pragma unroll
-          for (int i = 0; i < 32; i++) r[i] = 0u;
+        for (int i = 0; i < 8; i++) {
+          const uint4 v = rec ? reinterpret_cast<const uint4*>(rec + c0)[i] : make_uint4(0u, 0u, 0u, 0u);
+          r[4 * i] = v.x;
+          r[4 * i + 1] = v.y;
+          r[4 * i + 2] = v.z;
+          r[4 * i + 3] = v.w;
         }
         tmem_st32(tl + C::T_O + c0, r);
       }
       if (rec) {
         m = rec[D];
-        l = rec[D + 1];
+        lh = rec[D + 1 + hf];
       }
       fresh = false;
     }
     tmem_st_wait();
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+
     uint32_t ph = 0;
     bool ok = true;
     for (int t = tsh; t <= tlast && ok; t++) {
       if (t / ST != cur) {
-        store_state<D>(tl + C::T_O, vrow ? ws_rec(p, s, g, cur, row_seq, D) : nullptr, m, l);
+        store_state<D>(tl + C::T_O, vrow ? ws_rec(p, s, g, cur, row_seq, D) : nullptr, hf, m, lh);
         cur = t / ST;
         fresh = true;
         m = -INFINITY;
-        l = 0.f;
+        lh = 0.f;
       }
-      // build the node's K/V tile: cache rows below L, ancestors at L..L+d, zeros after
+      // gather the node's K/V tile: cache rows below L, ancestors at L..L+d, zeros after
       for (int idx = threadIdx.x; idx < kTile * (D / 8); idx += blockDim.x) {
         const int j = idx / (D / 8), cc = idx % (D / 8), pos = t * kTile + j;
-        uint4 kv = make_uint4(0u, 0u, 0u, 0u), vv = kv;
+        const __nv_bfloat16* ksrc = p.kt;
+        const __nv_bfloat16* vsrc = p.vt;
+        bool have = false;
         if (pos < L) {
-          const size_t r = (static_cast<size_t>(g) * p.cap + pos) * D;
-          kv = reinterpret_cast<const uint4*>(p.K[s] + r)[cc];
-          vv = reinterpret_cast<const uint4*>(p.V[s] + r)[cc];
+          const size_t r = (static_cast<size_t>(g) * p.cap + pos) * D + cc * 8;
+          ksrc = p.K[s] + r;
+          vsrc = p.V[s] + r;
+          have = true;
         } else if (pos < P) {
-          const int tn = p.decode ? node_g : off + anc[pos - L];
-          const size_t r = (static_cast<size_t>(tn) * p.Hkv + g) * D;
-          kv = reinterpret_cast<const uint4*>(p.kt + r)[cc];
-          vv = reinterpret_cast<const uint4*>(p.vt + r)[cc];
+          const size_t r = (static_cast<size_t>(anc_s[pos - L]) * p.Hkv + g) * D + cc * 8;
+          ksrc = p.kt + r;
+          vsrc = p.vt + r;
+          have = true;
         }
         const int kb = cc >> 3, c = cc & 7;
         const uint32_t o = kb * kBox + (j >> 3) * 1024 + (j & 7) * 128 + ((c ^ (j & 7)) << 4);
-        *reinterpret_cast<uint4*>(gb + o) = kv;
-        *reinterpret_cast<uint4*>(gb + C::TILE + o) = vv;
+        cp_async16(sb + o, ksrc, have);
+        cp_async16(sb + C::TILE + o, vsrc, have);
       }
+      cp_async_wait_all();
       fence_proxy_async_smem();
       tc_fence_before();
       __syncthreads();
@@ -593,19 +719,30 @@ __global__ void __launch_bounds__(128, 1) attn_tail_kernel(const __grid_constant
         issue_qk<D>(tbase + C::T_S, tbase + C::T_Q, sb);
         tc_commit(BAR);
       }
-      if (!mbar_wait(BAR, ph, kWaitCycles)) {
+      if (__syncthreads_or(!mbar_wait(BAR, ph, kWaitCycles))) {
         ok = false;
         break;
       }
       ph ^= 1;
       tc_fence_after();
-      float sv[kTile];
-      tmem_ld64f(tl + C::T_S, sv);
-      uint32_t Pw[kTile / 2];
+      float sv[kHalf];
+      tmem_ld32f(tl + C::T_S + hf * kHalf, sv);
+      const int nvalid = min(kTile, P - t * kTile) - hf * kHalf;
+      const float mh = half_max(sv, nvalid);
+      xmax[hf][lrow] = mh;
+      tc_fence_before();
+      __syncthreads();
+      tc_fence_after();
+      const float mo = xmax[hf ^ 1][lrow];
       float alpha;
-      softmax_tile(sv, min(kTile, P - t * kTile), p.c, m, l, Pw, alpha);
-      tmem_st32(tl + C::T_S, Pw);
-      if (!fresh && __any_sync(0xffffffffu, alpha != 1.f)) rescale_o<D>(tl + C::T_O, alpha);
+      const float m_new = next_max(m, fmaxf(mh, mo), p.c, alpha);
+      uint32_t Pw[kHalf / 2];
+      const float rs = half_probs(sv, nvalid, p.c, m_new, Pw);
+      lh = __fmaf_rn(lh, alpha, rs);
+      m = m_new;
+      tmem_st16(tl + C::T_S + hf * (kHalf / 2), Pw);
+      if (!fresh && __any_sync(0xffffffffu, alpha != 1.f))
+        rescale_o(tl + C::T_O, hf * (D / 2), (hf + 1) * (D / 2), alpha);
       tmem_st_wait();
       tc_fence_before();
       __syncthreads();
@@ -614,45 +751,115 @@ __global__ void __launch_bounds__(128, 1) attn_tail_kernel(const __grid_constant
         issue_pv<D>(tbase + C::T_O, tbase + C::T_S, sb + C::TILE, !fresh);
         tc_commit(BAR);
       }
-      if (!mbar_wait(BAR, ph, kWaitCycles)) {
+      if (__syncthreads_or(!mbar_wait(BAR, ph, kWaitCycles))) {
         ok = false;
         break;
       }
       ph ^= 1;
       tc_fence_after();
       fresh = false;
-      __syncthreads();
     }
     if (!ok) {
       set_status(p.status, TV_ERR_TIMEOUT);
     } else {
-      store_state<D>(tl + C::T_O, vrow ? ws_rec(p, s, g, cur, row_seq, D) : nullptr, m, l);
+      store_state<D>(tl + C::T_O, vrow ? ws_rec(p, s, g, cur, row_seq, D) : nullptr, hf, m, lh);
       __syncthreads();
-      // merge splits 0..cur in split order
+      // merge splits 0..cur in split order: weights 2^(m_s - max m), sums l_A + l_B
       const int ns = cur + 1;
-      const size_t sstride = static_cast<size_t>(p.rows_max) * (D + 4);
-      for (int idx = threadIdx.x; idx < p.G * (D / 4); idx += blockDim.x) {
+      const size_t sstride = static_cast<size_t>(p.rows_max) * C::REC;
+      float* wsm = reinterpret_cast<float*>(gb);                 // [ns][G] weights (tile area is free now)
+      float* ltot = wsm + static_cast<size_t>(ns) * G;           // [G]
+      const bool wstaged = (2 * static_cast<size_t>(ns) * G + 2 * G) * 4 <= 2 * C::TILE;
+      if (wstaged) {
+        // (m, l_A + l_B) of every (split, row), loaded in parallel
+        float* lsm = ltot + G;  // [ns][G]
+        for (int base = threadIdx.x; base < ns * G; base += 4 * blockDim.x) {
+          float mv4[4], la[4], lb[4];
+#pragma unroll
+          for (int u = 0; u < 4; u++) {
+            const int idx = base + u * blockDim.x;
+            if (idx < ns * G) {
+              const float* rec = ws_rec(p, s, g, idx / G, local * G + idx % G, D);
+              mv4[u] = rec[D];
+              la[u] = rec[D + 1];
+              lb[u] = rec[D + 2];
+            }
+          }
+#pragma unroll
+          for (int u = 0; u < 4; u++) {
+            const int idx = base + u * blockDim.x;
+            if (idx < ns * G) {
+              wsm[idx] = mv4[u];
+              lsm[idx] = __fadd_rn(la[u], lb[u]);
+            }
+          }
+        }
+        __syncthreads();
+        // max reference per row, then every weight in parallel, then the sums in split order
+        float* mref = lsm + static_cast<size_t>(ns) * G;  // [G]
+        for (int r = threadIdx.x; r < G; r += blockDim.x) {
+          float mm = -INFINITY;
+          for (int sp = 0; sp < ns; sp++) mm = fmaxf(mm, wsm[sp * G + r]);
+          mref[r] = mm;
+        }
+        __syncthreads();
+        for (int idx = threadIdx.x; idx < ns * G; idx += blockDim.x) {
+          const float ms = wsm[idx], mm = mref[idx % G];
+          wsm[idx] = (ms == mm) ? 1.f : ex2_approx(__fsub_rn(ms, mm));
+        }
+        __syncthreads();
+        for (int r = threadIdx.x; r < G; r += blockDim.x) {
+          float ls = 0.f;
+          for (int sp = 0; sp < ns; sp++) ls = __fmaf_rn(wsm[sp * G + r], lsm[sp * G + r], ls);
+          ltot[r] = ls;
+        }
+        __syncthreads();
+      }
+      for (int idx = threadIdx.x; idx < G * (D / 4); idx += blockDim.x) {
         const int r = idx / (D / 4), c4 = idx % (D / 4);
-        const float* rec0 = ws_rec(p, s, g, 0, local * p.G + r, D);
-        float mm = -INFINITY;
-        for (int sp = 0; sp < ns; sp++) mm = fmaxf(mm, rec0[sp * sstride + D]);
-        float ls = 0.f;
+        const float* rec0 = ws_rec(p, s, g, 0, local * G + r, D);
+        float mm = 0.f, ls = 0.f;
+        if (!wstaged) {
+          mm = -INFINITY;
+          for (int sp = 0; sp < ns; sp++) mm = fmaxf(mm, rec0[sp * sstride + D]);
+        }
         float4 o = make_float4(0.f, 0.f, 0.f, 0.f);
-        for (int sp = 0; sp < ns; sp++) {
-          const float* rec = rec0 + sp * sstride;
-          const float ms = rec[D];
-          const float wgt = (ms == mm) ? 1.f : ex2_approx(__fsub_rn(ms, mm));
-          ls = __fmaf_rn(wgt, rec[D + 1], ls);
-          const float4 v = reinterpret_cast<const float4*>(rec)[c4];
-          o.x = __fmaf_rn(wgt, v.x, o.x);
-          o.y = __fmaf_rn(wgt, v.y, o.y);
-          o.z = __fmaf_rn(wgt, v.z, o.z);
-          o.w = __fmaf_rn(wgt, v.w, o.w);
+        if (wstaged) {
+          // 8 splits' partial rows in flight at a time, accumulated in split order
+          for (int sp0 = 0; sp0 < ns; sp0 += 8) {
+            float4 v[8];
+#pragma unroll
+            for (int u = 0; u < 8; u++)
+              if (sp0 + u < ns) v[u] = reinterpret_cast<const float4*>(rec0 + (sp0 + u) * sstride)[c4];
+#pragma unroll
+            for (int u = 0; u < 8; u++) {
+              if (sp0 + u < ns) {
+                const float wgt = wsm[(sp0 + u) * G + r];
+                o.x = __fmaf_rn(wgt, v[u].x, o.x);
+                o.y = __fmaf_rn(wgt, v[u].y, o.y);
+                o.z = __fmaf_rn(wgt, v[u].z, o.z);
+                o.w = __fmaf_rn(wgt, v[u].w, o.w);
+              }
+            }
+          }
+          ls = ltot[r];
+        } else {
+          for (int sp = 0; sp < ns; sp++) {
+            const float* rec = rec0 + sp * sstride;
+            const float ms = rec[D];
+            const float wgt = (ms == mm) ? 1.f : ex2_approx(__fsub_rn(ms, mm));
+            ls = __fmaf_rn(wgt, __fadd_rn(rec[D + 1], rec[D + 2]), ls);
+            const float4 v = reinterpret_cast<const float4*>(rec)[c4];
+            o.x = __fmaf_rn(wgt, v.x, o.x);
+            o.y = __fmaf_rn(wgt, v.y, o.y);
+            o.z = __fmaf_rn(wgt, v.z, o.z);
+            o.w = __fmaf_rn(wgt, v.w, o.w);
+          }
         }
         uint2 packed;
         packed.x = pack_bf16x2(__fdiv_rn(o.x, ls), __fdiv_rn(o.y, ls));
         packed.y = pack_bf16x2(__fdiv_rn(o.z, ls), __fdiv_rn(o.w, ls));
-        *reinterpret_cast<uint2*>(p.out + (static_cast<size_t>(node_g) * p.Hq + g * p.G + r) * D + 4 * c4) = packed;
+        *reinterpret_cast<uint2*>(p.out + (static_cast<size_t>(node_g) * p.Hq + g * G + r) * D + 4 * c4) = packed;
       }
       if (p.decode) {
         // append the token's own key/value at row L
@@ -730,9 +937,9 @@ static tv_status launch_tc(const TcParams& p, int n_items_bound, int n_tail, cud
   }
   if (n_items_bound > 0) {
     const int grid = n_items_bound < num_sms() ? n_items_bound : num_sms();
-    attn_split_kernel<D><<<grid, 192, C::SMEM_SPLIT, st>>>(p);
+    attn_split_kernel<D><<<grid, 352, C::SMEM_SPLIT, st>>>(p);
   }
-  attn_tail_kernel<D><<<n_tail, 128, C::SMEM_TAIL, st>>>(p);
+  attn_tail_kernel<D><<<n_tail, 256, C::SMEM_TAIL, st>>>(p);
   return launch_status();
 }
 
@@ -740,6 +947,7 @@ tv_status attn_tc_launch(const tv_plan* plan, const AttnCall& a, void* ws, size_
   const tv_attn_layer* l = a.layer;
   if (!plan || plan->split < kTile || plan->split % kTile) return TV_ERR_ARG;
   const int G = l->Hq / l->Hkv;
+  if (G > kMaxGroup) return TV_ERR_SHAPE;
   const int n_max = a.decode ? 1 : a.n_max;
   const size_t need = attn_tc_ws_bytes(plan, l, a.n_seq, n_max, a.max_len);
   if (!ws || ws_bytes < need) return TV_ERR_WORKSPACE;

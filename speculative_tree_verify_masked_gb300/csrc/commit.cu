@@ -116,16 +116,19 @@ __global__ void __launch_bounds__(128) gdn_commit_kernel(const GdnCommitParams p
   const int row = rb * R + r;
   const bool valid = row < p.dv;
   float* Srow = lay.S[s] + (static_cast<size_t>(h) * p.dv + (valid ? row : 0)) * DK;
-  float st[16];
+  f2_t st[8];
   if (valid) {
-    load_row16<LPR>(st, Srow, jl);
+    load_row8<LPR>(st, Srow, jl);
   } else {
 #pragma unroll
-    for (int e = 0; e < 16; e++) st[e] = 0.f;
+    for (int e = 0; e < 8; e++) st[e] = 0ull;
   }
-  for (int j = 0; j < a; j++)
-    gdn_row_step<LPR, false>(st, kb[j], nullptr, jl, 0.f, vb[j][r], ab[j], bb[j], 0.f, true);
-  if (valid) store_row16<LPR>(Srow, st, jl);
+  for (int j = 0; j < a; j++) {
+    f2_t k[8];
+    load_row8<LPR>(k, kb[j], jl);
+    gdn_row_step<LPR, false>(st, k, k, 0.f, vb[j][r], ab[j], bb[j], 0.f, true);
+  }
+  if (valid) store_row8<LPR>(Srow, st, jl);
 }
 
 __global__ void commit_len_kernel(int32_t* len, const int32_t* acc_len, const int32_t* status, int n_seq) {

@@ -7,16 +7,40 @@
 //     c  = beta * (v_r - alpha * x)
 //     s' = alpha * s + c * k          (= alpha s (I - beta k k^T) + beta v_r k^T)
 //     o  = scale * (alpha * y + c * (k . q))   (= scale * s' . q)
-// A row is spread over LPR lanes, 16 elements each: element e of lane j is
-// column ((e / 4) * LPR + j) * 4 + (e % 4), so a lane group reads whole
-// 16-byte chunks of the row.  Every operation is an explicit IEEE op in a
-// fixed order (no contraction left to the compiler), and the lane reduction
-// is a butterfly whose pairwise sums are commutative, so all lanes of a group
-// hold the same bits.
+// A row is spread over LPR lanes, 16 elements each, held as 8 packed fp32
+// pairs: pair e of lane j covers columns ((e / 2) * LPR + j) * 4 + 2 (e % 2)
+// and the next one, so a lane group reads whole 16-byte chunks of the row.
+// The arithmetic uses the packed fp32x2 FMA / MUL instructions (two
+// independent IEEE round-to-nearest operations each); every operation is
+// explicit and in a fixed order, and the lane reduction is a butterfly whose
+// pairwise sums are commutative, so all lanes of a group hold the same bits.
 #pragma once
 #include "common.cuh"
 
 namespace tv {
+
+typedef unsigned long long f2_t;  // two fp32 values in one 64-bit register
+
+__device__ __forceinline__ f2_t f2_fma(f2_t a, f2_t b, f2_t c) {
+  f2_t d;
+  asm("fma.rn.f32x2 %0, %1, %2, %3;" : "=l"(d) : "l"(a), "l"(b), "l"(c));
+  return d;
+}
+__device__ __forceinline__ f2_t f2_mul(f2_t a, f2_t b) {
+  f2_t d;
+  asm("mul.rn.f32x2 %0, %1, %2;" : "=l"(d) : "l"(a), "l"(b));
+  return d;
+}
+__device__ __forceinline__ f2_t f2_dup(float x) {
+  f2_t d;
+  asm("mov.b64 %0, {%1, %1};" : "=l"(d) : "f"(x));
+  return d;
+}
+__device__ __forceinline__ float f2_hsum(f2_t a) {
+  float lo, hi;
+  asm("mov.b64 {%0, %1}, %2;" : "=f"(lo), "=f"(hi) : "l"(a));
+  return __fadd_rn(lo, hi);
+}
 
 template <int LPR>
 __device__ __forceinline__ float group_sum(float x) {
@@ -25,65 +49,57 @@ __device__ __forceinline__ float group_sum(float x) {
   return x;
 }
 
+// This lane's 8 pairs of a dk-long fp32 row (global or shared memory).
 template <int LPR>
-__device__ __forceinline__ void load_row16(float (&d)[16], const float* src, int j) {
-  const float4* p = reinterpret_cast<const float4*>(src);
+__device__ __forceinline__ void load_row8(f2_t (&d)[8], const float* src, int j) {
+  const ulonglong2* p = reinterpret_cast<const ulonglong2*>(src);
 #pragma unroll
   for (int c = 0; c < 4; c++) {
-    const float4 v = p[c * LPR + j];
-    d[4 * c + 0] = v.x;
-    d[4 * c + 1] = v.y;
-    d[4 * c + 2] = v.z;
-    d[4 * c + 3] = v.w;
+    const ulonglong2 v = p[c * LPR + j];
+    d[2 * c] = v.x;
+    d[2 * c + 1] = v.y;
   }
 }
-
 template <int LPR>
-__device__ __forceinline__ void store_row16(float* dst, const float (&s)[16], int j) {
-  float4* p = reinterpret_cast<float4*>(dst);
+__device__ __forceinline__ void store_row8(float* dst, const f2_t (&s)[8], int j) {
+  ulonglong2* p = reinterpret_cast<ulonglong2*>(dst);
 #pragma unroll
-  for (int c = 0; c < 4; c++) p[c * LPR + j] = make_float4(s[4 * c], s[4 * c + 1], s[4 * c + 2], s[4 * c + 3]);
-}
-
-// k . q for one token, sequential fused multiply-adds from zero.
-__device__ __forceinline__ float dot_seq(const float* a, const float* b, int n) {
-  float acc = 0.f;
-  for (int i = 0; i < n; i++) acc = __fmaf_rn(a[i], b[i], acc);
-  return acc;
+  for (int c = 0; c < 4; c++) p[c * LPR + j] = make_ulonglong2(s[2 * c], s[2 * c + 1]);
 }
 
 template <int LPR>
-__device__ __forceinline__ float row_dot(const float (&s)[16], const float (&w)[16]) {
-  float a0 = 0.f, a1 = 0.f;
+__device__ __forceinline__ float row_dot(const f2_t (&s)[8], const f2_t (&w)[8]) {
+  f2_t acc = 0ull;  // (+0.0f, +0.0f)
 #pragma unroll
-  for (int e = 0; e < 8; e++) a0 = __fmaf_rn(s[e], w[e], a0);
-#pragma unroll
-  for (int e = 8; e < 16; e++) a1 = __fmaf_rn(s[e], w[e], a1);
-  return group_sum<LPR>(__fadd_rn(a0, a1));
+  for (int e = 0; e < 8; e++) acc = f2_fma(s[e], w[e], acc);
+  return group_sum<LPR>(f2_hsum(acc));
 }
 
-// kv, qv: the token's key and query (fp32, dk values) in shared memory.
-// Returns o when WITH_OUT; advances s when `update`.
+// One token for one state row, with this lane's pairs of the token's key k
+// and query q already in registers and kq = k . q (from kq_group).  Returns
+// o when WITH_OUT; advances s when `update`.
 template <int LPR, bool WITH_OUT>
-__device__ __forceinline__ float gdn_row_step(float (&s)[16], const float* kv, const float* qv, int j, float kq,
-                                              float v, float alpha, float beta, float scale, bool update) {
-  float k[16];
-  load_row16<LPR>(k, kv, j);
+__device__ __forceinline__ float gdn_row_step(f2_t (&s)[8], const f2_t (&k)[8], const f2_t (&q)[8], float kq, float v,
+                                              float alpha, float beta, float scale, bool update) {
   const float x = row_dot<LPR>(s, k);
   float y = 0.f;
-  if (WITH_OUT) {
-    float q[16];
-    load_row16<LPR>(q, qv, j);
-    y = row_dot<LPR>(s, q);
-  }
+  if (WITH_OUT) y = row_dot<LPR>(s, q);
   const float c = __fmul_rn(beta, __fsub_rn(v, __fmul_rn(alpha, x)));
   float o = 0.f;
   if (WITH_OUT) o = __fmul_rn(scale, __fmaf_rn(c, kq, __fmul_rn(alpha, y)));
   if (update) {
+    const f2_t a2 = f2_dup(alpha), c2 = f2_dup(c);
 #pragma unroll
-    for (int e = 0; e < 16; e++) s[e] = __fmaf_rn(c, k[e], __fmul_rn(alpha, s[e]));
+    for (int e = 0; e < 8; e++) s[e] = f2_fma(c2, k[e], f2_mul(a2, s[e]));
   }
   return o;
+}
+
+// k . q of one token, by one lane group with the row layout (the same
+// reduction as a row dot), so every caller gets the same bits.
+template <int LPR>
+__device__ __forceinline__ float kq_group(const f2_t (&k)[8], const f2_t (&q)[8]) {
+  return row_dot<LPR>(k, q);
 }
 
 }  // namespace tv

@@ -3,166 +3,204 @@
 // Tree preparation derives, per node, the depth, the ancestor-or-self bitmask
 // (the tree mask of the merged draft tree, "One request, end to end" 2.6),
 // the ancestor at every depth (the rows a node attends to past the context)
-// and the traversal order of the recurrent layers.
+// and the traversal order of the recurrent layers.  One warp per sequence;
+// lane i owns nodes i and i + 32, and every table comes from walking at most
+// 15 parent links.
 //
 // Recurrent traversal.  Every node's Gated DeltaNet state is its parent's
 // state advanced by one token, so a depth-first walk needs the parent's state
-// only until its last child starts.  The walk visits the children of a node
-// with several children lightest subtree first and the heaviest last; the
-// parent's state is saved in a slot while the light subtrees run and the
-// heaviest child continues from that slot with the slot released.  Each saved
-// slot therefore sits above a light subtree of at most half the enclosing
-// size, so a tree of n nodes needs at most floor(log2(n / 3)) + 1 slots:
-// 5 for 64 nodes.  The order never changes any node's arithmetic: each state
-// is always exactly one step from its parent's.
+// only until its last child starts.  Leaves never advance the state (only
+// their outputs are needed), so the children of a node are visited leaves
+// first, then the non-leaf children lightest subtree first and the heaviest
+// last.  A node with two or more non-leaf children saves its state in a slot
+// while its light non-leaf subtrees run; the heaviest continues from the slot
+// with the slot released.  A save at slot level l happens inside l nested
+// light non-leaf subtrees, each at most half of the enclosing subtree, and a
+// saving node has at least five nodes below and including it, so a tree of n
+// nodes needs at most floor(log2(n / 5)) + 1 slots: 4 for 64 nodes.  The order
+// never changes any node's arithmetic: each state is exactly one step from its
+// parent's.
 #include "common.cuh"
 #include "host.hpp"
 
 namespace tv {
 
-__global__ void tree_prepare_kernel(const int32_t* __restrict__ node_off, const int32_t* __restrict__ parent,
-                                    void* meta, int32_t* status, int n_seq, int n_total, int n_max) {
-  const int s = threadIdx.x;
-  if (s >= n_seq) return;
+// Order among the children of one parent: leaves (0), light non-leaf (1), the
+// heaviest non-leaf child (2); ties by index.
+__device__ __forceinline__ int child_class(int c, const int* nch, const int* heavy, const int* par) {
+  return nch[c] == 0 ? 0 : (heavy[par[c]] == c ? 2 : 1);
+}
+
+__device__ __forceinline__ void tree_invalid(MetaView& mv, int s, int off, int32_t* status) {
+  set_status(status, TV_ERR_TREE);
+  mv.seq[s] = SeqInfo{0, off, 0, 0};
+}
+
+__global__ void __launch_bounds__(32) tree_prepare_kernel(const int32_t* __restrict__ node_off,
+                                                          const int32_t* __restrict__ parent, void* meta,
+                                                          int32_t* status, int n_seq, int n_total, int n_max) {
+  const int s = blockIdx.x;
+  const int lane = threadIdx.x;
+  __shared__ int par[TV_MAX_NODES], nch[TV_MAX_NODES], nnl[TV_MAX_NODES], size[TV_MAX_NODES];
+  __shared__ int hkey[TV_MAX_NODES], heavy[TV_MAX_NODES], rel[TV_MAX_NODES], first_light[TV_MAX_NODES];
   MetaView mv = meta_view(meta, n_total);
   const int off = node_off[s];
   const int end = node_off[s + 1];
   const int n = end - off;
-  bool ok = off >= 0 && end <= n_total && n >= 1 && n <= n_max && n <= TV_MAX_NODES &&
-            (s > 0 || off == 0) && (s < n_seq - 1 || end == n_total);
-  int par[TV_MAX_NODES], dep[TV_MAX_NODES], nch[TV_MAX_NODES], size[TV_MAX_NODES], heavy[TV_MAX_NODES];
-  uint64_t anc[TV_MAX_NODES];
-  int max_depth = 0;
-  if (ok) {
-    for (int i = 0; i < n && ok; i++) {
-      const int p = parent[off + i];
-      if (i == 0) {
-        ok = (p == -1);
-        par[0] = -1;
-        dep[0] = 0;
-        anc[0] = 1ull;
-      } else {
-        ok = (p >= 0 && p < i);
-        if (ok) {
-          par[i] = p;
-          dep[i] = dep[p] + 1;
-          anc[i] = anc[p] | (1ull << i);
-          ok = dep[i] < TV_MAX_PATH;
-          max_depth = dep[i] > max_depth ? dep[i] : max_depth;
-        }
-      }
-    }
-  }
+  const bool ok = off >= 0 && end <= n_total && n >= 1 && n <= n_max && n <= TV_MAX_NODES &&
+                  (s > 0 || off == 0) && (s < n_seq - 1 || end == n_total);
   if (!ok) {
-    set_status(status, TV_ERR_TREE);
-    mv.seq[s] = SeqInfo{0, off, 0, 0};
+    if (lane == 0) tree_invalid(mv, s, off, status);
     return;
   }
-  for (int i = 0; i < n; i++) {
-    mv.anc[off + i] = anc[i];
-    mv.depth[off + i] = dep[i];
-    int8_t* row = mv.anc_at + static_cast<size_t>(off + i) * TV_MAX_PATH;
-    for (int e = 0; e < TV_MAX_PATH; e++) row[e] = -1;
-    for (int j = i; j != -1; j = par[j]) row[dep[j]] = static_cast<int8_t>(j);
-  }
-  // subtree sizes and heaviest child (lowest index among equals)
-  for (int i = 0; i < n; i++) {
+  bool good = true;
+  for (int i = lane; i < n; i += 32) {
+    const int p = parent[off + i];
+    good = good && (i == 0 ? p == -1 : (p >= 0 && p < i));
+    par[i] = (i == 0 || !(p >= 0 && p < i)) ? -1 : p;
     nch[i] = 0;
+    nnl[i] = 0;
     size[i] = 1;
-    heavy[i] = -1;
+    hkey[i] = -1;
+    first_light[i] = 1 << 30;
   }
-  for (int i = n - 1; i >= 1; i--) size[par[i]] += size[i];
-  for (int i = 1; i < n; i++) {
-    const int p = par[i];
-    nch[p]++;
-    if (heavy[p] < 0 || size[i] > size[heavy[p]]) heavy[p] = i;
+  if (!__all_sync(0xffffffffu, good)) {
+    if (lane == 0) tree_invalid(mv, s, off, status);
+    return;
   }
-  // depth-first walk, lightest subtrees first; stack entries (node, src, level)
-  int st_node[TV_MAX_NODES], st_src[TV_MAX_NODES], st_lvl[TV_MAX_NODES];
-  int sp = 0, k = 0, max_slot = -1;
-  st_node[0] = 0;
-  st_src[0] = 0;
-  st_lvl[0] = 0;
-  sp = 1;
-  while (sp > 0 && ok) {
-    sp--;
-    const int u = st_node[sp], src = st_src[sp], lv = st_lvl[sp];
-    int save = 0;
-    if (nch[u] >= 2) {
-      if (lv >= kMaxSlots) {
-        ok = false;
-        break;
-      }
-      save = 1 + lv;
-      max_slot = lv > max_slot ? lv : max_slot;
+  __syncwarp();
+  // depth, ancestor bitmask, ancestor at every depth; subtree sizes; child counts
+  int my_depth = 0;
+  for (int i = lane; i < n; i += 32) {
+    int d = -1;
+    uint64_t mask = 0;
+    for (int j = i; j != -1; j = par[j]) {
+      mask |= 1ull << j;
+      d++;
     }
-    mv.sched[off + k] = sched_encode(u, src, save, nch[u] > 0 ? 1 : 0);
-    k++;
-    if (nch[u] == 0) continue;
-    if (nch[u] == 1) {
-      st_node[sp] = heavy[u];
-      st_src[sp] = 0;
-      st_lvl[sp] = lv;
-      sp++;
+    if (d >= TV_MAX_PATH) {
+      good = false;
       continue;
     }
-    st_node[sp] = heavy[u];
-    st_src[sp] = 1 + lv;
-    st_lvl[sp] = lv;
-    sp++;
-    int first_light = -1;
-    for (int c = n - 1; c >= 1; c--)
-      if (par[c] == u && c != heavy[u]) first_light = c;
-    for (int c = n - 1; c >= 1; c--) {
-      if (par[c] == u && c != heavy[u]) {
-        st_node[sp] = c;
-        st_src[sp] = (c == first_light) ? 0 : 1 + lv;
-        st_lvl[sp] = lv + 1;
-        sp++;
-      }
-    }
+    my_depth = d > my_depth ? d : my_depth;
+    mv.anc[off + i] = mask;
+    mv.depth[off + i] = d;
+    int8_t* row = mv.anc_at + static_cast<size_t>(off + i) * TV_MAX_PATH;
+    int e = d;
+    for (int j = i; j != -1; j = par[j], e--) row[e] = static_cast<int8_t>(j);
+    for (int x = d + 1; x < TV_MAX_PATH; x++) row[x] = -1;
+    for (int j = par[i]; j != -1; j = par[j]) atomicAdd(&size[j], 1);
+    if (i > 0) atomicAdd(&nch[par[i]], 1);
   }
-  if (!ok || k != n) {
-    set_status(status, TV_ERR_TREE);
-    mv.seq[s] = SeqInfo{0, off, 0, 0};
+  if (!__all_sync(0xffffffffu, good)) {
+    if (lane == 0) tree_invalid(mv, s, off, status);
     return;
   }
-  mv.seq[s] = SeqInfo{n, off, max_depth, max_slot + 1};
+  __syncwarp();
+  // non-leaf children and the heaviest of them (largest subtree, lowest index)
+  for (int i = lane; i < n; i += 32) {
+    if (i > 0 && nch[i] > 0) {
+      atomicAdd(&nnl[par[i]], 1);
+      atomicMax(&hkey[par[i]], (size[i] << 8) | (255 - i));
+    }
+  }
+  __syncwarp();
+  for (int i = lane; i < n; i += 32) heavy[i] = hkey[i] < 0 ? -1 : 255 - (hkey[i] & 255);
+  __syncwarp();
+  for (int i = lane; i < n; i += 32)
+    if (i > 0 && child_class(i, nch, heavy, par) == 1) atomicMin(&first_light[par[i]], i);
+  // offset of each node within its parent's subtree: 1 + sizes of the siblings before it
+  for (int i = lane; i < n; i += 32) {
+    int r = 0;
+    if (i > 0) {
+      const int p = par[i];
+      const int ci = child_class(i, nch, heavy, par);
+      r = 1;
+      for (int j = p + 1; j < n; j++) {
+        if (par[j] != p || j == i) continue;
+        const int cj = child_class(j, nch, heavy, par);
+        if (cj < ci || (cj == ci && j < i)) r += size[j];
+      }
+    }
+    rel[i] = r;
+  }
+  __syncwarp();
+  // preorder position, slot levels and the traversal entry of every node
+  int my_slot = -1;
+  for (int i = lane; i < n; i += 32) {
+    int pos = 0, lv = 0, last_edge_light = 0;
+    for (int j = i; j > 0; j = par[j]) {
+      pos += rel[j];
+      const int light = (nnl[par[j]] >= 2 && child_class(j, nch, heavy, par) == 1) ? 1 : 0;
+      if (j == i) last_edge_light = light;
+      lv += light;
+    }
+    const int lv_parent = lv - last_edge_light;
+    int src = 0;
+    if (i > 0) {
+      const int p = par[i];
+      const int ci = child_class(i, nch, heavy, par);
+      const bool from_registers = ci == 0 || nnl[p] < 2 || (ci == 1 && first_light[p] == i);
+      src = from_registers ? 0 : 1 + lv_parent;
+    }
+    int save = 0;
+    if (nnl[i] >= 2) {
+      save = 1 + lv;
+      my_slot = lv > my_slot ? lv : my_slot;
+    }
+    if (lv >= kMaxSlots) good = false;
+    mv.sched[off + pos] = sched_encode(i, src, save, nch[i] > 0 ? 1 : 0);
+  }
+  if (!__all_sync(0xffffffffu, good)) {
+    if (lane == 0) tree_invalid(mv, s, off, status);
+    return;
+  }
+  for (int o = 16; o >= 1; o >>= 1) {
+    my_depth = max(my_depth, __shfl_xor_sync(0xffffffffu, my_depth, o));
+    my_slot = max(my_slot, __shfl_xor_sync(0xffffffffu, my_slot, o));
+  }
+  if (lane == 0) mv.seq[s] = SeqInfo{n, off, my_depth, my_slot + 1};
 }
 
 // Longest agreeing path plus one token ("One request, end to end" 2.6).
-__global__ void accept_kernel(const int32_t* __restrict__ tok, const int32_t* __restrict__ greedy,
-                              const void* meta, int n_seq, int n_total, int32_t* path, int32_t* acc_len,
-                              int32_t* bonus, int32_t* status) {
-  const int s = threadIdx.x;
-  if (s >= n_seq) return;
+// One warp per sequence: a node agrees when every edge on its root path
+// carries the target's greedy token at the edge's parent; the deepest agreeing
+// node wins, lowest index among equally deep ones.
+__global__ void __launch_bounds__(32) accept_kernel(const int32_t* __restrict__ tok,
+                                                    const int32_t* __restrict__ greedy, const void* meta,
+                                                    int n_total, int32_t* path, int32_t* acc_len, int32_t* bonus,
+                                                    int32_t* status) {
+  const int s = blockIdx.x;
+  const int lane = threadIdx.x;
   int32_t* prow = path + s * TV_MAX_PATH;
   if (status_bad(status)) {
-    for (int e = 0; e < TV_MAX_PATH; e++) prow[e] = -1;
-    acc_len[s] = 0;
-    bonus[s] = -1;
+    if (lane < TV_MAX_PATH) prow[lane] = -1;
+    if (lane == 0) {
+      acc_len[s] = 0;
+      bonus[s] = -1;
+    }
     return;
   }
   MetaView mv = meta_view(const_cast<void*>(meta), n_total);
   const SeqInfo info = mv.seq[s];
   const int n = info.n, off = info.off;
-  bool agree[TV_MAX_NODES];
-  agree[0] = true;
-  int best = 0, best_depth = 0;
-  for (int i = 1; i < n; i++) {
+  int key = -1;
+  for (int i = lane; i < n; i += 32) {
     const int d = mv.depth[off + i];
-    const int p = mv.anc_at[static_cast<size_t>(off + i) * TV_MAX_PATH + d - 1];
-    agree[i] = agree[p] && tok[off + i] == greedy[off + p];
-    if (agree[i] && d > best_depth) {
-      best = i;
-      best_depth = d;
-    }
+    const int8_t* row = mv.anc_at + static_cast<size_t>(off + i) * TV_MAX_PATH;
+    bool agree = true;
+    for (int e = 1; e <= d; e++) agree = agree && tok[off + row[e]] == greedy[off + row[e - 1]];
+    if (agree) key = max(key, (d << 8) | (255 - i));
   }
-  const int a = best_depth + 1;
+  for (int o = 16; o >= 1; o >>= 1) key = max(key, __shfl_xor_sync(0xffffffffu, key, o));
+  const int best = 255 - (key & 255);
+  const int a = (key >> 8) + 1;
   const int8_t* arow = mv.anc_at + static_cast<size_t>(off + best) * TV_MAX_PATH;
-  for (int e = 0; e < TV_MAX_PATH; e++) prow[e] = e < a ? arow[e] : -1;
-  acc_len[s] = a;
-  bonus[s] = greedy[off + best];
+  if (lane < TV_MAX_PATH) prow[lane] = lane < a ? arow[lane] : -1;
+  if (lane == 0) {
+    acc_len[s] = a;
+    bonus[s] = greedy[off + best];
+  }
 }
 
 __global__ void len_advance_kernel(int32_t* len, const int32_t* by, int32_t inc, int n_seq) {
@@ -181,7 +219,7 @@ extern "C" size_t tv_tree_meta_bytes(int32_t n_seq, int32_t n_total) {
 
 extern "C" tv_status tv_tree_prepare(const tv_tree* t, tv_stream stream) {
   if (!tree_ok(t)) return TV_ERR_ARG;
-  tree_prepare_kernel<<<1, 32, 0, reinterpret_cast<cudaStream_t>(stream)>>>(
+  tree_prepare_kernel<<<t->n_seq, 32, 0, reinterpret_cast<cudaStream_t>(stream)>>>(
       t->node_off, t->parent, t->meta, t->status, t->n_seq, t->n_total, t->n_max);
   return launch_status();
 }
@@ -191,8 +229,8 @@ extern "C" tv_status tv_accept_path(const tv_tree* t, const int32_t* tok, const 
   if (!tree_ok(t) || !tok || !greedy || !path || !acc_len || !bonus) return TV_ERR_ARG;
   if (!aligned16(tok) || !aligned16(greedy) || !aligned16(path) || !aligned16(acc_len) || !aligned16(bonus))
     return TV_ERR_ALIGN;
-  accept_kernel<<<1, 32, 0, reinterpret_cast<cudaStream_t>(stream)>>>(tok, greedy, t->meta, t->n_seq, t->n_total,
-                                                                       path, acc_len, bonus, t->status);
+  accept_kernel<<<t->n_seq, 32, 0, reinterpret_cast<cudaStream_t>(stream)>>>(tok, greedy, t->meta, t->n_total, path,
+                                                                              acc_len, bonus, t->status);
   return launch_status();
 }
 

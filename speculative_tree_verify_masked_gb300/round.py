@@ -16,11 +16,39 @@ from . import binding as B
 from . import synth
 
 DEFAULT_SPLIT = 4096  # positions per KV split (multiple of 64)
+TILE = 64
+
+
+def auto_split(ctx_lens, n_nodes, Hq, Hkv, num_sms, lo=512, hi=16384):
+    """The split size (positions, multiple of 64) whose split-kernel makespan
+    is smallest for these context lengths and trees: items (split x KV head x
+    128-row block) are dealt round-robin to one persistent CTA per SM, an item
+    costs its tiles plus four tiles of start-up and write-back, and among equal makespans the
+    larger split (fewer partial states to merge) wins.  A deployment fixes
+    the result once; verify and decode must use the same value."""
+    G = Hq // Hkv
+    best = None
+    for split in range(lo, hi + 1, TILE):
+        st = split // TILE
+        costs = []
+        for L, n in zip(ctx_lens, n_nodes):
+            tsh = L // TILE
+            nrb = -(-n * G // 128)
+            for sp in range(-(-tsh // st)):
+                c = min(st, tsh - sp * st) + 4
+                costs += [c] * (Hkv * nrb)
+        loads = [0] * num_sms
+        for w, c in enumerate(costs):
+            loads[w % num_sms] += c
+        key = (max(loads) if costs else 0, -split)
+        if best is None or key < best[0]:
+            best = (key, split)
+    return best[1]
 
 
 class VerifyRound:
-    def __init__(self, cfg: synth.Workload, device="cuda", split: int = DEFAULT_SPLIT, layers=None,
-                 cap_extra: int = 64, seed_layers=None):
+    def __init__(self, cfg: synth.Workload, device="cuda", split: int | None = None, layers=None,
+                 cap_extra: int = 64):
         self.cfg = cfg
         self.device = device
         s = cfg.shapes
@@ -36,6 +64,10 @@ class VerifyRound:
         self.len = self.len0.clone()
         self.max_len = max(cfg.ctx_lens)
         self.cap = self.max_len + cap_extra
+        if split is None:
+            sms = torch.cuda.get_device_properties(device).multi_processor_count
+            split = auto_split(cfg.ctx_lens, self.n_nodes, s.Hq, s.Hkv, sms)
+        self.split = split
         self.plan = B.plan(split)
         self.attn_scale = 1.0 / math.sqrt(s.D)
         self.gdn_scale = 1.0 / math.sqrt(s.dk)
