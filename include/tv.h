@@ -73,7 +73,8 @@ typedef enum {
   TV_ERR_CUDA = 7,      /* a CUDA runtime call failed (launch, attribute) */
   TV_ERR_WORKSPACE = 8, /* workspace smaller than the *_workspace_bytes bound */
   TV_ERR_TIMEOUT = 9,   /* device: a bounded wait inside a kernel expired */
-  TV_ERR_LEN = 10       /* device: a sequence length above the host bound max_len */
+  TV_ERR_LEN = 10,      /* device: a sequence length above the host bound max_len */
+  TV_ERR_SCRATCH = 11   /* host: request larger than the fixed scratch of tv_attn_tree_verify_static */
 } tv_status;
 
 typedef enum { TV_F32 = 0, TV_BF16 = 1 } tv_dtype;
@@ -153,6 +154,35 @@ tv_status tv_attn_tree_verify(const tv_plan* plan, const tv_attn_layer* layer, c
                               const int32_t* len, int32_t max_len, const void* q, const void* k_t,
                               const void* v_t, void* out, float scale, void* workspace,
                               size_t workspace_bytes, tv_stream stream);
+
+/* Size of the fixed device scratch array behind tv_attn_tree_verify_static. */
+#define TV_STATIC_SCRATCH_BYTES ((size_t)48 << 20)
+size_t tv_attn_static_scratch_bytes(void);
+
+/* tv_attn_tree_verify without a workspace argument: the per-split partial
+ * states go to a fixed 48 MiB array of device memory inside the library (one
+ * per device), so the call allocates nothing and needs no scratch from the
+ * caller.  The pages have no counterpart; it serves callers that cannot hand
+ * over device scratch: a C or foreign-language host that links only this
+ * library and has no device allocator of its own, and a caller whose memory
+ * plan is fixed before the round starts and must not take a cudaMalloc in the
+ * middle of it (cudaMalloc can synchronise the device and stall other
+ * streams).
+ *  Arguments, layout and results: exactly those of tv_attn_tree_verify.
+ *  Limit: requests whose tv_attn_workspace_bytes(plan, layer, tree->n_seq,
+ *    tree->n_max, max_len) exceeds TV_STATIC_SCRATCH_BYTES return
+ *    TV_ERR_SCRATCH before anything is enqueued.
+ *  Setup: the first call on each device looks up the array's device address
+ *    (this loads the module); make that first call before any stream capture.
+ *  Start values: none needed; every scratch record a call reads was written
+ *    earlier in the same call.
+ *  Concurrency: all calls on one device share the one array, so two calls
+ *    whose work can overlap (different streams, or different host threads
+ *    without ordering) race on it and give wrong results.  Calls ordered on
+ *    one stream are safe. */
+tv_status tv_attn_tree_verify_static(const tv_plan* plan, const tv_attn_layer* layer, const tv_tree* tree,
+                                     const int32_t* len, int32_t max_len, const void* q, const void* k_t,
+                                     const void* v_t, void* out, float scale, tv_stream stream);
 
 /* ------------------------------------------------------------------------
  * Gated DeltaNet: the gated delta rule along every node's ancestor path

@@ -24,7 +24,7 @@ TV_F32, TV_BF16 = 0, 1
 
 STATUS_NAMES = {0: "TV_OK", 1: "TV_ERR_ARG", 2: "TV_ERR_SHAPE", 3: "TV_ERR_DTYPE", 4: "TV_ERR_ALIGN",
                 5: "TV_ERR_TREE", 6: "TV_ERR_CAPACITY", 7: "TV_ERR_CUDA", 8: "TV_ERR_WORKSPACE",
-                9: "TV_ERR_TIMEOUT", 10: "TV_ERR_LEN"}
+                9: "TV_ERR_TIMEOUT", 10: "TV_ERR_LEN", 11: "TV_ERR_SCRATCH"}
 
 
 class TvError(RuntimeError):
@@ -88,13 +88,17 @@ def lib():
                                      vp, vp]
         L.tv_len_advance.restype = c_int32
         L.tv_len_advance.argtypes = [vp, vp, c_int32, c_int32, vp]
+        L.tv_attn_static_scratch_bytes.restype = c_size_t
+        L.tv_attn_static_scratch_bytes.argtypes = []
+        L.tv_attn_tree_verify_static.restype = c_int32
+        L.tv_attn_tree_verify_static.argtypes = [P, A, T, vp, c_int32, vp, vp, vp, vp, c_float, vp]
         _lib = L
     return _lib
 
 
 EXPORTED = ["tv_status_string", "tv_version", "tv_tree_meta_bytes", "tv_tree_prepare", "tv_attn_workspace_bytes",
             "tv_attn_tree_verify", "tv_gdn_tree_verify", "tv_accept_path", "tv_commit_path", "tv_decode_step",
-            "tv_len_advance"]
+            "tv_len_advance", "tv_attn_static_scratch_bytes", "tv_attn_tree_verify_static"]
 
 
 def _check(code: int, where: str):
@@ -208,6 +212,18 @@ def tv_attn_tree_verify(pl, layer: AttnLayer, tree: Tree, len_, max_len, q, k_t,
                                      ctypes.byref(tree.c), _ptr(len_), max_len, _ptr(q), _ptr(k_t), _ptr(v_t),
                                      _ptr(out), scale, _ptr(ws), 0 if ws is None else ws.numel() * ws.element_size(),
                                      _stream(stream)), "tv_attn_tree_verify")
+
+
+def tv_attn_static_scratch_bytes() -> int:
+    return int(lib().tv_attn_static_scratch_bytes())
+
+
+def tv_attn_tree_verify_static(pl, layer: AttnLayer, tree: Tree, len_, max_len, q, k_t, v_t, out, scale,
+                               stream=None):
+    _check(lib().tv_attn_tree_verify_static(ctypes.byref(pl) if pl is not None else None, ctypes.byref(layer.c),
+                                            ctypes.byref(tree.c), _ptr(len_), max_len, _ptr(q), _ptr(k_t),
+                                            _ptr(v_t), _ptr(out), scale, _stream(stream)),
+           "tv_attn_tree_verify_static")
 
 
 def tv_gdn_tree_verify(layer: GdnLayer, tree: Tree, q, k, v, alpha, beta, out, scale, stream=None):

@@ -38,6 +38,7 @@ extern "C" const char* tv_status_string(tv_status s) {
     case TV_ERR_WORKSPACE: return "workspace too small";
     case TV_ERR_TIMEOUT: return "bounded device wait expired";
     case TV_ERR_LEN: return "sequence length above max_len";
+    case TV_ERR_SCRATCH: return "request exceeds the fixed static scratch (TV_STATIC_SCRATCH_BYTES)";
   }
   return "unknown status";
 }
