@@ -101,6 +101,9 @@ typedef struct {
   void* meta;              /* device, tv_tree_meta_bytes() bytes: derived tables (private layout) */
   int32_t* status;         /* device [1] error word, 0 = ok; shared by the calls of a round */
 } tv_tree;
+/* Every call that takes a tv_tree returns TV_ERR_ARG, enqueueing nothing, when
+ * the descriptor is ill formed on the host: NULL, counts out of range, or a
+ * NULL or non-16-byte-aligned pointer field. */
 
 /* Bytes of the `meta` buffer for a launch of n_total nodes. */
 size_t tv_tree_meta_bytes(int32_t n_seq, int32_t n_total);
