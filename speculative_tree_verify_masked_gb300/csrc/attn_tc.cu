@@ -18,13 +18,16 @@
 // Kernels.
 //  split kernel (persistent, one CTA per SM): the tiles that every node of a
 //    sequence shares (positions below 64*floor(L/64), all cache rows) for up to
-//    128 query rows (node x head of one KV head) at once.  Warp 0 streams K/V
-//    tiles with TMA (128B-swizzled boxes) through a ring of stages; warp 1
-//    issues the tcgen05 MMAs (Q and P live in TMEM, K and V in shared memory,
-//    S and O accumulate in TMEM); warps 2-5 and 6-9 run the softmax, one TMEM
-//    lane (query row) and one half tile per thread.  S is double-buffered so
-//    QK^T of tile t+1 runs on the tensor core while the softmax of tile t runs.
-//    Each split's state goes to the workspace.
+//    128 query rows (node x head of one KV head) at once.  Warps 0 and 10
+//    stream K and V tiles with TMA (128B-swizzled boxes) through two rings,
+//    with L2 prefetch further ahead; warp 1 issues QK^T (Q in TMEM, K in
+//    shared memory, S double-buffered in TMEM) and warp 11 issues PV (P in a
+//    ring of shared-memory slots, V in shared memory, O in TMEM); warps 2-5
+//    and 6-9 run the softmax, one TMEM lane (query row) and one half tile per
+//    thread.  An S buffer is reused as soon as the softmax has read it, so
+//    QK^T runs ahead of the softmax and the tensor pipe overlaps the narrow
+//    QK^T steps with the wide PV steps.  Each split's state goes to the
+//    workspace.
 //  tail kernel (one CTA per node and KV head): the node's own tiles (cache
 //    rows past the last shared tile plus its ancestors at their logical
 //    slots, gathered into shared memory with cp.async), continuing the split
@@ -47,6 +50,7 @@ constexpr int kTile = 64;       // KV positions per tile
 constexpr int kHalf = 32;       // positions per softmax half
 constexpr int kBox = 64 * 128;  // one [64 rows x 128 B] 128B-swizzled box
 constexpr int kMaxGroup = 64;   // query heads per KV head on this path
+constexpr int kPrefetch = 8;    // tiles of L2 prefetch ahead of the ring loads
 
 template <int D>
 struct Tc {
@@ -54,18 +58,23 @@ struct Tc {
   static constexpr int TILE = kTile * D * 2;  // bytes of one K or V tile
   // K and V tiles stream through separate rings: a K slot frees as soon as
   // QK^T of its tile completes, a V slot after PV, so K loads run further ahead.
-  static constexpr int NK = (D == 256) ? 4 : 6;
-  static constexpr int NV = (D == 256) ? 2 : 6;
+  static constexpr int NK = (D == 256) ? 3 : (D == 128 ? 4 : 6);
+  static constexpr int NV = (D == 256) ? 2 : (D == 128 ? 4 : 6);
+  // P tiles (bf16, 128 rows x 64 positions, the PV A operand) live in a ring
+  // of shared-memory slots, so an S buffer in TMEM is free again as soon as
+  // the softmax has read it.
+  static constexpr int PTILE = 128 * kTile * 2;
+  static constexpr int NP = 3;
   static constexpr int T_O = 0;              // TMEM columns: O [D]
-  static constexpr int T_S = D;              //   S/P [2 x 64]
+  static constexpr int T_S = D;              //   S [2 x 64]
   static constexpr int T_Q = D + 2 * kTile;  //   Q [D/2] (bf16 pairs)
   static constexpr int COLS = (D + 2 * kTile + D / 2) <= 256 ? 256 : 512;
   static constexpr uint32_t IDESC_QK = idesc_bf16_f32(128, kTile, false, false);
   static constexpr uint32_t IDESC_PV = idesc_bf16_f32(128, D, false, true);
-  static constexpr int RING = (NK + NV) * TILE;
-  static constexpr int NBAR = 2 * (NK + NV) + 10;
+  static constexpr int RING = (NK + NV) * TILE + NP * PTILE;
+  static constexpr int NBAR = 2 * (NK + NV) + 2 * NP + 9;
   static constexpr int SMEM_SPLIT = 1024 + RING + NBAR * 8 + 16;
-  static constexpr int SMEM_TAIL = 1024 + 2 * TILE + 16 + 16;
+  static constexpr int SMEM_TAIL = 1024 + 2 * TILE + PTILE + 16 + 16;
   static constexpr int REC = D + 4;  // workspace record: O[D], m, l_A, l_B, pad
 };
 
@@ -105,11 +114,33 @@ __device__ __forceinline__ void issue_qk(uint32_t tS, uint32_t tQ, uint32_t ktil
 #pragma unroll
   for (int kk = 0; kk < D / 16; kk++) tc_mma_ts(tS, tQ + kk * 8, desc_k(ktile, kk), Tc<D>::IDESC_QK, kk > 0 ? 1u : 0u);
 }
+// One K=16 step of QK^T from the tile's step-0 descriptor (the start-address
+// field is in 16-byte units; every offset stays inside the field).
 template <int D>
-__device__ __forceinline__ void issue_pv(uint32_t tO, uint32_t tP, uint32_t vtile, bool acc) {
+__device__ __forceinline__ void issue_qk_step_from(uint32_t tS, uint32_t tQ, uint64_t kd0, int kk) {
+  const uint64_t d = kd0 + static_cast<uint64_t>(((kk >> 2) * kBox + (kk & 3) * 32) >> 4);
+  tc_mma_ts(tS, tQ + kk * 8, d, Tc<D>::IDESC_QK, kk > 0 ? 1u : 0u);
+}
+// P tile in shared memory, K-major with the 128-byte swizzle: row r (query
+// row) is one 128-byte line of 64 bf16 probabilities; 16-byte chunk c sits at
+// chunk position c ^ (r % 8) of its line, lines grouped in 1024-byte atoms.
+__device__ __forceinline__ void store_p_half(uint32_t pslot, int row, int hf, const uint32_t (&P)[kHalf / 2]) {
+  const uint32_t line = pslot + (row >> 3) * 1024 + (row & 7) * 128;
+#pragma unroll
+  for (int q = 0; q < 4; q++) {
+    const uint32_t c = static_cast<uint32_t>(hf * 4 + q);
+    asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(line + ((c ^ (row & 7)) << 4)), "r"(P[4 * q]),
+                 "r"(P[4 * q + 1]), "r"(P[4 * q + 2]), "r"(P[4 * q + 3])
+                 : "memory");
+  }
+}
+// O (+)= P V with P from a shared-memory slot (step kk: positions 16kk..16kk+15).
+template <int D>
+__device__ __forceinline__ void issue_pv_ss(uint32_t tO, uint32_t pslot, uint64_t vd0, bool acc) {
 #pragma unroll
   for (int kk = 0; kk < kTile / 16; kk++)
-    tc_mma_ts(tO, tP + kk * 8, desc_v(vtile, kk), Tc<D>::IDESC_PV, (acc || kk > 0) ? 1u : 0u);
+    tc_mma_ss(tO, sdesc_sw128(pslot + kk * 32, 16, 1024), vd0 + static_cast<uint64_t>((kk * 2048) >> 4),
+              Tc<D>::IDESC_PV, (acc || kk > 0) ? 1u : 0u);
 }
 
 // Max of the valid slots of one half tile (exact; any order gives the same).
@@ -162,15 +193,6 @@ __device__ __forceinline__ void tmem_ld32f(uint32_t taddr, float (&s)[kHalf]) {
   tmem_ld32(taddr, r);
 #pragma unroll
   for (int i = 0; i < 32; i++) s[i] = __uint_as_float(r[i]);
-}
-
-__device__ __forceinline__ void tmem_st16(uint32_t taddr, const uint32_t (&r)[16]) {
-  asm volatile(
-      "tcgen05.st.sync.aligned.32x32b.x16.b32 [%0], "
-      "{%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,%16};" ::"r"(taddr),
-      "r"(r[0]), "r"(r[1]), "r"(r[2]), "r"(r[3]), "r"(r[4]), "r"(r[5]), "r"(r[6]), "r"(r[7]), "r"(r[8]),
-      "r"(r[9]), "r"(r[10]), "r"(r[11]), "r"(r[12]), "r"(r[13]), "r"(r[14]), "r"(r[15])
-      : "memory");
 }
 
 // O columns [c0, c1) of this thread's lane times alpha.
@@ -262,6 +284,27 @@ __device__ inline Item item_at(const ItemSpace& is, const TcParams& p, int w) {
   return it;
 }
 
+// Warp-wide bounded wait: a non-blocking test first (the common case in a
+// full pipeline), then polling; gives up with the other roles.  The outcome
+// is the same in every lane.
+__device__ __forceinline__ bool wait_warp(uint32_t bar, uint32_t parity, volatile int* abort_flag) {
+  if (__all_sync(0xffffffffu, mbar_test(bar, parity))) return true;
+  const long long t0 = clock64();
+  while (true) {
+    const bool done = mbar_try_wait(bar, parity);
+    if (__all_sync(0xffffffffu, done)) return true;
+    int give_up = 0;
+    if (lane_id() == 0) {
+      if (*abort_flag) give_up = 1;
+      else if (clock64() - t0 > kWaitCycles) {
+        *abort_flag = 1;
+        give_up = 1;
+      }
+    }
+    if (__shfl_sync(0xffffffffu, give_up, 0)) return false;
+  }
+}
+
 // Bounded wait that also gives up as soon as another role has given up.
 __device__ __forceinline__ bool wait_role(uint32_t bar, uint32_t parity, volatile int* abort_flag) {
   if (mbar_try_wait(bar, parity)) return true;
@@ -277,7 +320,7 @@ __device__ __forceinline__ bool wait_role(uint32_t bar, uint32_t parity, volatil
 }
 
 template <int D>
-__global__ void __launch_bounds__(352, 1) attn_split_kernel(const __grid_constant__ TcParams p) {
+__global__ void __launch_bounds__(384, 1) attn_split_kernel(const __grid_constant__ TcParams p) {
   using C = Tc<D>;
   extern __shared__ uint8_t smem_raw[];
   __shared__ ItemSpace is;
@@ -293,16 +336,15 @@ __global__ void __launch_bounds__(352, 1) attn_split_kernel(const __grid_constan
   const uint32_t KFULL0 = bars, KEMPTY0 = bars + 8u * C::NK;
   const uint32_t VFULL0 = bars + 16u * C::NK, VEMPTY0 = VFULL0 + 8u * C::NV;
   const int nb = 2 * (C::NK + C::NV);
-  const uint32_t SFULL0 = bars + 8u * nb, PFULL0 = bars + 8u * (nb + 2);
-  // PV completion, one barrier per tile parity: the softmax of tile t waits for
-  // PV(t-1) only when it must rescale O.  When it waits, PV(t-2) is already
-  // complete (QK(t) was issued after it), so the barrier is at most one phase
-  // behind and its parity identifies the phase.
-  const uint32_t ODONE0 = bars + 8u * (nb + 4);
-  const uint32_t QREADY = bars + 8u * (nb + 6);
-  const uint32_t DRAIN = bars + 8u * (nb + 7);
-  const uint32_t XBAR0 = bars + 8u * (nb + 8);  // [2] half-max exchange, by tile parity
-  const uint32_t kring = sb, vring = sb + C::NK * C::TILE;
+  // S buffers (by tile parity): SFULL when QK^T has written S, SFREE when the
+  // softmax has read it.  P slots (tile % NP): PFULL when the softmax has
+  // written P, ODONE when PV has consumed it (and O holds that tile).
+  const uint32_t SFULL0 = bars + 8u * nb, SFREE0 = SFULL0 + 16u;
+  const uint32_t PFULL0 = SFREE0 + 16u, ODONE0 = PFULL0 + 8u * C::NP;
+  const uint32_t QREADY = ODONE0 + 8u * C::NP;
+  const uint32_t DRAIN = QREADY + 8u;  // [2] one per MMA warp
+  const uint32_t XBAR0 = DRAIN + 16u;  // [2] half-max exchange, by tile parity
+  const uint32_t kring = sb, vring = sb + C::NK * C::TILE, pring = vring + C::NV * C::TILE;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
 
   if (threadIdx.x == 0) {
@@ -316,14 +358,16 @@ __global__ void __launch_bounds__(352, 1) attn_split_kernel(const __grid_constan
     }
     for (int b = 0; b < 2; b++) {
       mbar_init(SFULL0 + 8u * b, 1);
-      mbar_init(PFULL0 + 8u * b, 256);
+      mbar_init(SFREE0 + 8u * b, 256);
+      mbar_init(XBAR0 + 8u * b, 256);
     }
-    mbar_init(ODONE0, 1);
-    mbar_init(ODONE0 + 8u, 1);
+    for (int i = 0; i < C::NP; i++) {
+      mbar_init(PFULL0 + 8u * i, 256);
+      mbar_init(ODONE0 + 8u * i, 1);
+    }
     mbar_init(QREADY, 256);
     mbar_init(DRAIN, 1);
-    mbar_init(XBAR0, 256);
-    mbar_init(XBAR0 + 8u, 256);
+    mbar_init(DRAIN + 8u, 1);
     *abort_flag = 0;
     fence_mbar_init();
     skip = status_bad(p.status) ? 1 : 0;
@@ -350,7 +394,18 @@ __global__ void __launch_bounds__(352, 1) attn_split_kernel(const __grid_constan
     bool ok = true;
     for (int w = blockIdx.x; w < total && ok; w += gridDim.x) {
       const Item I = item_at(is, p, w);
+      const int ybase = I.g * p.cap;
+      // L2 prefetch runs kPrefetch tiles ahead of the ring's loads, so a ring
+      // load waits for L2, not DRAM
+      for (int t = I.t0; t < min(I.t0 + kPrefetch, I.t1); t++)
+#pragma unroll
+        for (int kb = 0; kb < C::KB; kb++) tma_prefetch_l2_2d(&maps[I.s], kb * 64, ybase + t * kTile);
       for (int t = I.t0; t < I.t1; t++) {
+        if (t + kPrefetch < I.t1) {
+#pragma unroll
+          for (int kb = 0; kb < C::KB; kb++)
+            tma_prefetch_l2_2d(&maps[I.s], kb * 64, ybase + (t + kPrefetch) * kTile);
+        }
         const int st = it % nslot;
         if (!wait_role(empty0 + 8u * st, ((it / nslot) & 1) ^ 1, abort_flag)) {
           ok = false;
@@ -359,7 +414,7 @@ __global__ void __launch_bounds__(352, 1) attn_split_kernel(const __grid_constan
         const uint32_t full = full0 + 8u * st;
         mbar_arrive_expect_tx(full, C::TILE);
         const uint32_t dst = ring + st * C::TILE;
-        const int y = I.g * p.cap + t * kTile;
+        const int y = ybase + t * kTile;
 #pragma unroll
         for (int kb = 0; kb < C::KB; kb++) tma_load_2d(dst + kb * kBox, &maps[I.s], full, kb * 64, y);
         it++;
@@ -371,81 +426,82 @@ __global__ void __launch_bounds__(352, 1) attn_split_kernel(const __grid_constan
       for (uint32_t i = it > (uint32_t)nslot ? it - nslot : 0; i < it; i++)
         mbar_wait(full0 + 8u * (i % nslot), (i / nslot) & 1, kWaitCycles);
     }
-  } else if (!skip && warp == 1 && lane == 0) {
-    // ---------------- MMA issuer ----------------
-    uint32_t it = 0, sbuf = 0, q_ph = 0, pf_ph0 = 0, pf_ph1 = 0;
+  } else if (!skip && (warp == 1 || warp == 11)) {
+    // ---------------- MMA issuers, one warp each, whole-warp loops with one
+    // elected lane issuing.  Warp 1 issues QK^T(t) as soon as K(t) has landed
+    // and the softmax has read S(t-2) out of the same TMEM buffer; warp 11
+    // issues PV(t) as soon as P(t) and V(t) are in shared memory.  The two
+    // streams touch disjoint TMEM columns, and the tensor pipe overlaps the
+    // narrow QK^T steps with the wide PV steps. ----------------
+    const bool is_qk = warp == 1;
+    uint32_t t = 0, q_ph = 0;  // CTA-wide tile counter
     bool ok = true;
     for (int w = blockIdx.x; w < total && ok; w += gridDim.x) {
       const Item I = item_at(is, p, w);
       const int n = I.t1 - I.t0;
-      if (!wait_role(QREADY, q_ph, abort_flag)) {
-        ok = false;
-        break;
-      }
-      q_ph ^= 1;
-      tc_fence_after();
-      for (int k = 0; k < n; k++) {
-        const int ks = it % C::NK;
-        if (!wait_role(KFULL0 + 8u * ks, (it / C::NK) & 1, abort_flag)) {
+      if (is_qk) {
+        if (!wait_warp(QREADY, q_ph, abort_flag)) {
           ok = false;
           break;
         }
-        tc_fence_after();
-        const int b = sbuf & 1;
-        issue_qk<D>(tbase + C::T_S + b * kTile, tbase + C::T_Q, kring + ks * C::TILE);
-        tc_commit(SFULL0 + 8u * b);
-        tc_commit(KEMPTY0 + 8u * ks);
-        if (k > 0) {
-          const int pb = b ^ 1;
-          const uint32_t pt = it - 1;
-          const int vs = pt % C::NV;
-          if (!wait_role(PFULL0 + 8u * pb, pb ? pf_ph1 : pf_ph0, abort_flag) ||
-              !wait_role(VFULL0 + 8u * vs, (pt / C::NV) & 1, abort_flag)) {
+        q_ph ^= 1;
+      }
+      for (int k = 0; k < n; k++, t++) {
+        if (is_qk) {
+          const int ks = t % C::NK, b = t & 1;
+          if (!wait_warp(KFULL0 + 8u * ks, (t / C::NK) & 1, abort_flag) ||
+              (t >= 2 && !wait_warp(SFREE0 + 8u * b, ((t - 2) >> 1) & 1, abort_flag))) {
             ok = false;
             break;
           }
-          if (pb) pf_ph1 ^= 1; else pf_ph0 ^= 1;
           tc_fence_after();
-          issue_pv<D>(tbase + C::T_O, tbase + C::T_S + pb * kTile, vring + vs * C::TILE, k - 1 > 0);
-          tc_commit(VEMPTY0 + 8u * vs);
-          tc_commit(ODONE0 + 8u * (pt & 1));
+          const uint32_t tS = tbase + C::T_S + b * kTile, tQ = tbase + C::T_Q;
+          const uint64_t kd = desc_k(kring + ks * C::TILE, 0);
+          if (elect_one_sync()) {
+#pragma unroll
+            for (int kk = 0; kk < D / 16; kk++) issue_qk_step_from<D>(tS, tQ, kd, kk);
+            tc_commit(SFULL0 + 8u * b);
+            tc_commit(KEMPTY0 + 8u * ks);
+          }
+          __syncwarp();
+        } else {
+          const int ps = t % C::NP, vs = t % C::NV;
+          if (!wait_warp(PFULL0 + 8u * ps, (t / C::NP) & 1, abort_flag) ||
+              !wait_warp(VFULL0 + 8u * vs, (t / C::NV) & 1, abort_flag)) {
+            ok = false;
+            break;
+          }
+          tc_fence_after();
+          if (elect_one_sync()) {
+            issue_pv_ss<D>(tbase + C::T_O, pring + ps * C::PTILE, desc_v(vring + vs * C::TILE, 0), k > 0);
+            tc_commit(VEMPTY0 + 8u * vs);
+            tc_commit(ODONE0 + 8u * ps);
+          }
+          __syncwarp();
         }
-        it++;
-        sbuf++;
       }
-      if (!ok) break;
-      const int pb = (sbuf - 1) & 1;
-      const uint32_t pt = it - 1;
-      const int vs = pt % C::NV;
-      if (!wait_role(PFULL0 + 8u * pb, pb ? pf_ph1 : pf_ph0, abort_flag) ||
-          !wait_role(VFULL0 + 8u * vs, (pt / C::NV) & 1, abort_flag)) {
-        ok = false;
-        break;
-      }
-      if (pb) pf_ph1 ^= 1; else pf_ph0 ^= 1;
-      tc_fence_after();
-      issue_pv<D>(tbase + C::T_O, tbase + C::T_S + pb * kTile, vring + vs * C::TILE, n - 1 > 0);
-      tc_commit(VEMPTY0 + 8u * vs);
-      tc_commit(ODONE0 + 8u * (pt & 1));
     }
-    // every MMA issued by this thread completes before TMEM is released
-    tc_commit(DRAIN);
-    mbar_wait(DRAIN, 0, kWaitCycles);
-    if (!ok) set_status(p.status, TV_ERR_TIMEOUT);
+    // every MMA issued by this warp completes before TMEM is released
+    const uint32_t drain = DRAIN + (is_qk ? 0u : 8u);
+    if (elect_one_sync()) tc_commit(drain);
+    __syncwarp();
+    mbar_wait(drain, 0, kWaitCycles);
+    if (!ok && lane == 0) set_status(p.status, TV_ERR_TIMEOUT);
   } else if (!skip && warp >= 2 && warp <= 9) {
     // ---------------- softmax / epilogue: warps 2-9, two warpgroups, one half tile each ----------------
     const int hf = (warp - 2) >> 2;  // 0: slots 0-31, 1: slots 32-63
     const int quad = warp & 3;
     const int lrow = quad * 32 + lane;
     const uint32_t tl = tbase + (static_cast<uint32_t>(quad * 32) << 16);
-    uint32_t sbuf = 0, sf_ph0 = 0, sf_ph1 = 0, x_ph0 = 0, x_ph1 = 0;
+    uint32_t t = 0;  // CTA-wide tile counter
     bool ok = true;
     for (int w = blockIdx.x; w < total && ok; w += gridDim.x) {
       const Item I = item_at(is, p, w);
       const int n = I.t1 - I.t0;
       const int row = I.rb * 128 + lrow;
       const bool valid = row < is.rows[I.s];
-      // this half's Q columns (bf16 pairs) into TMEM
+      // this half's Q columns (bf16 pairs) into TMEM; every QK^T of the
+      // previous item has completed (its S was read)
       {
         const uint4* q4 = nullptr;
         if (valid) {
@@ -471,59 +527,63 @@ __global__ void __launch_bounds__(352, 1) attn_split_kernel(const __grid_constan
       mbar_arrive(QREADY);
       float m = -INFINITY, lh = 0.f;
       for (int k = 0; k < n; k++) {
-        const int b = sbuf & 1;
-        if (!wait_role(SFULL0 + 8u * b, b ? sf_ph1 : sf_ph0, abort_flag)) {
+        const int b = t & 1;
+        if (!wait_role(SFULL0 + 8u * b, (t >> 1) & 1, abort_flag)) {
           ok = false;
           break;
         }
-        if (b) sf_ph1 ^= 1; else sf_ph0 ^= 1;
         tc_fence_after();
         float sv[kHalf];
         tmem_ld32f(tl + C::T_S + b * kTile + hf * kHalf, sv);
-        const float mh = half_max(sv, kHalf);
-        const int xb = sbuf & 1;
-        xmax[xb][hf][lrow] = mh;
         tc_fence_before();
-        mbar_arrive(XBAR0 + 8u * xb);
-        if (!wait_role(XBAR0 + 8u * xb, xb ? x_ph1 : x_ph0, abort_flag)) {
+        mbar_arrive(SFREE0 + 8u * b);  // S(t) is in registers: QK^T(t+2) may overwrite the buffer
+        const float mh = half_max(sv, kHalf);
+        xmax[b][hf][lrow] = mh;
+        mbar_arrive(XBAR0 + 8u * b);
+        if (!wait_role(XBAR0 + 8u * b, (t >> 1) & 1, abort_flag)) {
           ok = false;
           break;
         }
-        if (xb) x_ph1 ^= 1; else x_ph0 ^= 1;
-        tc_fence_after();
-        const float mo = xmax[xb][hf ^ 1][lrow];
+        const float mo = xmax[b][hf ^ 1][lrow];
         float alpha;
         const float m_new = next_max(m, fmaxf(mh, mo), p.c, alpha);
         uint32_t P[kHalf / 2];
         const float rs = half_probs(sv, kHalf, p.c, m_new, P);
         lh = __fmaf_rn(lh, alpha, rs);
         m = m_new;
-        tmem_st16(tl + C::T_S + b * kTile + hf * (kHalf / 2), P);
+        const int ps = t % C::NP;
+        if (t >= static_cast<uint32_t>(C::NP) &&
+            !wait_role(ODONE0 + 8u * ps, ((t - C::NP) / C::NP) & 1, abort_flag)) {  // slot's previous PV done
+          ok = false;
+          break;
+        }
+        store_p_half(pring + ps * C::PTILE, lrow, hf, P);
         if (k > 0 && __any_sync(0xffffffffu, alpha != 1.f)) {
-          const uint32_t t = sbuf - 1;  // PV of the previous tile must be complete
-          if (!wait_role(ODONE0 + 8u * (t & 1), (t >> 1) & 1, abort_flag)) {
+          const uint32_t tp = t - 1;  // PV of the previous tile must be complete
+          if (!wait_role(ODONE0 + 8u * (tp % C::NP), (tp / C::NP) & 1, abort_flag)) {
             ok = false;
             break;
           }
           tc_fence_after();
           rescale_o(tl + C::T_O, hf * (D / 2), (hf + 1) * (D / 2), alpha);
+          tmem_st_wait();
         }
-        tmem_st_wait();
+        fence_proxy_async_smem();  // P visible to the tensor core
         tc_fence_before();
-        mbar_arrive(PFULL0 + 8u * b);
-        sbuf++;
+        mbar_arrive(PFULL0 + 8u * ps);
+        t++;
       }
       if (!ok) break;
       {
-        const uint32_t t = sbuf - 1;  // the item's last PV
-        if (!wait_role(ODONE0 + 8u * (t & 1), (t >> 1) & 1, abort_flag)) {
+        const uint32_t tp = t - 1;  // the item's last PV
+        if (!wait_role(ODONE0 + 8u * (tp % C::NP), (tp / C::NP) & 1, abort_flag)) {
           ok = false;
           break;
         }
       }
       tc_fence_after();
-      // the next item's first PV waits for QREADY, which every thread signals
-      // only after this read of O
+      // the next item's first PV needs P of its first tile, which this
+      // warpgroup writes only after this read of O
       store_state<D>(tl + C::T_O, valid ? ws_rec(p, I.s, I.g, I.split, row, D) : nullptr, hf, m, lh);
     }
     if (!ok) set_status(p.status, TV_ERR_TIMEOUT);
@@ -553,8 +613,9 @@ __global__ void __launch_bounds__(256, 1) attn_tail_kernel(const __grid_constant
   const uint32_t raw = smem_u32(smem_raw);
   const uint32_t sb = (raw + 1023u) & ~1023u;
   uint8_t* gb = smem_raw + (sb - raw);
-  const uint32_t BAR = sb + 2 * C::TILE, DRAIN = BAR + 8;
-  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(gb + 2 * C::TILE + 16);
+  const uint32_t pbase = sb + 2 * C::TILE;  // P tile (the PV A operand)
+  const uint32_t BAR = pbase + C::PTILE, DRAIN = BAR + 8;
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(gb + 2 * C::TILE + C::PTILE + 16);
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int hf = warp >> 2;  // softmax half of this thread
   const int lrow = (warp & 3) * 32 + lane;
@@ -740,15 +801,16 @@ __global__ void __launch_bounds__(256, 1) attn_tail_kernel(const __grid_constant
       const float rs = half_probs(sv, nvalid, p.c, m_new, Pw);
       lh = __fmaf_rn(lh, alpha, rs);
       m = m_new;
-      tmem_st16(tl + C::T_S + hf * (kHalf / 2), Pw);
+      store_p_half(pbase, lrow, hf, Pw);
       if (!fresh && __any_sync(0xffffffffu, alpha != 1.f))
         rescale_o(tl + C::T_O, hf * (D / 2), (hf + 1) * (D / 2), alpha);
       tmem_st_wait();
+      fence_proxy_async_smem();  // P visible to the tensor core
       tc_fence_before();
       __syncthreads();
       tc_fence_after();
       if (threadIdx.x == 0) {
-        issue_pv<D>(tbase + C::T_O, tbase + C::T_S, sb + C::TILE, !fresh);
+        issue_pv_ss<D>(tbase + C::T_O, pbase, desc_v(sb + C::TILE, 0), !fresh);
         tc_commit(BAR);
       }
       if (__syncthreads_or(!mbar_wait(BAR, ph, kWaitCycles))) {
@@ -937,7 +999,7 @@ static tv_status launch_tc(const TcParams& p, int n_items_bound, int n_tail, cud
   }
   if (n_items_bound > 0) {
     const int grid = n_items_bound < num_sms() ? n_items_bound : num_sms();
-    attn_split_kernel<D><<<grid, 352, C::SMEM_SPLIT, st>>>(p);
+    attn_split_kernel<D><<<grid, 384, C::SMEM_SPLIT, st>>>(p);
   }
   attn_tail_kernel<D><<<n_tail, 256, C::SMEM_TAIL, st>>>(p);
   return launch_status();
