@@ -1,27 +1,26 @@
 // Gated DeltaNet tree verify and single-token decode.
 //
 // Tree verify ("Adding a model", Gated DeltaNet layers; the gated delta rule
-// applied along every node's root path): one CTA owns 16 state rows of one
-// value head of one sequence and walks the tree in the order prepared by
-// tv_tree_prepare.  A lane group of LPR lanes holds two state rows (the
-// token's key and query are read once for both, and the two rows give two
-// independent dependency chains); the few states that must outlive a subtree
-// sit in shared-memory slots.  No per-node state is written to memory: the
-// kernel reads the committed state once and writes one output value per
-// (node, row).
+// applied along every node's root path): one warp (one CTA) owns 4 * 32/LPR
+// state rows of one value head of one sequence and walks the tree in the
+// order prepared by tv_tree_prepare.  A lane group of LPR lanes holds four
+// state rows, so each node's key and query, read once from shared memory (as
+// bf16), serve four rows, and the eight dot products of a step (s.k and s.q
+// of each row) are reduced together by one reduce-scatter.  The few states
+// that must outlive a subtree sit in shared-memory slots.  No per-node state
+// is written to memory: the kernel reads the committed state once and writes
+// one output value per (node, row).
 //
-// Work per (node, row): two dot products of length dk (s.k, s.q) and, for
-// nodes with children, one rank-1 update of the row, in packed fp32x2
-// arithmetic.  The kernel is bound by latency and shared-memory bandwidth,
-// not by the 4 * Hv * dv * dk bytes of state it reads.
+// Work per (node, row): two dot products of length dk and, for nodes with
+// children, one rank-1 update of the row, in packed fp32x2 arithmetic.  The
+// kernel is bound by the dependent chain of steps along the tree, not by the
+// 4 * Hv * dv * dk bytes of state it reads.
 #include "common.cuh"
 #include "gdn_step.cuh"
 #include "host.hpp"
 #include "launchers.hpp"
 
 namespace tv {
-
-constexpr int kGdnThreads = 64;
 
 struct GdnVerifyParams {
   float* S[TV_MAX_SEQ];
@@ -47,145 +46,136 @@ inline int slots_for(int n_max) {
 
 template <int LPR>
 struct GdnShape {
-  static constexpr int DK = 16 * LPR;           // key dim
-  static constexpr int NG = kGdnThreads / LPR;  // lane groups per CTA
-  static constexpr int R = 2 * NG;              // state rows per CTA (two per group)
+  static constexpr int DK = 16 * LPR;  // key dim
+  static constexpr int NG = 32 / LPR;  // lane groups per warp
+  static constexpr int RPG = 4;        // state rows per lane group
+  static constexpr int R = NG * RPG;   // state rows per CTA
+  static constexpr int NV = 2 * RPG;   // dot products per step and group (s.k, s.q per row)
 };
 
-template <int LPR>
+// Shared memory: slots [n_slots][R][DK] f32 | keys, queries [n_max][DK] T |
+// (alpha, beta, k.q, -) [n_max] | v [n_max][R] f32 | schedule [n_max].
+template <typename T, int LPR>
 inline size_t gdn_verify_smem(int n_max, int n_slots) {
   using Sh = GdnShape<LPR>;
   const size_t n = static_cast<size_t>(n_max);
-  return (2 * n * Sh::DK + 4 * n + n * Sh::R + static_cast<size_t>(n_slots) * Sh::R * Sh::DK) * 4 + 4 * n;
+  size_t b = static_cast<size_t>(n_slots) * Sh::R * Sh::DK * 4;
+  b += 2 * ((n * Sh::DK * sizeof(T) + 15) / 16 * 16);
+  b += n * 16 + n * Sh::R * 4 + n * 4;
+  return b;
 }
 
-// Stage the tree's keys and queries (this CTA's key head, fp32), the values at
-// this CTA's rows, alpha and beta of this value head and the traversal.
-// Every load of a thread is issued before any of them is used.
-template <typename T, int DK, int R>
-__device__ __forceinline__ void stage_node_inputs(const GdnVerifyParams& p, const MetaView& mv, int n, int off, int g,
-                                                  int h, int rb, float* kb, float* qb, float4* nc, float* vb,
-                                                  int* sch) {
-  constexpr int EPL = 16 / sizeof(T);  // elements per 16-byte load
-  constexpr int CPR = DK / EPL;        // 16-byte chunks per key row
-  const T* q = static_cast<const T*>(p.q);
-  const T* k = static_cast<const T*>(p.k);
-  const T* v = static_cast<const T*>(p.v);
-  const int nchunks = n * CPR;
-  for (int base = threadIdx.x; base < nchunks; base += 4 * blockDim.x) {
-    uint4 kv[4], qv[4];
-#pragma unroll
-    for (int u = 0; u < 4; u++) {
-      const int idx = base + u * blockDim.x;
-      if (idx < nchunks) {
-        const size_t src = (static_cast<size_t>(off + idx / CPR) * p.Hk + g) * DK + (idx % CPR) * EPL;
-        kv[u] = *reinterpret_cast<const uint4*>(k + src);
-        qv[u] = *reinterpret_cast<const uint4*>(q + src);
-      }
-    }
-#pragma unroll
-    for (int u = 0; u < 4; u++) {
-      const int idx = base + u * blockDim.x;
-      if (idx < nchunks) {
-        const T* ke = reinterpret_cast<const T*>(&kv[u]);
-        const T* qe = reinterpret_cast<const T*>(&qv[u]);
-        float* kd = kb + (idx / CPR) * DK + (idx % CPR) * EPL;
-        float* qd = qb + (idx / CPR) * DK + (idx % CPR) * EPL;
-#pragma unroll
-        for (int e = 0; e < EPL; e++) {
-          kd[e] = to_f32(ke[e]);
-          qd[e] = to_f32(qe[e]);
-        }
-      }
-    }
-  }
-  for (int base = threadIdx.x; base < n * R; base += 4 * blockDim.x) {
-    float vv[4];
-#pragma unroll
-    for (int u = 0; u < 4; u++) {
-      const int idx = base + u * blockDim.x;
-      const int row = rb * R + idx % R;
-      vv[u] = (idx < n * R && row < p.dv)
-                  ? to_f32(v[(static_cast<size_t>(off + idx / R) * p.Hv + h) * p.dv + row])
-                  : 0.f;
-    }
-#pragma unroll
-    for (int u = 0; u < 4; u++)
-      if (base + u * blockDim.x < n * R) vb[base + u * blockDim.x] = vv[u];
-  }
-  for (int idx = threadIdx.x; idx < n; idx += blockDim.x) {
-    const size_t ah = static_cast<size_t>(off + idx) * p.Hv + h;
-    const float a = p.alpha[ah], b = p.beta[ah];
-    sch[idx] = mv.sched[off + idx];
-    nc[idx] = make_float4(a, b, 0.f, 0.f);
-  }
+__device__ __forceinline__ void cp_async16_g(void* dst, const void* src) {
+  asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(static_cast<uint32_t>(__cvta_generic_to_shared(dst))), "l"(src) : "memory");
 }
 
 template <typename T, int LPR>
-__global__ void __launch_bounds__(kGdnThreads) gdn_verify_kernel(const GdnVerifyParams p) {
+__global__ void __launch_bounds__(32) gdn_verify_kernel(const GdnVerifyParams p) {
   using Sh = GdnShape<LPR>;
-  constexpr int DK = Sh::DK, NG = Sh::NG, R = Sh::R;
+  constexpr int DK = Sh::DK, R = Sh::R, RPG = Sh::RPG, NV = Sh::NV;
   const int s = blockIdx.y;
   const int rb_per_head = (p.dv + R - 1) / R;
   const int h = blockIdx.x / rb_per_head;
   const int rb = blockIdx.x % rb_per_head;
-  if (status_bad(p.status)) return;
+  const int lane = threadIdx.x, gi = lane / LPR, j = lane % LPR;
+
+  // this group's four state rows first (they do not depend on the tree), so
+  // their loads overlap everything up to the first step
+  f2_t st[RPG][8];
+  bool valid[RPG];
+#pragma unroll
+  for (int r = 0; r < RPG; r++) {
+    const int row = rb * R + gi * RPG + r;
+    valid[r] = row < p.dv;
+    if (valid[r]) {
+      load_row8<LPR>(st[r], p.S[s] + (static_cast<size_t>(h) * p.dv + row) * DK, j);
+    } else {
+#pragma unroll
+      for (int e = 0; e < 8; e++) st[r][e] = 0ull;
+    }
+  }
   MetaView mv = meta_view(const_cast<void*>(p.meta), p.n_total);
   const SeqInfo info = mv.seq[s];
+  if (status_bad(p.status)) return;
   const int n = info.n, off = info.off;
   if (n <= 0 || n > p.n_max) return;
   if (info.max_slot > p.n_slots) {
-    if (threadIdx.x == 0) set_status(p.status, TV_ERR_TREE);
+    if (lane == 0) set_status(p.status, TV_ERR_TREE);
     return;
   }
   const int g = h / (p.Hv / p.Hk);
 
   extern __shared__ float4 smem4[];
-  float* kb = reinterpret_cast<float*>(smem4);                     // [n_max][DK] keys, fp32
-  float* qb = kb + p.n_max * DK;                                   // [n_max][DK] queries
-  float4* nc = reinterpret_cast<float4*>(qb + p.n_max * DK);       // [n_max] (alpha, beta, k.q, -)
-  float* vb = reinterpret_cast<float*>(nc + p.n_max);              // [n_max][R] v at this CTA's rows
-  float* slots = vb + p.n_max * R;                                 // [n_slots][R][DK]
-  int* sch = reinterpret_cast<int*>(slots + p.n_slots * R * DK);   // [n_max] traversal
+  float* slots = reinterpret_cast<float*>(smem4);  // [n_slots][R][DK]
+  T* kb = reinterpret_cast<T*>(slots + static_cast<size_t>(p.n_slots) * R * DK);
+  const size_t kq_bytes = (static_cast<size_t>(p.n_max) * DK * sizeof(T) + 15) / 16 * 16;
+  T* qb = reinterpret_cast<T*>(reinterpret_cast<uint8_t*>(kb) + kq_bytes);
+  float4* nc = reinterpret_cast<float4*>(reinterpret_cast<uint8_t*>(qb) + kq_bytes);  // [n_max]
+  float* vb = reinterpret_cast<float*>(nc + p.n_max);                                // [n_max][R]
+  int* sch = reinterpret_cast<int*>(vb + static_cast<size_t>(p.n_max) * R);          // [n_max]
 
-  // this group's two state rows first, so their loads overlap the staging
-  const int gi = threadIdx.x / LPR, j = threadIdx.x % LPR;
-  const int r0 = gi, r1 = gi + NG;
-  const int row0 = rb * R + r0, row1 = rb * R + r1;
-  const bool valid0 = row0 < p.dv, valid1 = row1 < p.dv;
-  f2_t s0[8], s1[8];
-  if (valid0) {
-    load_row8<LPR>(s0, p.S[s] + (static_cast<size_t>(h) * p.dv + row0) * DK, j);
-  } else {
-#pragma unroll
-    for (int e = 0; e < 8; e++) s0[e] = 0ull;
-  }
-  if (valid1) {
-    load_row8<LPR>(s1, p.S[s] + (static_cast<size_t>(h) * p.dv + row1) * DK, j);
-  } else {
-#pragma unroll
-    for (int e = 0; e < 8; e++) s1[e] = 0ull;
-  }
-  stage_node_inputs<T, DK, R>(p, mv, n, off, g, h, rb, kb, qb, nc, vb, sch);
-  __syncthreads();
-  // k . q of every node, one lane group per node.  Every group runs every
-  // round (the lane reduction needs all lanes of the warp); a group past the
-  // last node reduces zeros and writes nothing.
-  for (int base = 0; base < n; base += NG) {
-    const int node = base + gi;
-    const bool act = node < n;
-    f2_t k[8], q[8];
-    if (act) {
-      load_row8<LPR>(k, kb + node * DK, j);
-      load_row8<LPR>(q, qb + node * DK, j);
-    } else {
-#pragma unroll
-      for (int e = 0; e < 8; e++) k[e] = q[e] = 0ull;
+  // stage the tree's keys and queries of this key head (raw, asynchronously),
+  // then the values of this CTA's rows, alpha, beta and the traversal, with
+  // every load issued before any is used
+  {
+    constexpr int CPR = DK * static_cast<int>(sizeof(T)) / 16;  // 16-byte chunks per key row
+    const T* qg = static_cast<const T*>(p.q);
+    const T* kg = static_cast<const T*>(p.k);
+    for (int idx = lane; idx < n * CPR; idx += 32) {
+      const size_t src = (static_cast<size_t>(off + idx / CPR) * p.Hk + g) * DK + (idx % CPR) * (16 / sizeof(T));
+      cp_async16_g(kb + static_cast<size_t>(idx / CPR) * DK + (idx % CPR) * (16 / sizeof(T)), kg + src);
+      cp_async16_g(qb + static_cast<size_t>(idx / CPR) * DK + (idx % CPR) * (16 / sizeof(T)), qg + src);
     }
-    const float kq = kq_group<LPR>(k, q);
-    if (act && j == 0) nc[node].z = kq;
+    asm volatile("cp.async.commit_group;" ::: "memory");
+    const T* vg = static_cast<const T*>(p.v);
+    for (int base = lane; base < n * R; base += 16 * 32) {
+      float vv[16];
+#pragma unroll
+      for (int u = 0; u < 16; u++) {
+        const int idx = base + u * 32;
+        const int row = rb * R + idx % R;
+        vv[u] = (idx < n * R && row < p.dv)
+                    ? to_f32(vg[(static_cast<size_t>(off + idx / R) * p.Hv + h) * p.dv + row])
+                    : 0.f;
+      }
+#pragma unroll
+      for (int u = 0; u < 16; u++)
+        if (base + u * 32 < n * R) vb[base + u * 32] = vv[u];
+    }
+    for (int idx = lane; idx < n; idx += 32) {
+      const size_t ah = static_cast<size_t>(off + idx) * p.Hv + h;
+      const float a = p.alpha[ah], b = p.beta[ah];
+      sch[idx] = mv.sched[off + idx];
+      nc[idx] = make_float4(a, b, 0.f, 0.f);
+    }
+    asm volatile("cp.async.wait_all;" ::: "memory");
+    __syncwarp();
   }
-  __syncthreads();
+  // k . q of every node: each group takes eight nodes at a time, and one
+  // reduce-scatter finishes all of them
+  for (int base = 0; base < n; base += 8 * Sh::NG) {
+    float part[8];
+#pragma unroll
+    for (int m = 0; m < 8; m++) {
+      const int node = base + gi * 8 + m;
+      part[m] = 0.f;
+      if (node < n) {
+        f2_t kk[8], qq[8];
+        load_row8_any<LPR>(kk, kb + static_cast<size_t>(node) * DK, j);
+        load_row8_any<LPR>(qq, qb + static_cast<size_t>(node) * DK, j);
+        part[m] = row_partial(kk, qq);
+      }
+    }
+    reduce_scatter<LPR, 8>(part, j);
+#pragma unroll
+    for (int i = 0; i < rs_count<LPR, 8>(); i++) {
+      const int m = rs_value<LPR, 8>(j, i);
+      const int node = base + gi * 8 + m;
+      const bool writer = rs_first<LPR, 8>(j);
+      if (writer && node < n) nc[node].z = part[i];
+    }
+  }
+  __syncwarp();
 
   T* out = static_cast<T*>(p.out);
   for (int step = 0; step < n; step++) {
@@ -193,25 +183,53 @@ __global__ void __launch_bounds__(kGdnThreads) gdn_verify_kernel(const GdnVerify
     const int node = e & 0xFF, src = (e >> 8) & 0xFF, save = (e >> 16) & 0xFF;
     const bool has_children = (e >> 24) & 1;
     if (src) {
-      load_row8<LPR>(s0, slots + ((src - 1) * R + r0) * DK, j);
-      load_row8<LPR>(s1, slots + ((src - 1) * R + r1) * DK, j);
+#pragma unroll
+      for (int r = 0; r < RPG; r++) load_row8<LPR>(st[r], slots + ((src - 1) * R + gi * RPG + r) * DK, j);
     }
     f2_t k[8], q[8];
-    load_row8<LPR>(k, kb + node * DK, j);
-    load_row8<LPR>(q, qb + node * DK, j);
+    load_row8_any<LPR>(k, kb + static_cast<size_t>(node) * DK, j);
+    load_row8_any<LPR>(q, qb + static_cast<size_t>(node) * DK, j);
     const float4 c4 = nc[node];
-    const float o0 =
-        gdn_row_step<LPR, true>(s0, k, q, c4.z, vb[node * R + r0], c4.x, c4.y, p.scale, has_children);
-    const float o1 =
-        gdn_row_step<LPR, true>(s1, k, q, c4.z, vb[node * R + r1], c4.x, c4.y, p.scale, has_children);
-    if (save) {
-      store_row8<LPR>(slots + ((save - 1) * R + r0) * DK, s0, j);
-      store_row8<LPR>(slots + ((save - 1) * R + r1) * DK, s1, j);
+    float part[NV];
+#pragma unroll
+    for (int r = 0; r < RPG; r++) {
+      part[2 * r] = row_partial(st[r], k);
+      part[2 * r + 1] = row_partial(st[r], q);
     }
-    if (j == 0) {
-      T* orow = out + (static_cast<size_t>(off + node) * p.Hv + h) * p.dv;
-      if (valid0) orow[row0] = from_f32<T>(o0);
-      if (valid1) orow[row1] = from_f32<T>(o1);
+    reduce_scatter<LPR, NV>(part, j);
+    float c[RPG];
+#pragma unroll
+    for (int r = 0; r < RPG; r++) {
+      const float x = __shfl_sync(0xffffffffu, part[rs_index<LPR, NV>(2 * r)], rs_lane<LPR, NV>(2 * r), LPR);
+      c[r] = gdn_c(x, vb[node * R + gi * RPG + r], c4.x, c4.y);
+    }
+    // one lane holding y of a row writes that row's output
+#pragma unroll
+    for (int i = 0; i < rs_count<LPR, NV>(); i++) {
+      const int m = rs_value<LPR, NV>(j, i);
+      const bool writer = rs_first<LPR, NV>(j);
+      if (writer && (m & 1)) {
+        const int r = m >> 1;
+        float cr = c[0];
+#pragma unroll
+        for (int rr = 1; rr < RPG; rr++)
+          if (rr == r) cr = c[rr];
+        bool vr = valid[0];
+#pragma unroll
+        for (int rr = 1; rr < RPG; rr++)
+          if (rr == r) vr = valid[rr];
+        if (vr)
+          out[(static_cast<size_t>(off + node) * p.Hv + h) * p.dv + rb * R + gi * RPG + r] =
+              from_f32<T>(gdn_o(cr, c4.z, c4.x, part[i], p.scale));
+      }
+    }
+    if (has_children) {
+#pragma unroll
+      for (int r = 0; r < RPG; r++) gdn_update(st[r], k, c4.x, c[r]);
+    }
+    if (save) {
+#pragma unroll
+      for (int r = 0; r < RPG; r++) store_row8<LPR>(slots + ((save - 1) * R + gi * RPG + r) * DK, st[r], j);
     }
   }
 }
@@ -283,12 +301,12 @@ static void launch_verify(const GdnVerifyParams& p, int n_seq, cudaStream_t st) 
   constexpr int R = GdnShape<LPR>::R;
   static bool attrs = false;  // one-time, sized for the largest tree
   if (!attrs) {
-    const int smem_max = static_cast<int>(gdn_verify_smem<LPR>(TV_MAX_NODES, slots_for(TV_MAX_NODES)));
+    const int smem_max = static_cast<int>(gdn_verify_smem<T, LPR>(TV_MAX_NODES, slots_for(TV_MAX_NODES)));
     cudaFuncSetAttribute(gdn_verify_kernel<T, LPR>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem_max);
     attrs = true;
   }
   const dim3 grid(p.Hv * ((p.dv + R - 1) / R), n_seq);
-  gdn_verify_kernel<T, LPR><<<grid, kGdnThreads, gdn_verify_smem<LPR>(p.n_max, p.n_slots), st>>>(p);
+  gdn_verify_kernel<T, LPR><<<grid, 32, gdn_verify_smem<T, LPR>(p.n_max, p.n_slots), st>>>(p);
 }
 
 template <typename T, int LPR>
