@@ -74,7 +74,9 @@ struct Tc {
   static constexpr int RING = (NK + NV) * TILE + NP * PTILE;
   static constexpr int NBAR = 2 * (NK + NV) + 2 * NP + 9;
   static constexpr int SMEM_SPLIT = 1024 + RING + NBAR * 8 + 16;
-  static constexpr int SMEM_TAIL = 1024 + 2 * TILE + PTILE + 16 + 16;
+  // tail kernel: tiles, P, barriers, then (sized at launch) the staged
+  // partial states of the splits the split kernel finished
+  static constexpr int TAIL_FIXED = 1024 + 2 * TILE + PTILE + 1024;
   static constexpr int REC = D + 4;  // workspace record: O[D], m, l_A, l_B, pad
 };
 
@@ -93,6 +95,7 @@ struct TcParams {
   int32_t* status;
   float* ws;
   int n_seq, n_total, Hq, Hkv, G, cap, max_len, split_tiles, max_splits, rows_max, decode;
+  int n_mstage;  // tail kernel: finished splits whose states are staged in shared memory
   float c;  // scale * log2(e)
 };
 
@@ -614,7 +617,7 @@ __global__ void __launch_bounds__(256, 1) attn_tail_kernel(const __grid_constant
   const uint32_t sb = (raw + 1023u) & ~1023u;
   uint8_t* gb = smem_raw + (sb - raw);
   const uint32_t pbase = sb + 2 * C::TILE;  // P tile (the PV A operand)
-  const uint32_t BAR = pbase + C::PTILE, DRAIN = BAR + 8;
+  const uint32_t BAR = pbase + C::PTILE, DRAIN = BAR + 8, MBAR = BAR + 16;
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(gb + 2 * C::TILE + C::PTILE + 16);
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int hf = warp >> 2;  // softmax half of this thread
@@ -622,27 +625,42 @@ __global__ void __launch_bounds__(256, 1) attn_tail_kernel(const __grid_constant
   const int item = blockIdx.x;
   const int g = item % p.Hkv;
   const int node_g = item / p.Hkv;  // global node (verify) or sequence (decode)
-  int s = 0, off = 0, depth = 0;
-  const int8_t* anc = nullptr;
+  // the node's sequence, offset, depth, ancestors and context length, with
+  // every global load issued before any result is used
+  int s = 0, off = 0, depth = 0, L = 0;
   if (p.decode) {
     s = node_g;
     off = node_g;
+    L = p.len[s];
+    if (threadIdx.x < TV_MAX_PATH) anc_s[threadIdx.x] = node_g;
   } else {
-    while (s < p.n_seq - 1 && node_g >= p.node_off[s + 1]) s++;
-    off = p.node_off[s];
+    int ends[TV_MAX_SEQ], lens[TV_MAX_SEQ];
+#pragma unroll
+    for (int i = 0; i < TV_MAX_SEQ; i++) {
+      ends[i] = i < p.n_seq ? p.node_off[i + 1] : 0;
+      lens[i] = i < p.n_seq ? p.len[i] : 0;
+    }
+    const int off0 = p.node_off[0];
     MetaView mv = meta_view(const_cast<void*>(p.meta), p.n_total);
     depth = mv.depth[node_g];
-    anc = mv.anc_at + static_cast<size_t>(node_g) * TV_MAX_PATH;
+    const int a = threadIdx.x < TV_MAX_PATH ? mv.anc_at[static_cast<size_t>(node_g) * TV_MAX_PATH + threadIdx.x] : 0;
+    off = off0;
+    L = lens[0];
+#pragma unroll
+    for (int i = 0; i + 1 < TV_MAX_SEQ; i++) {
+      if (i + 1 < p.n_seq && node_g >= ends[i]) {
+        s = i + 1;
+        off = ends[i];
+        L = lens[i + 1];
+      }
+    }
+    if (threadIdx.x < TV_MAX_PATH) anc_s[threadIdx.x] = threadIdx.x > depth ? node_g : off + a;
   }
   const int local = node_g - off;
-  const int L = p.len[s];
-  if (threadIdx.x < TV_MAX_PATH) {
-    const int a = p.decode ? -1 : anc[threadIdx.x];  // the ancestor row, read whole
-    anc_s[threadIdx.x] = (p.decode || threadIdx.x > depth) ? node_g : off + a;
-  }
   if (threadIdx.x == 0) {
     mbar_init(BAR, 1);
     mbar_init(DRAIN, 1);
+    mbar_init(MBAR, 1);
     fence_mbar_init();
     int bad = status_bad(p.status) ? 1 : 0;
     if (!bad && (L < 0 || L > p.max_len)) {
@@ -738,6 +756,22 @@ __global__ void __launch_bounds__(256, 1) attn_tail_kernel(const __grid_constant
     tc_fence_before();
     __syncthreads();
     tc_fence_after();
+    // The finished splits' states (the node's G rows of a split are one
+    // contiguous block) come in by bulk copies issued now, so their latency
+    // hides behind the node's own tiles; the node's final split state is
+    // kept in shared memory too.  Shared layout: [nst][G][REC], then [G][REC].
+    const uint32_t mst_s = sb + (C::TAIL_FIXED - 1024);
+    const int nst = min(cur, p.n_mstage);
+    const uint32_t mown_s = mst_s + static_cast<uint32_t>(nst * G * C::REC * 4);
+    float* const mown = reinterpret_cast<float*>(gb + (C::TAIL_FIXED - 1024) + nst * G * C::REC * 4);
+    if (warp == 0 && nst > 0) {
+      // one lane sets the byte count first; the copies are spread over the warp
+      const uint32_t bytes = static_cast<uint32_t>(G * C::REC * 4);
+      if (lane == 0) mbar_arrive_expect_tx(MBAR, bytes * nst);
+      __syncwarp();
+      for (int sp = lane; sp < nst; sp += 32)
+        bulk_g2s(mst_s + sp * bytes, ws_rec(p, s, g, sp, local * G, D), bytes, MBAR);
+    }
 
     uint32_t ph = 0;
     bool ok = true;
@@ -821,14 +855,30 @@ __global__ void __launch_bounds__(256, 1) attn_tail_kernel(const __grid_constant
       tc_fence_after();
       fresh = false;
     }
+    // the staged splits have landed (every thread observes the barrier, and
+    // no copy is in flight when the CTA leaves, whatever happened before)
+    if (__syncthreads_or(nst > 0 && !mbar_wait(MBAR, 0, kWaitCycles))) ok = false;
     if (!ok) {
       set_status(p.status, TV_ERR_TIMEOUT);
     } else {
-      store_state<D>(tl + C::T_O, vrow ? ws_rec(p, s, g, cur, row_seq, D) : nullptr, hf, m, lh);
+      store_state<D>(tl + C::T_O, vrow ? mown + lrow * C::REC : nullptr, hf, m, lh);
       __syncthreads();
       // merge splits 0..cur in split order: weights 2^(m_s - max m), sums l_A + l_B
       const int ns = cur + 1;
-      const size_t sstride = static_cast<size_t>(p.rows_max) * C::REC;
+      // O columns 4*c4 .. 4*c4+3 and (m, l_A, l_B) of split sp, row r
+      auto rec4 = [&](int sp, int r, int c4) -> float4 {
+        float4 v;
+        if (sp < nst || sp == cur) {
+          const uint32_t a = (sp < nst ? mst_s + static_cast<uint32_t>((sp * G + r) * C::REC * 4)
+                                       : mown_s + static_cast<uint32_t>(r * C::REC * 4)) + 16u * c4;
+          asm volatile("ld.shared.v4.f32 {%0, %1, %2, %3}, [%4];"
+                       : "=f"(v.x), "=f"(v.y), "=f"(v.z), "=f"(v.w)
+                       : "r"(a));
+        } else {
+          v = reinterpret_cast<const float4*>(ws_rec(p, s, g, sp, local * G + r, D))[c4];
+        }
+        return v;
+      };
       float* wsm = reinterpret_cast<float*>(gb);                 // [ns][G] weights (tile area is free now)
       float* ltot = wsm + static_cast<size_t>(ns) * G;           // [G]
       const bool wstaged = (2 * static_cast<size_t>(ns) * G + 2 * G) * 4 <= 2 * C::TILE;
@@ -841,10 +891,10 @@ __global__ void __launch_bounds__(256, 1) attn_tail_kernel(const __grid_constant
           for (int u = 0; u < 4; u++) {
             const int idx = base + u * blockDim.x;
             if (idx < ns * G) {
-              const float* rec = ws_rec(p, s, g, idx / G, local * G + idx % G, D);
-              mv4[u] = rec[D];
-              la[u] = rec[D + 1];
-              lb[u] = rec[D + 2];
+              const float4 t4 = rec4(idx / G, idx % G, D / 4);  // m, l_A, l_B, pad
+              mv4[u] = t4.x;
+              la[u] = t4.y;
+              lb[u] = t4.z;
             }
           }
 #pragma unroll
@@ -879,22 +929,21 @@ __global__ void __launch_bounds__(256, 1) attn_tail_kernel(const __grid_constant
       }
       for (int idx = threadIdx.x; idx < G * (D / 4); idx += blockDim.x) {
         const int r = idx / (D / 4), c4 = idx % (D / 4);
-        const float* rec0 = ws_rec(p, s, g, 0, local * G + r, D);
         float mm = 0.f, ls = 0.f;
         if (!wstaged) {
           mm = -INFINITY;
-          for (int sp = 0; sp < ns; sp++) mm = fmaxf(mm, rec0[sp * sstride + D]);
+          for (int sp = 0; sp < ns; sp++) mm = fmaxf(mm, rec4(sp, r, D / 4).x);
         }
         float4 o = make_float4(0.f, 0.f, 0.f, 0.f);
         if (wstaged) {
-          // 8 splits' partial rows in flight at a time, accumulated in split order
-          for (int sp0 = 0; sp0 < ns; sp0 += 8) {
-            float4 v[8];
+          // up to 16 splits' partial rows in flight at a time, accumulated in split order
+          for (int sp0 = 0; sp0 < ns; sp0 += 16) {
+            float4 v[16];
 #pragma unroll
-            for (int u = 0; u < 8; u++)
-              if (sp0 + u < ns) v[u] = reinterpret_cast<const float4*>(rec0 + (sp0 + u) * sstride)[c4];
+            for (int u = 0; u < 16; u++)
+              if (sp0 + u < ns) v[u] = rec4(sp0 + u, r, c4);
 #pragma unroll
-            for (int u = 0; u < 8; u++) {
+            for (int u = 0; u < 16; u++) {
               if (sp0 + u < ns) {
                 const float wgt = wsm[(sp0 + u) * G + r];
                 o.x = __fmaf_rn(wgt, v[u].x, o.x);
@@ -907,11 +956,11 @@ __global__ void __launch_bounds__(256, 1) attn_tail_kernel(const __grid_constant
           ls = ltot[r];
         } else {
           for (int sp = 0; sp < ns; sp++) {
-            const float* rec = rec0 + sp * sstride;
-            const float ms = rec[D];
+            const float4 t4 = rec4(sp, r, D / 4);
+            const float ms = t4.x;
             const float wgt = (ms == mm) ? 1.f : ex2_approx(__fsub_rn(ms, mm));
-            ls = __fmaf_rn(wgt, __fadd_rn(rec[D + 1], rec[D + 2]), ls);
-            const float4 v = reinterpret_cast<const float4*>(rec)[c4];
+            ls = __fmaf_rn(wgt, __fadd_rn(t4.y, t4.z), ls);
+            const float4 v = rec4(sp, r, c4);
             o.x = __fmaf_rn(wgt, v.x, o.x);
             o.y = __fmaf_rn(wgt, v.y, o.y);
             o.z = __fmaf_rn(wgt, v.z, o.z);
@@ -984,15 +1033,25 @@ size_t attn_tc_ws_bytes(const tv_plan* plan, const tv_attn_layer* layer, int n_s
   return static_cast<size_t>(n_seq) * layer->Hkv * splits * static_cast<size_t>(n_max) * G * (layer->D + 4) * 4;
 }
 
+// Dynamic shared memory the tail kernel may use (the per-block limit less
+// its static arrays, with a margin).
+constexpr int kTailSmemMax = 232448 - 2048;
+
 template <int D>
-static tv_status launch_tc(const TcParams& p, int n_items_bound, int n_tail, cudaStream_t st) {
+static tv_status launch_tc(TcParams& p, int n_items_bound, int n_tail, cudaStream_t st) {
   using C = Tc<D>;
+  // stage as many finished splits' states as fit next to the tail's tiles
+  const int per_split = p.G * C::REC * 4;
+  const int fit = (kTailSmemMax - C::TAIL_FIXED) / per_split - 1;  // less the node's own final split
+  if (fit < 0) return TV_ERR_SHAPE;
+  p.n_mstage = fit < p.max_splits ? fit : p.max_splits;
+  const int smem_tail = C::TAIL_FIXED + (p.n_mstage + 1) * per_split;
   // one-time attribute setup (never inside a stream capture after the first call)
   static bool attrs = false;
   if (!attrs) {
     if (cudaFuncSetAttribute(attn_split_kernel<D>, cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM_SPLIT) !=
             cudaSuccess ||
-        cudaFuncSetAttribute(attn_tail_kernel<D>, cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM_TAIL) !=
+        cudaFuncSetAttribute(attn_tail_kernel<D>, cudaFuncAttributeMaxDynamicSharedMemorySize, kTailSmemMax) !=
             cudaSuccess)
       return TV_ERR_CUDA;
     attrs = true;
@@ -1001,7 +1060,7 @@ static tv_status launch_tc(const TcParams& p, int n_items_bound, int n_tail, cud
     const int grid = n_items_bound < num_sms() ? n_items_bound : num_sms();
     attn_split_kernel<D><<<grid, 384, C::SMEM_SPLIT, st>>>(p);
   }
-  attn_tail_kernel<D><<<n_tail, 256, C::SMEM_TAIL, st>>>(p);
+  attn_tail_kernel<D><<<n_tail, 256, smem_tail, st>>>(p);
   return launch_status();
 }
 
