@@ -100,7 +100,23 @@ typedef struct {
   const int32_t* parent;   /* device [n_total], sequence-local parent, -1 at the root */
   void* meta;              /* device, tv_tree_meta_bytes() bytes: derived tables (private layout) */
   int32_t* status;         /* device [1] error word, 0 = ok; shared by the calls of a round */
+  int32_t flags;           /* TV_TREE_* bits (host), 0 by default */
 } tv_tree;
+
+/* TV_TREE_OVERLAP: the calls that take this tree launch their kernels with
+ * programmatic dependent launch, so that a kernel can start (shared- and
+ * tensor-memory setup, loads of the recurrent state, L2 prefetch of its first
+ * KV tiles) while the kernel before it on the stream finishes; the next
+ * kernel is let in only after a kernel's own wait for its predecessor has
+ * returned (at its start for the attention split kernel, at exit elsewhere),
+ * so everything older than the predecessor has completed.  Before waiting, a
+ * kernel reads only the recurrent states (GDN verify), the lengths and
+ * node_off (attention), and the tree tables (the attention tail, whose
+ * predecessor is always its own split kernel); no kernel of a verify round
+ * (prepare, per-layer verify, accept, commit, in that order on one stream)
+ * writes these directly before such a read.  The caller must not enqueue its
+ * own kernel that writes them directly before a call with this flag. */
+#define TV_TREE_OVERLAP 1
 /* Every call that takes a tv_tree returns TV_ERR_ARG, enqueueing nothing, when
  * the descriptor is ill formed on the host: NULL, counts out of range, or a
  * NULL or non-16-byte-aligned pointer field. */

@@ -35,7 +35,10 @@ class TvError(RuntimeError):
 
 class tv_tree(ctypes.Structure):
     _fields_ = [("n_seq", c_int32), ("n_total", c_int32), ("n_max", c_int32), ("node_off", c_void_p),
-                ("parent", c_void_p), ("meta", c_void_p), ("status", c_void_p)]
+                ("parent", c_void_p), ("meta", c_void_p), ("status", c_void_p), ("flags", c_int32)]
+
+
+TV_TREE_OVERLAP = 1
 
 
 class tv_attn_layer(ctypes.Structure):
@@ -139,7 +142,7 @@ def _ptr_array(tensors):
 class Tree:
     """Device buffers of a tv_tree for a list of per-sequence parent arrays."""
 
-    def __init__(self, parents, device="cuda", n_max=None):
+    def __init__(self, parents, device="cuda", n_max=None, overlap: bool = False):
         sizes = [len(p) for p in parents]
         off = [0]
         for n in sizes:
@@ -154,7 +157,7 @@ class Tree:
                                 device=device)
         self.status = torch.zeros(4, dtype=torch.int32, device=device)
         self.c = tv_tree(self.n_seq, self.n_total, self.n_max, self.node_off.data_ptr(), self.parent.data_ptr(),
-                         self.meta.data_ptr(), self.status.data_ptr())
+                         self.meta.data_ptr(), self.status.data_ptr(), TV_TREE_OVERLAP if overlap else 0)
 
     def status_code(self) -> int:
         return int(self.status[0].item())

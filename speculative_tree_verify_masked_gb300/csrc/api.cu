@@ -61,7 +61,7 @@ extern "C" tv_status tv_attn_tree_verify(const tv_plan* plan, const tv_attn_laye
   if (max_len < 0 || max_len > l->cap || !(scale > 0.f) || !std::isfinite(scale)) return TV_ERR_ARG;
   if (!aligned16(len) || !aligned16(q) || !aligned16(k_t) || !aligned16(v_t) || !aligned16(out)) return TV_ERR_ALIGN;
   AttnCall c{l, t->n_seq, t->n_total, t->n_max, t->node_off, t->meta, len, max_len, q, k_t, v_t, out, scale,
-             t->status, 0};
+             t->status, 0, tree_overlap(t)};
   cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
   if (l->dtype == TV_F32) return attn_f32_launch(c, st);
   return attn_tc_launch(plan, c, ws, ws_bytes, st);
@@ -80,7 +80,7 @@ extern "C" tv_status tv_decode_step(const tv_plan* plan, const tv_attn_layer* at
   if (ls != TV_OK) return ls;
   if (!len || max_len < 0 || max_len > attn->cap || !(scale > 0.f) || !std::isfinite(scale)) return TV_ERR_ARG;
   if (!aligned16(len) || !aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(out)) return TV_ERR_ALIGN;
-  AttnCall c{attn, n_seq, n_seq, 1, nullptr, nullptr, len, max_len, q, k, v, out, scale, status, 1};
+  AttnCall c{attn, n_seq, n_seq, 1, nullptr, nullptr, len, max_len, q, k, v, out, scale, status, 1, false};
   if (attn->dtype == TV_F32) return attn_f32_launch(c, st);
   return attn_tc_launch(plan, c, ws, ws_bytes, st);
 }

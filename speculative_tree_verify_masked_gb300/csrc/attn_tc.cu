@@ -373,8 +373,7 @@ __global__ void __launch_bounds__(384, 1) attn_split_kernel(const __grid_constan
     mbar_init(DRAIN + 8u, 1);
     *abort_flag = 0;
     fence_mbar_init();
-    skip = status_bad(p.status) ? 1 : 0;
-    item_space(p, is);
+    item_space(p, is);  // lengths and node offsets: not written by the previous kernel of a round
   }
   if (warp == 1) {
     tmem_alloc(smem_u32(tmem_slot), C::COLS);
@@ -385,6 +384,18 @@ __global__ void __launch_bounds__(384, 1) attn_split_kernel(const __grid_constan
   tc_fence_after();
   const uint32_t tbase = *tmem_slot;
   const int total = is.cum[p.n_seq];
+  // L2 prefetch of the first item's first tiles while the previous kernel ends
+  if ((warp == 0 || warp == 10) && lane == 0 && static_cast<int>(blockIdx.x) < total) {
+    const Item I = item_at(is, p, blockIdx.x);
+    const CUtensorMap* map = warp == 0 ? &p.tmK[I.s] : &p.tmV[I.s];
+    for (int t = I.t0; t < min(I.t0 + kPrefetch, I.t1); t++)
+#pragma unroll
+      for (int kb = 0; kb < C::KB; kb++) tma_prefetch_l2_2d(map, kb * 64, I.g * p.cap + t * kTile);
+  }
+  pdl_wait();  // queries, status and the workspace (read by the previous tail) from here on
+  pdl_trigger();
+  if (threadIdx.x == 0) skip = status_bad(p.status) ? 1 : 0;
+  __syncthreads();
 
   if (!skip && (warp == 0 || warp == 10) && lane == 0) {
     // ---------------- TMA producers: warp 0 streams K tiles, warp 10 V tiles ----------------
@@ -657,6 +668,8 @@ __global__ void __launch_bounds__(256, 1) attn_tail_kernel(const __grid_constant
     if (threadIdx.x < TV_MAX_PATH) anc_s[threadIdx.x] = threadIdx.x > depth ? node_g : off + a;
   }
   const int local = node_g - off;
+  // the split kernel before this one writes the workspace and may set the status
+  pdl_wait();
   if (threadIdx.x == 0) {
     mbar_init(BAR, 1);
     mbar_init(DRAIN, 1);
@@ -1038,7 +1051,7 @@ size_t attn_tc_ws_bytes(const tv_plan* plan, const tv_attn_layer* layer, int n_s
 constexpr int kTailSmemMax = 232448 - 2048;
 
 template <int D>
-static tv_status launch_tc(TcParams& p, int n_items_bound, int n_tail, cudaStream_t st) {
+static tv_status launch_tc(TcParams& p, int n_items_bound, int n_tail, cudaStream_t st, bool ov) {
   using C = Tc<D>;
   // stage as many finished splits' states as fit next to the tail's tiles
   const int per_split = p.G * C::REC * 4;
@@ -1058,9 +1071,9 @@ static tv_status launch_tc(TcParams& p, int n_items_bound, int n_tail, cudaStrea
   }
   if (n_items_bound > 0) {
     const int grid = n_items_bound < num_sms() ? n_items_bound : num_sms();
-    attn_split_kernel<D><<<grid, 384, C::SMEM_SPLIT, st>>>(p);
+    launch_k(ov, attn_split_kernel<D>, dim3(grid), dim3(384), C::SMEM_SPLIT, st, p);
   }
-  attn_tail_kernel<D><<<n_tail, 256, smem_tail, st>>>(p);
+  launch_k(ov, attn_tail_kernel<D>, dim3(n_tail), dim3(256), smem_tail, st, p);
   return launch_status();
 }
 
@@ -1111,9 +1124,9 @@ tv_status attn_tc_launch(const tv_plan* plan, const AttnCall& a, void* ws, size_
   const int items_bound = a.n_seq * l->Hkv * splits_bound * ((n_max * G + 127) / 128);
   const int n_tail = (a.decode ? a.n_seq : a.n_total) * l->Hkv;
   switch (l->D) {
-    case 64: return launch_tc<64>(p, items_bound, n_tail, st);
-    case 128: return launch_tc<128>(p, items_bound, n_tail, st);
-    case 256: return launch_tc<256>(p, items_bound, n_tail, st);
+    case 64: return launch_tc<64>(p, items_bound, n_tail, st, a.overlap);
+    case 128: return launch_tc<128>(p, items_bound, n_tail, st, a.overlap);
+    case 256: return launch_tc<256>(p, items_bound, n_tail, st, a.overlap);
     default: return TV_ERR_SHAPE;
   }
 }

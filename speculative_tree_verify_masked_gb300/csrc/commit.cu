@@ -19,6 +19,7 @@ constexpr int kGdnCommitLayers = 32;
 // Capacity and path-length checks for every sequence, before anything is written.
 __global__ void commit_check_kernel(const int32_t* acc_len, const int32_t* len, int32_t* status, int n_seq,
                                     int min_cap) {
+  pdl_wait();
   const int s = threadIdx.x;
   if (s >= n_seq || status_bad(status)) return;
   const int a = acc_len[s], L = len[s];
@@ -43,6 +44,7 @@ struct AttnCommitParams {
 };
 
 __global__ void __launch_bounds__(128) attn_commit_kernel(const AttnCommitParams p) {
+  pdl_wait();
   const int g = blockIdx.x, s = blockIdx.y, li = blockIdx.z;
   if (status_bad(p.status)) return;
   const int a = p.acc_len[s], L = p.len[s];
@@ -80,6 +82,7 @@ struct GdnCommitParams {
 
 template <typename T, int LPR>
 __global__ void __launch_bounds__(128) gdn_commit_kernel(const GdnCommitParams p) {
+  pdl_wait();
   constexpr int DK = 16 * LPR;
   constexpr int R = 128 / LPR;
   const int s = blockIdx.y, li = blockIdx.z;
@@ -132,15 +135,16 @@ __global__ void __launch_bounds__(128) gdn_commit_kernel(const GdnCommitParams p
 }
 
 __global__ void commit_len_kernel(int32_t* len, const int32_t* acc_len, const int32_t* status, int n_seq) {
+  pdl_wait();
   const int s = threadIdx.x;
   if (s < n_seq && !status_bad(status)) len[s] += acc_len[s];
 }
 
 template <typename T, int LPR>
-static void launch_gdn_commit(const GdnCommitParams& p, int n_seq, int nl, cudaStream_t st) {
+static void launch_gdn_commit(const GdnCommitParams& p, int n_seq, int nl, cudaStream_t st, bool ov) {
   constexpr int R = 128 / LPR;
   const dim3 grid(p.Hv * ((p.dv + R - 1) / R), n_seq, nl);
-  gdn_commit_kernel<T, LPR><<<grid, 128, 0, st>>>(p);
+  launch_k(ov, gdn_commit_kernel<T, LPR>, grid, dim3(128), 0, st, p);
 }
 
 }  // namespace tv
@@ -183,7 +187,9 @@ extern "C" tv_status tv_commit_path(const tv_tree* t, const int32_t* path, const
       if (!aligned16(l.S[s])) return TV_ERR_ALIGN;
     }
   }
-  commit_check_kernel<<<1, 32, 0, st>>>(acc_len, len, t->status, n_seq, min_cap);
+  const bool ov = tree_overlap(t);
+  launch_k(ov, commit_check_kernel, dim3(1), dim3(32), 0, st, acc_len, static_cast<const int32_t*>(len), t->status,
+           n_seq, min_cap);
   for (int base = 0; base < n_attn; base += kAttnCommitLayers) {
     const int nl = n_attn - base < kAttnCommitLayers ? n_attn - base : kAttnCommitLayers;
     AttnCommitParams p{};
@@ -207,7 +213,7 @@ extern "C" tv_status tv_commit_path(const tv_tree* t, const int32_t* path, const
     bool same_cap = true;
     for (int i = 0; i < nl; i++) same_cap = same_cap && attn[base + i].cap == p.cap;
     if (!same_cap) return TV_ERR_SHAPE;
-    attn_commit_kernel<<<dim3(p.Hkv, n_seq, nl), 128, 0, st>>>(p);
+    launch_k(ov, attn_commit_kernel, dim3(p.Hkv, n_seq, nl), dim3(128), 0, st, p);
   }
   for (int base = 0; base < n_gdn; base += kGdnCommitLayers) {
     const int nl = n_gdn - base < kGdnCommitLayers ? n_gdn - base : kGdnCommitLayers;
@@ -229,11 +235,12 @@ extern "C" tv_status tv_commit_path(const tv_tree* t, const int32_t* path, const
     p.dv = gdn[0].dv;
     const bool bf = gdn[0].dtype == TV_BF16;
     if (gdn[0].dk == 128) {
-      if (bf) launch_gdn_commit<__nv_bfloat16, 8>(p, n_seq, nl, st); else launch_gdn_commit<float, 8>(p, n_seq, nl, st);
+      if (bf) launch_gdn_commit<__nv_bfloat16, 8>(p, n_seq, nl, st, ov); else launch_gdn_commit<float, 8>(p, n_seq, nl, st, ov);
     } else {
-      if (bf) launch_gdn_commit<__nv_bfloat16, 4>(p, n_seq, nl, st); else launch_gdn_commit<float, 4>(p, n_seq, nl, st);
+      if (bf) launch_gdn_commit<__nv_bfloat16, 4>(p, n_seq, nl, st, ov); else launch_gdn_commit<float, 4>(p, n_seq, nl, st, ov);
     }
   }
-  commit_len_kernel<<<1, 32, 0, st>>>(len, acc_len, t->status, n_seq);
+  launch_k(ov, commit_len_kernel, dim3(1), dim3(32), 0, st, len, acc_len, static_cast<const int32_t*>(t->status),
+           n_seq);
   return launch_status();
 }

@@ -10,6 +10,17 @@
 
 namespace tv {
 
+// Programmatic dependent launch: let the next kernel on the stream start its
+// own set-up, and wait until the previous kernel has finished and its writes
+// are visible.  Both are no-ops for a kernel launched without the attribute.
+// A kernel that never calls pdl_trigger lets the next one start as its
+// blocks exit; only the attention split kernel triggers early (its successor
+// takes one CTA per SM wherever a split CTA has finished, while an early
+// launch of the narrow GDN CTAs would place them unevenly).
+__device__ __forceinline__ void pdl_trigger() { asm volatile("griddepcontrol.launch_dependents;" ::: "memory"); }
+__device__ __forceinline__ void pdl_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+
+
 // A bounded wait gives up after this many SM clocks (about a second).
 constexpr long long kWaitCycles = 1LL << 31;
 

@@ -79,8 +79,9 @@ __global__ void __launch_bounds__(32) gdn_verify_kernel(const GdnVerifyParams p)
   const int rb = blockIdx.x % rb_per_head;
   const int lane = threadIdx.x, gi = lane / LPR, j = lane % LPR;
 
-  // this group's four state rows first (they do not depend on the tree), so
-  // their loads overlap everything up to the first step
+  // this group's four state rows first (they do not depend on the tree, and
+  // no kernel of the round before commit writes them), so their loads overlap
+  // the previous kernel's end and everything up to the first step
   f2_t st[RPG][8];
   bool valid[RPG];
 #pragma unroll
@@ -94,6 +95,7 @@ __global__ void __launch_bounds__(32) gdn_verify_kernel(const GdnVerifyParams p)
       for (int e = 0; e < 8; e++) st[r][e] = 0ull;
     }
   }
+  pdl_wait();  // tree tables, status and node inputs come from earlier kernels
   MetaView mv = meta_view(const_cast<void*>(p.meta), p.n_total);
   const SeqInfo info = mv.seq[s];
   if (status_bad(p.status)) return;
@@ -297,7 +299,7 @@ static bool gdn_shape_ok(const tv_gdn_layer* l) {
 }
 
 template <typename T, int LPR>
-static void launch_verify(const GdnVerifyParams& p, int n_seq, cudaStream_t st) {
+static void launch_verify(const GdnVerifyParams& p, int n_seq, cudaStream_t st, bool ov) {
   constexpr int R = GdnShape<LPR>::R;
   static bool attrs = false;  // one-time, sized for the largest tree
   if (!attrs) {
@@ -306,7 +308,7 @@ static void launch_verify(const GdnVerifyParams& p, int n_seq, cudaStream_t st) 
     attrs = true;
   }
   const dim3 grid(p.Hv * ((p.dv + R - 1) / R), n_seq);
-  gdn_verify_kernel<T, LPR><<<grid, 32, gdn_verify_smem<T, LPR>(p.n_max, p.n_slots), st>>>(p);
+  launch_k(ov, gdn_verify_kernel<T, LPR>, grid, dim3(32), gdn_verify_smem<T, LPR>(p.n_max, p.n_slots), st, p);
 }
 
 template <typename T, int LPR>
@@ -366,10 +368,11 @@ extern "C" tv_status tv_gdn_tree_verify(const tv_gdn_layer* l, const tv_tree* t,
   p.Hk = l->Hk; p.Hv = l->Hv; p.dv = l->dv; p.scale = scale;
   cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
   const bool bf = l->dtype == TV_BF16;
+  const bool ov = tree_overlap(t);
   if (l->dk == 128) {
-    if (bf) launch_verify<__nv_bfloat16, 8>(p, t->n_seq, st); else launch_verify<float, 8>(p, t->n_seq, st);
+    if (bf) launch_verify<__nv_bfloat16, 8>(p, t->n_seq, st, ov); else launch_verify<float, 8>(p, t->n_seq, st, ov);
   } else {
-    if (bf) launch_verify<__nv_bfloat16, 4>(p, t->n_seq, st); else launch_verify<float, 4>(p, t->n_seq, st);
+    if (bf) launch_verify<__nv_bfloat16, 4>(p, t->n_seq, st, ov); else launch_verify<float, 4>(p, t->n_seq, st, ov);
   }
   return launch_status();
 }

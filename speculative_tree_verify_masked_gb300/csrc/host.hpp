@@ -1,6 +1,7 @@
 // Host-side helpers shared by the C-ABI entry points.
 #pragma once
 #include <cstdint>
+#include <utility>
 #include <cuda_runtime.h>
 
 #include "tv.h"
@@ -8,6 +9,29 @@
 namespace tv {
 
 inline bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+// Launch with or without programmatic dependent launch (the kernel may start
+// while the previous kernel on the stream is finishing; it orders itself with
+// griddepcontrol.wait).
+template <typename... KArgs, typename... Args>
+inline void launch_k(bool overlap, void (*kernel)(KArgs...), dim3 grid, dim3 block, size_t smem, cudaStream_t st,
+                     Args&&... args) {
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = grid;
+  cfg.blockDim = block;
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = st;
+  cudaLaunchAttribute attr[1];
+  if (overlap) {
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+  }
+  cudaLaunchKernelEx(&cfg, kernel, std::forward<Args>(args)...);
+}
+
+inline bool tree_overlap(const tv_tree* t) { return t && (t->flags & TV_TREE_OVERLAP) != 0; }
 
 // Status of the launches just enqueued.  Clears a sticky-free launch error
 // so that the next call starts clean.

@@ -25,6 +25,7 @@ struct AttnCall {
   float scale;
   int32_t* status;
   int decode;
+  bool overlap;  // programmatic dependent launch (TV_TREE_OVERLAP)
 };
 
 tv_status attn_f32_launch(const AttnCall& c, cudaStream_t st);

@@ -39,6 +39,7 @@ __device__ __forceinline__ void tree_invalid(MetaView& mv, int s, int off, int32
 __global__ void __launch_bounds__(32) tree_prepare_kernel(const int32_t* __restrict__ node_off,
                                                           const int32_t* __restrict__ parent, void* meta,
                                                           int32_t* status, int n_seq, int n_total, int n_max) {
+  pdl_wait();  // the previous round's calls read the tables this kernel rewrites
   const int s = blockIdx.x;
   const int lane = threadIdx.x;
   __shared__ int par[TV_MAX_NODES], nch[TV_MAX_NODES], nnl[TV_MAX_NODES], size[TV_MAX_NODES];
@@ -170,6 +171,7 @@ __global__ void __launch_bounds__(32) accept_kernel(const int32_t* __restrict__ 
                                                     const int32_t* __restrict__ greedy, const void* meta,
                                                     int n_total, int32_t* path, int32_t* acc_len, int32_t* bonus,
                                                     int32_t* status) {
+  pdl_wait();
   const int s = blockIdx.x;
   const int lane = threadIdx.x;
   int32_t* prow = path + s * TV_MAX_PATH;
@@ -219,8 +221,8 @@ extern "C" size_t tv_tree_meta_bytes(int32_t n_seq, int32_t n_total) {
 
 extern "C" tv_status tv_tree_prepare(const tv_tree* t, tv_stream stream) {
   if (!tree_ok(t)) return TV_ERR_ARG;
-  tree_prepare_kernel<<<t->n_seq, 32, 0, reinterpret_cast<cudaStream_t>(stream)>>>(
-      t->node_off, t->parent, t->meta, t->status, t->n_seq, t->n_total, t->n_max);
+  launch_k(tree_overlap(t), tree_prepare_kernel, dim3(t->n_seq), dim3(32), 0, reinterpret_cast<cudaStream_t>(stream),
+           t->node_off, t->parent, t->meta, t->status, t->n_seq, t->n_total, t->n_max);
   return launch_status();
 }
 
@@ -229,8 +231,8 @@ extern "C" tv_status tv_accept_path(const tv_tree* t, const int32_t* tok, const 
   if (!tree_ok(t) || !tok || !greedy || !path || !acc_len || !bonus) return TV_ERR_ARG;
   if (!aligned16(tok) || !aligned16(greedy) || !aligned16(path) || !aligned16(acc_len) || !aligned16(bonus))
     return TV_ERR_ALIGN;
-  accept_kernel<<<t->n_seq, 32, 0, reinterpret_cast<cudaStream_t>(stream)>>>(tok, greedy, t->meta, t->n_total, path,
-                                                                              acc_len, bonus, t->status);
+  launch_k(tree_overlap(t), accept_kernel, dim3(t->n_seq), dim3(32), 0, reinterpret_cast<cudaStream_t>(stream), tok,
+           greedy, static_cast<const void*>(t->meta), t->n_total, path, acc_len, bonus, t->status);
   return launch_status();
 }
 

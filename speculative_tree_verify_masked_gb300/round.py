@@ -48,7 +48,7 @@ def auto_split(ctx_lens, n_nodes, Hq, Hkv, num_sms, lo=512, hi=16384):
 
 class VerifyRound:
     def __init__(self, cfg: synth.Workload, device="cuda", split: int | None = None, layers=None,
-                 cap_extra: int = 64):
+                 cap_extra: int = 64, overlap: bool = True):
         self.cfg = cfg
         self.device = device
         s = cfg.shapes
@@ -56,7 +56,9 @@ class VerifyRound:
         self.trees = [synth.tree_and_tokens(cfg, q) for q in range(cfg.n_seq)]
         self.parents = [t[0] for t in self.trees]
         self.n_nodes = [len(p) for p in self.parents]
-        self.tree = B.Tree(self.parents, device=device)
+        # the round's calls run in round order on one stream, so each kernel may
+        # start while the one before it finishes (TV_TREE_OVERLAP)
+        self.tree = B.Tree(self.parents, device=device, overlap=overlap)
         self.tok = torch.tensor([x for t in self.trees for x in t[1]], dtype=torch.int32, device=device)
         self.greedy = torch.tensor([x for t in self.trees for x in t[2]], dtype=torch.int32, device=device)
         self.expected_paths = [t[3] for t in self.trees]
