@@ -1,9 +1,10 @@
 // Gated DeltaNet tree verify and single-token decode.
 //
 // Tree verify ("Adding a model", Gated DeltaNet layers; the gated delta rule
-// applied along every node's root path): one warp (one CTA) owns 4 * 32/LPR
-// state rows of one value head of one sequence and walks the tree in the
-// order prepared by tv_tree_prepare.  A lane group of LPR lanes holds four
+// applied along every node's root path): a CTA of four warps owns
+// 4 * 4 * 32/LPR state rows of one value head of one sequence (the warps share
+// one staged copy of the tree's keys, queries and gates) and each warp walks
+// the tree in the order prepared by tv_tree_prepare.  A lane group of LPR lanes holds four
 // state rows, so each node's key and query, read once from shared memory (as
 // bf16), serve four rows, and the eight dot products of a step (s.k and s.q
 // of each row) are reduced together by one reduce-scatter.  The few states
@@ -49,7 +50,9 @@ struct GdnShape {
   static constexpr int DK = 16 * LPR;  // key dim
   static constexpr int NG = 32 / LPR;  // lane groups per warp
   static constexpr int RPG = 4;        // state rows per lane group
-  static constexpr int R = NG * RPG;   // state rows per CTA
+  static constexpr int W = 4;          // warps per CTA (one per SM sub-partition)
+  static constexpr int NGC = NG * W;   // lane groups per CTA
+  static constexpr int R = NGC * RPG;  // state rows per CTA
   static constexpr int NV = 2 * RPG;   // dot products per step and group (s.k, s.q per row)
 };
 
@@ -70,14 +73,15 @@ __device__ __forceinline__ void cp_async16_g(void* dst, const void* src) {
 }
 
 template <typename T, int LPR>
-__global__ void __launch_bounds__(32) gdn_verify_kernel(const GdnVerifyParams p) {
+__global__ void __launch_bounds__(32 * GdnShape<LPR>::W) gdn_verify_kernel(const GdnVerifyParams p) {
   using Sh = GdnShape<LPR>;
   constexpr int DK = Sh::DK, R = Sh::R, RPG = Sh::RPG, NV = Sh::NV;
   const int s = blockIdx.y;
   const int rb_per_head = (p.dv + R - 1) / R;
   const int h = blockIdx.x / rb_per_head;
   const int rb = blockIdx.x % rb_per_head;
-  const int lane = threadIdx.x, gi = lane / LPR, j = lane % LPR;
+  const int tid = threadIdx.x, lane = tid & 31, j = lane % LPR;
+  const int gi = (tid >> 5) * Sh::NG + lane / LPR;  // lane group within the CTA
 
   // this group's four state rows first (they do not depend on the tree, and
   // no kernel of the round before commit writes them), so their loads overlap
@@ -102,7 +106,7 @@ __global__ void __launch_bounds__(32) gdn_verify_kernel(const GdnVerifyParams p)
   const int n = info.n, off = info.off;
   if (n <= 0 || n > p.n_max) return;
   if (info.max_slot > p.n_slots) {
-    if (lane == 0) set_status(p.status, TV_ERR_TREE);
+    if (tid == 0) set_status(p.status, TV_ERR_TREE);
     return;
   }
   const int g = h / (p.Hv / p.Hk);
@@ -123,18 +127,18 @@ __global__ void __launch_bounds__(32) gdn_verify_kernel(const GdnVerifyParams p)
     constexpr int CPR = DK * static_cast<int>(sizeof(T)) / 16;  // 16-byte chunks per key row
     const T* qg = static_cast<const T*>(p.q);
     const T* kg = static_cast<const T*>(p.k);
-    for (int idx = lane; idx < n * CPR; idx += 32) {
+    for (int idx = tid; idx < n * CPR; idx += blockDim.x) {
       const size_t src = (static_cast<size_t>(off + idx / CPR) * p.Hk + g) * DK + (idx % CPR) * (16 / sizeof(T));
       cp_async16_g(kb + static_cast<size_t>(idx / CPR) * DK + (idx % CPR) * (16 / sizeof(T)), kg + src);
       cp_async16_g(qb + static_cast<size_t>(idx / CPR) * DK + (idx % CPR) * (16 / sizeof(T)), qg + src);
     }
     asm volatile("cp.async.commit_group;" ::: "memory");
     const T* vg = static_cast<const T*>(p.v);
-    for (int base = lane; base < n * R; base += 16 * 32) {
+    for (int base = tid; base < n * R; base += 16 * blockDim.x) {
       float vv[16];
 #pragma unroll
       for (int u = 0; u < 16; u++) {
-        const int idx = base + u * 32;
+        const int idx = base + u * blockDim.x;
         const int row = rb * R + idx % R;
         vv[u] = (idx < n * R && row < p.dv)
                     ? to_f32(vg[(static_cast<size_t>(off + idx / R) * p.Hv + h) * p.dv + row])
@@ -142,20 +146,20 @@ __global__ void __launch_bounds__(32) gdn_verify_kernel(const GdnVerifyParams p)
       }
 #pragma unroll
       for (int u = 0; u < 16; u++)
-        if (base + u * 32 < n * R) vb[base + u * 32] = vv[u];
+        if (base + u * blockDim.x < n * R) vb[base + u * blockDim.x] = vv[u];
     }
-    for (int idx = lane; idx < n; idx += 32) {
+    for (int idx = tid; idx < n; idx += blockDim.x) {
       const size_t ah = static_cast<size_t>(off + idx) * p.Hv + h;
       const float a = p.alpha[ah], b = p.beta[ah];
       sch[idx] = mv.sched[off + idx];
       nc[idx] = make_float4(a, b, 0.f, 0.f);
     }
     asm volatile("cp.async.wait_all;" ::: "memory");
-    __syncwarp();
+    __syncthreads();
   }
   // k . q of every node: each group takes eight nodes at a time, and one
   // reduce-scatter finishes all of them
-  for (int base = 0; base < n; base += 8 * Sh::NG) {
+  for (int base = 0; base < n; base += 8 * Sh::NGC) {
     float part[8];
 #pragma unroll
     for (int m = 0; m < 8; m++) {
@@ -177,7 +181,7 @@ __global__ void __launch_bounds__(32) gdn_verify_kernel(const GdnVerifyParams p)
       if (writer && node < n) nc[node].z = part[i];
     }
   }
-  __syncwarp();
+  __syncthreads();
 
   T* out = static_cast<T*>(p.out);
   for (int step = 0; step < n; step++) {
@@ -308,7 +312,8 @@ static void launch_verify(const GdnVerifyParams& p, int n_seq, cudaStream_t st, 
     attrs = true;
   }
   const dim3 grid(p.Hv * ((p.dv + R - 1) / R), n_seq);
-  launch_k(ov, gdn_verify_kernel<T, LPR>, grid, dim3(32), gdn_verify_smem<T, LPR>(p.n_max, p.n_slots), st, p);
+  launch_k(ov, gdn_verify_kernel<T, LPR>, grid, dim3(32 * GdnShape<LPR>::W), gdn_verify_smem<T, LPR>(p.n_max, p.n_slots),
+           st, p);
 }
 
 template <typename T, int LPR>
