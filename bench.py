@@ -150,7 +150,7 @@ def oracle_sample_inputs(cfg, device):
     n = len(parent)
     L = cfg.ctx_lens[0]
     attn_li = cfg.attn_layers[0]
-    gdn_lis = [i for i in range(attn_li + 1) if not cfg.is_attn(i)][:3]
+    gdn_lis = [i for i in range(cfg.n_layers) if not cfg.is_attn(i)][:3]
     a = synth.attn_layer_inputs(cfg, attn_li, 0, n, L + 64, device)
     gs = [synth.gdn_layer_inputs(cfg, li, 0, n, device) for li in gdn_lis]
     return parent, tok, greedy, a, gs
@@ -164,7 +164,7 @@ def time_oracle(cfg, inputs, attn_kv_heads, attn_nodes, gdn_heads, gdn_nodes):
     nodes of each of the block's GDN layers, plus the accept walk and the
     commit.  The round estimate scales attention by query rows (each costs
     one pass over the context) and GDN by (recurrence steps x value heads).
-    Returns (seconds, estimated seconds per round)."""
+    Returns (seconds, estimated seconds per round, attention seconds, GDN seconds)."""
     import numpy as np
 
     import oracle.tree_verify as O
@@ -198,7 +198,7 @@ def time_oracle(cfg, inputs, attn_kv_heads, attn_nodes, gdn_heads, gdn_nodes):
     n_gdn = cfg.n_layers - n_attn
     est_attn = (t1 - t0) * (n * s.Hq) / (na * ka * G) * n_attn
     est_gdn = (t2 - t1) * (steps_f * s.Hv) / (steps_s * gh) * (n_gdn / len(gs))
-    return t2 - t0, est_attn + est_gdn
+    return t2 - t0, est_attn + est_gdn, t1 - t0, t2 - t1
 
 
 def blas_threads():
@@ -339,14 +339,24 @@ def run_ours(args, rank, world, local_rank):
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
         inp = oracle_sample_inputs(cfg, dev)
         s = cfg.shapes
-        secs, est = time_oracle(cfg, inp, 1, n_nodes[0], max(1, s.Hv // s.Hk), n_nodes[0])
+        # calibrate on the smallest sample, then size it for about 12 s of CPU work
+        grp = max(1, s.Hv // s.Hk)  # value heads per key head: whole groups only
+        _, _, ta, tg = time_oracle(cfg, inp, 1, n_nodes[0], grp, n_nodes[0])
+        ka = int(min(s.Hkv, max(1, 6.0 // max(ta, 1e-3))))
+        gh = int(min(s.Hv, max(grp, (6.0 / max(tg, 1e-3)) * grp))) // grp * grp
+        secs, ests = 0.0, []
+        while secs < 10.0 and len(ests) < 5:  # at least 10 s of CPU work in all
+            t, e, _, _ = time_oracle(cfg, inp, ka, n_nodes[0], gh, n_nodes[0])
+            secs += t
+            ests.append(e)
+        est = statistics.median(ests)
         cpu = {"value": round(nodes_per_round / est, 3) if cfg.n_seq == 1 else None, "unit": UNIT,
                "cores": blas_threads(), "kind": "oracle",
-               "sample": (f"fp64 numpy oracle on sequence 0: one attention layer restricted to 1 of {s.Hkv} KV heads "
-                          f"(all {n_nodes[0]} nodes, full context) and {min(3, cfg.n_layers - 1)} GDN layers restricted "
-                          f"to {s.Hv // s.Hk} of {s.Hv} value heads, plus accept and commit; {secs:.1f} s of CPU work "
-                          f"scaled by heads and layers to one {cfg.n_layers}-layer round "
-                          f"({est:.1f} s estimated per round)"),
+               "sample": (f"fp64 numpy oracle on sequence 0: one attention layer restricted to {ka} of {s.Hkv} KV "
+                          f"heads (all {n_nodes[0]} nodes, full context) and {min(3, cfg.n_layers - 1)} GDN layers "
+                          f"restricted to {gh} of {s.Hv} value heads, plus accept and commit, run {len(ests)} times; "
+                          f"{secs:.1f} s of CPU work in all, scaled by heads and layers to one "
+                          f"{cfg.n_layers}-layer round (median {est:.1f} s estimated per round)"),
                "est_round_s": round(est, 2)}
 
     hbm_peak, peak_kind = peaks()
@@ -398,7 +408,7 @@ def run_reference(args, rank, world):
     n_nodes = len(inp[0])
     # calibrate the smallest sample, then size each step so the run stays near two minutes
     time_oracle(cfg, inp, 1, 1, 1, 1)
-    secs1, _ = time_oracle(cfg, inp, 1, 1, 1, 1)
+    secs1 = time_oracle(cfg, inp, 1, 1, 1, 1)[0]
     budget = 120.0 / max(1, args.steps + args.warmup)
     grow = max(1.0, budget / max(secs1, 1e-4))
     na = max(1, min(n_nodes, int(grow)))
@@ -409,7 +419,7 @@ def run_reference(args, rank, world):
     ests = []
     t0 = time.perf_counter()
     for _ in range(args.steps):
-        _, est = time_oracle(cfg, inp, 1, na, gh, ng)
+        est = time_oracle(cfg, inp, 1, na, gh, ng)[1]
         ests.append(est)
     wall = time.perf_counter() - t0
     est = statistics.median(ests)
