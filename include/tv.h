@@ -105,8 +105,8 @@ typedef struct {
 
 /* TV_TREE_OVERLAP: the calls that take this tree launch their kernels with
  * programmatic dependent launch, so that a kernel can start (shared- and
- * tensor-memory setup, loads of the recurrent state, L2 prefetch of its first
- * KV tiles) while the kernel before it on the stream finishes; the next
+ * tensor-memory setup, loads of the recurrent state) while the kernel before
+ * it on the stream finishes; the next
  * kernel is let in only after a kernel's own wait for its predecessor has
  * returned (at its start for the attention split kernel, at exit elsewhere),
  * so everything older than the predecessor has completed.  Before waiting, a

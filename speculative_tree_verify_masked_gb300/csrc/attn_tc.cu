@@ -19,15 +19,18 @@
 //  split kernel (persistent, one CTA per SM): the tiles that every node of a
 //    sequence shares (positions below 64*floor(L/64), all cache rows) for up to
 //    128 query rows (node x head of one KV head) at once.  Warps 0 and 10
-//    stream K and V tiles with TMA (128B-swizzled boxes) through two rings,
-//    with L2 prefetch further ahead; warp 1 issues QK^T (Q in TMEM, K in
+//    stream K and V tiles with TMA (128B-swizzled boxes) through two rings;
+//    warp 1 issues QK^T (Q in TMEM, K in
 //    shared memory, S double-buffered in TMEM) and warp 11 issues PV (P in a
 //    ring of shared-memory slots, V in shared memory, O in TMEM); warps 2-5
 //    and 6-9 run the softmax, one TMEM lane (query row) and one half tile per
 //    thread.  An S buffer is reused as soon as the softmax has read it, so
 //    QK^T runs ahead of the softmax and the tensor pipe overlaps the narrow
-//    QK^T steps with the wide PV steps.  Each split's state goes to the
-//    workspace.
+//    QK^T steps with the wide PV steps.  When the largest tree spans two
+//    128-row blocks, the two row blocks of a (sequence, KV head, split) run
+//    as a 2-CTA cluster that shares one K/V stream: each CTA loads half of
+//    every tile's boxes and multicasts them to both, so each tile leaves DRAM
+//    once.  Each split's state goes to the workspace.
 //  tail kernel (one CTA per node and KV head): the node's own tiles (cache
 //    rows past the last shared tile plus its ancestors at their logical
 //    slots, gathered into shared memory with cp.async), continuing the split
@@ -50,7 +53,6 @@ constexpr int kTile = 64;       // KV positions per tile
 constexpr int kHalf = 32;       // positions per softmax half
 constexpr int kBox = 64 * 128;  // one [64 rows x 128 B] 128B-swizzled box
 constexpr int kMaxGroup = 64;   // query heads per KV head on this path
-constexpr int kPrefetch = 8;    // tiles of L2 prefetch ahead of the ring loads
 
 template <int D>
 struct Tc {
@@ -96,6 +98,7 @@ struct TcParams {
   float* ws;
   int n_seq, n_total, Hq, Hkv, G, cap, max_len, split_tiles, max_splits, rows_max, decode;
   int n_mstage;  // tail kernel: finished splits whose states are staged in shared memory
+  int pair;      // split kernel: 2-CTA clusters, one per (sequence, KV head, split), CTA rank = row block
   float c;  // scale * log2(e)
 };
 
@@ -265,20 +268,20 @@ __device__ inline void item_space(const TcParams& p, ItemSpace& is) {
     nodes = nodes < 0 ? 0 : (nodes > TV_MAX_NODES ? TV_MAX_NODES : nodes);
     is.off[s] = p.decode ? s : p.node_off[s];
     is.rows[s] = nodes * p.G;
-    is.nrb[s] = (is.rows[s] + 127) / 128;
+    is.nrb[s] = p.pair ? 1 : (is.rows[s] + 127) / 128;  // a pair covers row blocks 0 and 1
     is.tsh[s] = L / kTile;
     const int nsplit = (is.tsh[s] + p.split_tiles - 1) / p.split_tiles;
     is.cum[s + 1] = is.cum[s] + nsplit * p.Hkv * is.nrb[s];
   }
 }
 
-__device__ inline Item item_at(const ItemSpace& is, const TcParams& p, int w) {
+__device__ inline Item item_at(const ItemSpace& is, const TcParams& p, int w, int rank) {
   int s = 0;
   while (s < p.n_seq - 1 && w >= is.cum[s + 1]) s++;
   int r = w - is.cum[s];
   Item it;
   it.s = s;
-  it.rb = r % is.nrb[s];
+  it.rb = p.pair ? rank : r % is.nrb[s];
   r /= is.nrb[s];
   it.g = r % p.Hkv;
   it.split = r / p.Hkv;
@@ -349,15 +352,25 @@ __global__ void __launch_bounds__(384, 1) attn_split_kernel(const __grid_constan
   const uint32_t XBAR0 = DRAIN + 16u;  // [2] half-max exchange, by tile parity
   const uint32_t kring = sb, vring = sb + C::NK * C::TILE, pring = vring + C::NV * C::TILE;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  // Pair mode: a 2-CTA cluster shares the K/V stream of one (sequence, KV
+  // head, split); CTA rank r computes row block r, loads half of each tile's
+  // boxes and multicasts them to both CTAs, and a ring slot is refilled only
+  // after both CTAs' QK^T / PV have read it.
+  const bool pair = p.pair != 0;
+  const int rank = pair ? static_cast<int>(cluster_ctarank()) : 0;
+  const int cid = pair ? static_cast<int>(blockIdx.x) / 2 : static_cast<int>(blockIdx.x);
+  const int ncl = pair ? static_cast<int>(gridDim.x) / 2 : static_cast<int>(gridDim.x);
+  const int kb0 = pair ? rank * (C::KB / 2) : 0, kb1 = pair ? kb0 + C::KB / 2 : C::KB;
+  constexpr uint16_t kBoth = 3;
 
   if (threadIdx.x == 0) {
     for (int i = 0; i < C::NK; i++) {
       mbar_init(KFULL0 + 8u * i, 1);
-      mbar_init(KEMPTY0 + 8u * i, 1);
+      mbar_init(KEMPTY0 + 8u * i, pair ? 2 : 1);
     }
     for (int i = 0; i < C::NV; i++) {
       mbar_init(VFULL0 + 8u * i, 1);
-      mbar_init(VEMPTY0 + 8u * i, 1);
+      mbar_init(VEMPTY0 + 8u * i, pair ? 2 : 1);
     }
     for (int b = 0; b < 2; b++) {
       mbar_init(SFULL0 + 8u * b, 1);
@@ -382,16 +395,9 @@ __global__ void __launch_bounds__(384, 1) attn_split_kernel(const __grid_constan
   tc_fence_before();
   __syncthreads();
   tc_fence_after();
+  if (pair) cluster_sync();  // both CTAs' barriers exist before either signals the other
   const uint32_t tbase = *tmem_slot;
   const int total = is.cum[p.n_seq];
-  // L2 prefetch of the first item's first tiles while the previous kernel ends
-  if ((warp == 0 || warp == 10) && lane == 0 && static_cast<int>(blockIdx.x) < total) {
-    const Item I = item_at(is, p, blockIdx.x);
-    const CUtensorMap* map = warp == 0 ? &p.tmK[I.s] : &p.tmV[I.s];
-    for (int t = I.t0; t < min(I.t0 + kPrefetch, I.t1); t++)
-#pragma unroll
-      for (int kb = 0; kb < C::KB; kb++) tma_prefetch_l2_2d(map, kb * 64, I.g * p.cap + t * kTile);
-  }
   pdl_wait();  // queries, status and the workspace (read by the previous tail) from here on
   pdl_trigger();
   if (threadIdx.x == 0) skip = status_bad(p.status) ? 1 : 0;
@@ -406,20 +412,10 @@ __global__ void __launch_bounds__(384, 1) attn_split_kernel(const __grid_constan
     const CUtensorMap* maps = is_k ? p.tmK : p.tmV;
     uint32_t it = 0;
     bool ok = true;
-    for (int w = blockIdx.x; w < total && ok; w += gridDim.x) {
-      const Item I = item_at(is, p, w);
+    for (int w = cid; w < total && ok; w += ncl) {
+      const Item I = item_at(is, p, w, rank);
       const int ybase = I.g * p.cap;
-      // L2 prefetch runs kPrefetch tiles ahead of the ring's loads, so a ring
-      // load waits for L2, not DRAM
-      for (int t = I.t0; t < min(I.t0 + kPrefetch, I.t1); t++)
-#pragma unroll
-        for (int kb = 0; kb < C::KB; kb++) tma_prefetch_l2_2d(&maps[I.s], kb * 64, ybase + t * kTile);
       for (int t = I.t0; t < I.t1; t++) {
-        if (t + kPrefetch < I.t1) {
-#pragma unroll
-          for (int kb = 0; kb < C::KB; kb++)
-            tma_prefetch_l2_2d(&maps[I.s], kb * 64, ybase + (t + kPrefetch) * kTile);
-        }
         const int st = it % nslot;
         if (!wait_role(empty0 + 8u * st, ((it / nslot) & 1) ^ 1, abort_flag)) {
           ok = false;
@@ -429,8 +425,14 @@ __global__ void __launch_bounds__(384, 1) attn_split_kernel(const __grid_constan
         mbar_arrive_expect_tx(full, C::TILE);
         const uint32_t dst = ring + st * C::TILE;
         const int y = ybase + t * kTile;
+        if (pair) {
+          // this CTA's half of the boxes, into both CTAs (each CTA's full
+          // barrier expects the whole tile)
+          for (int kb = kb0; kb < kb1; kb++) tma_load_2d_mc(dst + kb * kBox, &maps[I.s], full, kb * 64, y, kBoth);
+        } else {
 #pragma unroll
-        for (int kb = 0; kb < C::KB; kb++) tma_load_2d(dst + kb * kBox, &maps[I.s], full, kb * 64, y);
+          for (int kb = 0; kb < C::KB; kb++) tma_load_2d(dst + kb * kBox, &maps[I.s], full, kb * 64, y);
+        }
         it++;
       }
     }
@@ -450,8 +452,8 @@ __global__ void __launch_bounds__(384, 1) attn_split_kernel(const __grid_constan
     const bool is_qk = warp == 1;
     uint32_t t = 0, q_ph = 0;  // CTA-wide tile counter
     bool ok = true;
-    for (int w = blockIdx.x; w < total && ok; w += gridDim.x) {
-      const Item I = item_at(is, p, w);
+    for (int w = cid; w < total && ok; w += ncl) {
+      const Item I = item_at(is, p, w, rank);
       const int n = I.t1 - I.t0;
       if (is_qk) {
         if (!wait_warp(QREADY, q_ph, abort_flag)) {
@@ -475,7 +477,7 @@ __global__ void __launch_bounds__(384, 1) attn_split_kernel(const __grid_constan
 #pragma unroll
             for (int kk = 0; kk < D / 16; kk++) issue_qk_step_from<D>(tS, tQ, kd, kk);
             tc_commit(SFULL0 + 8u * b);
-            tc_commit(KEMPTY0 + 8u * ks);
+            if (pair) tc_commit_mc(KEMPTY0 + 8u * ks, kBoth); else tc_commit(KEMPTY0 + 8u * ks);
           }
           __syncwarp();
         } else {
@@ -488,7 +490,7 @@ __global__ void __launch_bounds__(384, 1) attn_split_kernel(const __grid_constan
           tc_fence_after();
           if (elect_one_sync()) {
             issue_pv_ss<D>(tbase + C::T_O, pring + ps * C::PTILE, desc_v(vring + vs * C::TILE, 0), k > 0);
-            tc_commit(VEMPTY0 + 8u * vs);
+            if (pair) tc_commit_mc(VEMPTY0 + 8u * vs, kBoth); else tc_commit(VEMPTY0 + 8u * vs);
             tc_commit(ODONE0 + 8u * ps);
           }
           __syncwarp();
@@ -509,8 +511,8 @@ __global__ void __launch_bounds__(384, 1) attn_split_kernel(const __grid_constan
     const uint32_t tl = tbase + (static_cast<uint32_t>(quad * 32) << 16);
     uint32_t t = 0;  // CTA-wide tile counter
     bool ok = true;
-    for (int w = blockIdx.x; w < total && ok; w += gridDim.x) {
-      const Item I = item_at(is, p, w);
+    for (int w = cid; w < total && ok; w += ncl) {
+      const Item I = item_at(is, p, w, rank);
       const int n = I.t1 - I.t0;
       const int row = I.rb * 128 + lrow;
       const bool valid = row < is.rows[I.s];
@@ -605,6 +607,7 @@ __global__ void __launch_bounds__(384, 1) attn_split_kernel(const __grid_constan
   tc_fence_before();
   __syncthreads();
   tc_fence_after();
+  if (pair) cluster_sync();  // the peer no longer writes into this CTA's shared memory or barriers
   if (warp == 1) tmem_dealloc(tbase, C::COLS);
 }
 
@@ -1070,8 +1073,31 @@ static tv_status launch_tc(TcParams& p, int n_items_bound, int n_tail, cudaStrea
     attrs = true;
   }
   if (n_items_bound > 0) {
-    const int grid = n_items_bound < num_sms() ? n_items_bound : num_sms();
-    launch_k(ov, attn_split_kernel<D>, dim3(grid), dim3(384), C::SMEM_SPLIT, st, p);
+    if (p.pair) {
+      // one 2-CTA cluster per item, at most one cluster per pair of SMs
+      const int pairs = n_items_bound < num_sms() / 2 ? n_items_bound : num_sms() / 2;
+      cudaLaunchConfig_t cfg = {};
+      cfg.gridDim = dim3(2 * pairs);
+      cfg.blockDim = dim3(384);
+      cfg.dynamicSmemBytes = C::SMEM_SPLIT;
+      cfg.stream = st;
+      cudaLaunchAttribute attr[2];
+      attr[0].id = cudaLaunchAttributeClusterDimension;
+      attr[0].val.clusterDim.x = 2;
+      attr[0].val.clusterDim.y = 1;
+      attr[0].val.clusterDim.z = 1;
+      cfg.attrs = attr;
+      cfg.numAttrs = 1;
+      if (ov) {
+        attr[1].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+        attr[1].val.programmaticStreamSerializationAllowed = 1;
+        cfg.numAttrs = 2;
+      }
+      cudaLaunchKernelEx(&cfg, attn_split_kernel<D>, p);
+    } else {
+      const int grid = n_items_bound < num_sms() ? n_items_bound : num_sms();
+      launch_k(ov, attn_split_kernel<D>, dim3(grid), dim3(384), C::SMEM_SPLIT, st, p);
+    }
   }
   launch_k(ov, attn_tail_kernel<D>, dim3(n_tail), dim3(256), smem_tail, st, p);
   return launch_status();
@@ -1121,7 +1147,11 @@ tv_status attn_tc_launch(const tv_plan* plan, const AttnCall& a, void* ws, size_
   p.c = a.scale * 1.4426950408889634f;
   const int tiles_bound = a.max_len / kTile;
   const int splits_bound = (tiles_bound + p.split_tiles - 1) / p.split_tiles;
-  const int items_bound = a.n_seq * l->Hkv * splits_bound * ((n_max * G + 127) / 128);
+  // pair mode when the largest tree spans exactly two 128-row blocks (and a
+  // tile's boxes split evenly between the two CTAs)
+  const int nrb_max = (n_max * G + 127) / 128;
+  p.pair = (!a.decode && l->D >= 128 && nrb_max == 2) ? 1 : 0;
+  const int items_bound = a.n_seq * l->Hkv * splits_bound * (p.pair ? 1 : nrb_max);
   const int n_tail = (a.decode ? a.n_seq : a.n_total) * l->Hkv;
   switch (l->D) {
     case 64: return launch_tc<64>(p, items_bound, n_tail, st, a.overlap);
