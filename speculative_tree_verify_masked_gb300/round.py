@@ -71,6 +71,8 @@ class VerifyRound:
             split = auto_split(cfg.ctx_lens, self.n_nodes, s.Hq, s.Hkv, sms)
         self.split = split
         self.plan = B.plan(split)
+        self._attn_marks = None  # events around attention layers while capturing
+        self._graph_marks = None
         self.attn_scale = 1.0 / math.sqrt(s.D)
         self.gdn_scale = 1.0 / math.sqrt(s.dk)
         self.attn, self.gdn = {}, {}
@@ -123,7 +125,16 @@ class VerifyRound:
     def verify(self, stream=None):
         self.prepare(stream)
         for li in self.layers:
+            marks = self._attn_marks is not None and li in self.attn
+            if marks:
+                # external events become timing-capable record nodes of the graph
+                a = torch.cuda.Event(enable_timing=True, external=True)
+                b = torch.cuda.Event(enable_timing=True, external=True)
+                a.record()
             self.verify_layer(li, stream)
+            if marks:
+                b.record()
+                self._attn_marks.append((a, b))
 
     def accept(self, stream=None):
         B.tv_accept_path(self.tree, self.tok, self.greedy, self.path, self.acc_len, self.bonus, stream)
@@ -144,8 +155,11 @@ class VerifyRound:
     def status(self) -> int:
         return self.tree.status_code()
 
-    def capture(self):
-        """Capture run() in a CUDA graph on a side stream; returns the graph."""
+    def capture(self, attn_marks: bool = False):
+        """Capture run() in a CUDA graph on a side stream; returns the graph.
+        With attn_marks, CUDA events recorded around every attention layer
+        become part of the graph; after a replay, attn_marks_ms() gives each
+        layer's time in that replay."""
         g = torch.cuda.CUDAGraph()
         s = torch.cuda.Stream()
         s.wait_stream(torch.cuda.current_stream())
@@ -153,6 +167,13 @@ class VerifyRound:
             self.run()  # warm (attribute setup outside capture)
         torch.cuda.current_stream().wait_stream(s)
         torch.cuda.synchronize()
+        self._attn_marks = [] if attn_marks else None
         with torch.cuda.graph(g):
             self.run()
+        self._graph_marks, self._attn_marks = self._attn_marks, None
         return g
+
+    def attn_marks_ms(self):
+        """Per attention layer, the ms between the events around it in the
+        latest replay of the graph captured with attn_marks."""
+        return [a.elapsed_time(b) for a, b in (self._graph_marks or [])]
