@@ -108,7 +108,8 @@ typedef struct {
  * tensor-memory setup, loads of the recurrent state) while the kernel before
  * it on the stream finishes; the next
  * kernel is let in only after a kernel's own wait for its predecessor has
- * returned (at its start for the attention split kernel, at exit elsewhere),
+ * returned (right after that wait in the attention split kernel and GDN
+ * verify, at exit elsewhere),
  * so everything older than the predecessor has completed.  Before waiting, a
  * kernel reads only the recurrent states (GDN verify), the lengths and
  * node_off (attention), and the tree tables (the attention tail, whose

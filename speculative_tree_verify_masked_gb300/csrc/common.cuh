@@ -14,9 +14,10 @@ namespace tv {
 // own set-up, and wait until the previous kernel has finished and its writes
 // are visible.  Both are no-ops for a kernel launched without the attribute.
 // A kernel that never calls pdl_trigger lets the next one start as its
-// blocks exit; only the attention split kernel triggers early (its successor
-// takes one CTA per SM wherever a split CTA has finished, while an early
-// launch of the narrow GDN CTAs would place them unevenly).
+// blocks exit.  The attention split kernel and GDN verify trigger early: both
+// run at most one CTA per SM, so an early successor only takes SMs they do
+// not use (measured: 1.8 % per round from GDN; the tail kernel's early
+// trigger cost time).
 __device__ __forceinline__ void pdl_trigger() { asm volatile("griddepcontrol.launch_dependents;" ::: "memory"); }
 __device__ __forceinline__ void pdl_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
 

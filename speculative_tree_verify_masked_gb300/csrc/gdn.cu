@@ -100,6 +100,7 @@ __global__ void __launch_bounds__(32 * GdnShape<LPR>::W) gdn_verify_kernel(const
     }
   }
   pdl_wait();  // tree tables, status and node inputs come from earlier kernels
+  pdl_trigger();
   MetaView mv = meta_view(const_cast<void*>(p.meta), p.n_total);
   const SeqInfo info = mv.seq[s];
   if (status_bad(p.status)) return;
