@@ -236,3 +236,36 @@ def test_relabel_permutes_rows():
                              out, r.gdn_scale)
         torch.cuda.synchronize()
         assert torch.equal(out, g["out"][idx])
+
+
+@pytest.mark.parametrize("cfg_id", [2, 3, 4])
+def test_overlapped_launch_gives_same_bits(cfg_id):
+    """A round launched with TV_TREE_OVERLAP (programmatic dependent launch)
+    gives the same bits as the same round launched plainly: outputs of every
+    verified layer, the accepted path, and the committed caches and states.
+    On the 64-layer workload the attention layers also run as 2-CTA clusters."""
+    cfg = synth.workload(cfg_id)
+    layers = None if cfg.n_layers <= 2 else [0, 1, 2, 3, 7]
+    runs = []
+    for overlap in (False, True):
+        r = VerifyRound(cfg, layers=layers, overlap=overlap)
+        r.run()
+        torch.cuda.synchronize()
+        assert r.status() == 0
+        got = {"path": r.path.clone(), "acc": r.acc_len.clone(), "bonus": r.bonus.clone(), "len": r.len.clone()}
+        for li, a in r.attn.items():
+            got[f"out{li}"] = bits(a["out"]).clone()
+            got[f"K{li}"] = [bits(k).clone() for k in a["layer"].K]
+        for li, g in r.gdn.items():
+            got[f"out{li}"] = bits(g["out"]).clone()
+            got[f"S{li}"] = [bits(st).clone() for st in g["layer"].S]
+        runs.append(got)
+        del r
+        torch.cuda.empty_cache()
+    plain, ov = runs
+    for k in plain:
+        if isinstance(plain[k], list):
+            for x, y in zip(plain[k], ov[k]):
+                assert torch.equal(x, y), k
+        else:
+            assert torch.equal(plain[k], ov[k]), k
