@@ -245,6 +245,81 @@ __device__ __forceinline__ void store_state(uint32_t tO, float* rec, int hf, flo
   }
 }
 
+// Queries of one row into TMEM (bf16 pairs, columns T_Q ..).  For D >= 128
+// each half-tile thread moves its half of the row (D/4 columns from hf*D/4);
+// for D = 64 the half-0 thread moves the whole row (32 columns).
+template <int D>
+struct QShare {
+  static constexpr int N = D >= 128 ? D / 16 : D / 8;  // 16-byte pieces per thread
+  static constexpr int COL0 = D >= 128 ? D / 4 : 0;    // first column of half 1
+};
+template <int D>
+__device__ __forceinline__ void q_fetch(const __nv_bfloat16* qrow, int hf, uint4 (&qv)[QShare<D>::N]) {
+  const bool act = qrow != nullptr && (D >= 128 || hf == 0);
+  const uint4* q4 = act ? reinterpret_cast<const uint4*>(qrow) + hf * QShare<D>::N : nullptr;
+#pragma unroll
+  for (int i = 0; i < QShare<D>::N; i++) qv[i] = act ? q4[i] : make_uint4(0u, 0u, 0u, 0u);
+}
+template <int D>
+__device__ __forceinline__ void q_store(uint32_t tq, int hf, const uint4 (&qv)[QShare<D>::N]) {
+  if (D < 128 && hf != 0) return;
+#pragma unroll
+  for (int j = 0; j < QShare<D>::N / 8; j++) {
+    uint32_t r[32];
+#pragma unroll
+    for (int i = 0; i < 8; i++) {
+      r[4 * i] = qv[8 * j + i].x;
+      r[4 * i + 1] = qv[8 * j + i].y;
+      r[4 * i + 2] = qv[8 * j + i].z;
+      r[4 * i + 3] = qv[8 * j + i].w;
+    }
+    tmem_st32(tq + hf * QShare<D>::COL0 + 32 * j, r);
+  }
+}
+
+// The split state of a warp's 32 rows (this half's O columns, then m and the
+// half sums) to the workspace.  A thread holds one row after tcgen05.ld; the
+// warp turns each 32-column block around through 4 KB of shared memory (rows
+// of 128 bytes, 16-byte units at unit ^ (row % 8)) so that one store
+// instruction writes 128 contiguous bytes of each of four rows instead of 16
+// bytes of each of 32.  rec(r) is the record of warp row r or null.
+template <int D, typename Rec>
+__device__ __forceinline__ void store_state_warp(uint32_t tO, uint32_t xbuf, int hf, int lane, float m, float lh,
+                                                 Rec rec) {
+#pragma unroll 1
+  for (int c0 = hf * (D / 2); c0 < (hf + 1) * (D / 2); c0 += 32) {
+    uint32_t r[32];
+    tmem_ld32(tO + c0, r);
+#pragma unroll
+    for (int u = 0; u < 8; u++)
+      asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(xbuf + lane * 128 + ((u ^ (lane & 7)) << 4)),
+                   "r"(r[4 * u]), "r"(r[4 * u + 1]), "r"(r[4 * u + 2]), "r"(r[4 * u + 3])
+                   : "memory");
+    __syncwarp();
+#pragma unroll
+    for (int i = 0; i < 8; i++) {
+      const int rr = 4 * i + (lane >> 3), u = lane & 7;
+      float4 v;
+      asm volatile("ld.shared.v4.f32 {%0, %1, %2, %3}, [%4];"
+                   : "=f"(v.x), "=f"(v.y), "=f"(v.z), "=f"(v.w)
+                   : "r"(xbuf + rr * 128 + ((u ^ (rr & 7)) << 4))
+                   : "memory");
+      float* d = rec(rr);
+      if (d) *reinterpret_cast<float4*>(d + c0 + 4 * u) = v;
+    }
+    __syncwarp();
+  }
+  float* own = rec(lane);
+  if (own) {
+    if (hf == 0) {
+      own[D] = m;
+      own[D + 1] = lh;
+    } else {
+      own[D + 2] = lh;
+    }
+  }
+}
+
 // ---------------------------------------------------------------------------
 // split kernel
 // ---------------------------------------------------------------------------
@@ -328,6 +403,7 @@ __device__ __forceinline__ bool wait_role(uint32_t bar, uint32_t parity, volatil
 template <int D>
 __global__ void __launch_bounds__(384, 1) attn_split_kernel(const __grid_constant__ TcParams p) {
   using C = Tc<D>;
+  static_assert(C::NP * C::PTILE >= 8 * 4096, "the state store turns rows around in the P ring");
   extern __shared__ uint8_t smem_raw[];
   __shared__ ItemSpace is;
   __shared__ int skip;
@@ -401,6 +477,19 @@ __global__ void __launch_bounds__(384, 1) attn_split_kernel(const __grid_constan
   pdl_wait();  // queries, status and the workspace (read by the previous tail) from here on
   pdl_trigger();
   if (threadIdx.x == 0) skip = status_bad(p.status) ? 1 : 0;
+  // softmax threads: the first item's query row, in flight during the status read
+  uint4 qv[QShare<D>::N];
+  const bool softmax_warp = warp >= 2 && warp <= 9;
+  const int hf = (warp - 2) >> 2;  // softmax half: 0: slots 0-31, 1: slots 32-63
+  const int quad = warp & 3;
+  const int lrow = quad * 32 + lane;
+  auto q_row = [&](const Item& I) -> const __nv_bfloat16* {
+    const int row = I.rb * 128 + lrow;
+    if (row >= is.rows[I.s]) return nullptr;
+    const int node = row / p.G, jh = row % p.G;
+    return p.q + (static_cast<size_t>(is.off[I.s] + node) * p.Hq + I.g * p.G + jh) * D;
+  };
+  if (softmax_warp && cid < total) q_fetch<D>(q_row(item_at(is, p, cid, rank)), hf, qv);
   __syncthreads();
 
   if (!skip && (warp == 0 || warp == 10) && lane == 0) {
@@ -505,39 +594,16 @@ __global__ void __launch_bounds__(384, 1) attn_split_kernel(const __grid_constan
     if (!ok && lane == 0) set_status(p.status, TV_ERR_TIMEOUT);
   } else if (!skip && warp >= 2 && warp <= 9) {
     // ---------------- softmax / epilogue: warps 2-9, two warpgroups, one half tile each ----------------
-    const int hf = (warp - 2) >> 2;  // 0: slots 0-31, 1: slots 32-63
-    const int quad = warp & 3;
-    const int lrow = quad * 32 + lane;
     const uint32_t tl = tbase + (static_cast<uint32_t>(quad * 32) << 16);
     uint32_t t = 0;  // CTA-wide tile counter
     bool ok = true;
     for (int w = cid; w < total && ok; w += ncl) {
       const Item I = item_at(is, p, w, rank);
       const int n = I.t1 - I.t0;
-      const int row = I.rb * 128 + lrow;
-      const bool valid = row < is.rows[I.s];
-      // this half's Q columns (bf16 pairs) into TMEM; every QK^T of the
+      // this thread's Q share (bf16 pairs) into TMEM; every QK^T of the
       // previous item has completed (its S was read)
-      {
-        const uint4* q4 = nullptr;
-        if (valid) {
-          const int node = row / p.G, jh = row % p.G;
-          q4 = reinterpret_cast<const uint4*>(p.q + (static_cast<size_t>(is.off[I.s] + node) * p.Hq + I.g * p.G + jh) * D);
-        }
-#pragma unroll 1
-        for (int c0 = hf * (D / 4); c0 < (hf + 1) * (D / 4); c0 += 32) {
-          uint32_t r[32];
-#pragma unroll
-          for (int i = 0; i < 8; i++) {
-            const uint4 v = q4 ? q4[c0 / 4 + i] : make_uint4(0u, 0u, 0u, 0u);
-            r[4 * i] = v.x;
-            r[4 * i + 1] = v.y;
-            r[4 * i + 2] = v.z;
-            r[4 * i + 3] = v.w;
-          }
-          tmem_st32(tl + C::T_Q + c0, r);
-        }
-      }
+      if (w != cid) q_fetch<D>(q_row(I), hf, qv);
+      q_store<D>(tl + C::T_Q, hf, qv);
       tmem_st_wait();
       tc_fence_before();
       mbar_arrive(QREADY);
@@ -599,8 +665,14 @@ __global__ void __launch_bounds__(384, 1) attn_split_kernel(const __grid_constan
       }
       tc_fence_after();
       // the next item's first PV needs P of its first tile, which this
-      // warpgroup writes only after this read of O
-      store_state<D>(tl + C::T_O, valid ? ws_rec(p, I.s, I.g, I.split, row, D) : nullptr, hf, m, lh);
+      // warpgroup writes only after this read of O.  Every PV of the item is
+      // complete, so the P ring is free: warp k of the softmax turns its rows
+      // around in the ring's k-th 4 KB.
+      const int rbase = I.rb * 128 + quad * 32, nrows = is.rows[I.s];
+      store_state_warp<D>(tl + C::T_O, pring + static_cast<uint32_t>(warp - 2) * 4096u, hf, lane, m, lh,
+                          [&](int r) -> float* {
+                            return rbase + r < nrows ? ws_rec(p, I.s, I.g, I.split, rbase + r, D) : nullptr;
+                          });
     }
     if (!ok) set_status(p.status, TV_ERR_TIMEOUT);
   }
