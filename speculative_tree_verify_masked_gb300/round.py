@@ -92,11 +92,7 @@ class VerifyRound:
                 d["out"] = torch.empty((d["v"].shape[0], s.Hv, s.dv), dtype=s.kv_dtype, device=device)
                 d["layer"] = layer
                 self.gdn[li] = d
-        ws_bytes = 0
-        if self.attn:
-            first = next(iter(self.attn.values()))["layer"]
-            ws_bytes = B.tv_attn_workspace_bytes(self.plan, first, cfg.n_seq, self.tree.n_max, self.max_len)
-        self.ws = torch.empty(max(16, ws_bytes) // 4 + 4, dtype=torch.float32, device=device) if ws_bytes else None
+        self._alloc_ws()
         self.path = torch.full((cfg.n_seq, B.TV_MAX_PATH), -1, dtype=torch.int32, device=device)
         self.acc_len = torch.zeros(cfg.n_seq, dtype=torch.int32, device=device)
         self.bonus = torch.zeros(cfg.n_seq, dtype=torch.int32, device=device)
@@ -107,6 +103,22 @@ class VerifyRound:
             [self.attn[li]["v_t"] for li in al], [self.gdn[li]["layer"] for li in gl],
             [self.gdn[li]["k"] for li in gl], [self.gdn[li]["v"] for li in gl],
             [self.gdn[li]["alpha"] for li in gl], [self.gdn[li]["beta"] for li in gl])
+
+    def _alloc_ws(self):
+        ws_bytes = 0
+        if self.attn:
+            first = next(iter(self.attn.values()))["layer"]
+            ws_bytes = B.tv_attn_workspace_bytes(self.plan, first, self.cfg.n_seq, self.tree.n_max, self.max_len)
+        self.ws = (torch.empty(max(16, ws_bytes) // 4 + 4, dtype=torch.float32, device=self.device)
+                   if ws_bytes else None)
+
+    def set_split(self, split: int):
+        """Another plan (positions per KV split) and a workspace sized for it.
+        Graphs captured before hold the old plan and workspace."""
+        self.split = split
+        self.plan = B.plan(split)
+        self.ws = None
+        self._alloc_ws()
 
     # -- steps of the round -------------------------------------------------
     def prepare(self, stream=None):
