@@ -185,18 +185,48 @@ __global__ void __launch_bounds__(32 * GdnShape<LPR>::W) gdn_verify_kernel(const
   __syncthreads();
 
   T* out = static_cast<T*>(p.out);
+  // The next node's schedule entry, key, query, gates and values do not depend
+  // on the state: each step loads them for the step after, so only the state
+  // chain (dots, reduce-scatter, update) is on the critical path.
+  int e_nx = sch[0];
+  f2_t k_nx[8], q_nx[8];
+  float4 c_nx;
+  float v_nx[RPG];
+  {
+    const int node = e_nx & 0xFF;
+    load_row8_any<LPR>(k_nx, kb + static_cast<size_t>(node) * DK, j);
+    load_row8_any<LPR>(q_nx, qb + static_cast<size_t>(node) * DK, j);
+    c_nx = nc[node];
+#pragma unroll
+    for (int r = 0; r < RPG; r++) v_nx[r] = vb[node * R + gi * RPG + r];
+  }
   for (int step = 0; step < n; step++) {
-    const int e = sch[step];
+    const int e = e_nx;
     const int node = e & 0xFF, src = (e >> 8) & 0xFF, save = (e >> 16) & 0xFF;
     const bool has_children = (e >> 24) & 1;
+    f2_t k[8], q[8];
+#pragma unroll
+    for (int i = 0; i < 8; i++) {
+      k[i] = k_nx[i];
+      q[i] = q_nx[i];
+    }
+    const float4 c4 = c_nx;
+    float v[RPG];
+#pragma unroll
+    for (int r = 0; r < RPG; r++) v[r] = v_nx[r];
+    if (step + 1 < n) {
+      e_nx = sch[step + 1];
+      const int nn = e_nx & 0xFF;
+      load_row8_any<LPR>(k_nx, kb + static_cast<size_t>(nn) * DK, j);
+      load_row8_any<LPR>(q_nx, qb + static_cast<size_t>(nn) * DK, j);
+      c_nx = nc[nn];
+#pragma unroll
+      for (int r = 0; r < RPG; r++) v_nx[r] = vb[nn * R + gi * RPG + r];
+    }
     if (src) {
 #pragma unroll
       for (int r = 0; r < RPG; r++) load_row8<LPR>(st[r], slots + ((src - 1) * R + gi * RPG + r) * DK, j);
     }
-    f2_t k[8], q[8];
-    load_row8_any<LPR>(k, kb + static_cast<size_t>(node) * DK, j);
-    load_row8_any<LPR>(q, qb + static_cast<size_t>(node) * DK, j);
-    const float4 c4 = nc[node];
     float part[NV];
 #pragma unroll
     for (int r = 0; r < RPG; r++) {
@@ -208,7 +238,15 @@ __global__ void __launch_bounds__(32 * GdnShape<LPR>::W) gdn_verify_kernel(const
 #pragma unroll
     for (int r = 0; r < RPG; r++) {
       const float x = __shfl_sync(0xffffffffu, part[rs_index<LPR, NV>(2 * r)], rs_lane<LPR, NV>(2 * r), LPR);
-      c[r] = gdn_c(x, vb[node * R + gi * RPG + r], c4.x, c4.y);
+      c[r] = gdn_c(x, v[r], c4.x, c4.y);
+    }
+    if (has_children) {
+#pragma unroll
+      for (int r = 0; r < RPG; r++) gdn_update(st[r], k, c4.x, c[r]);
+    }
+    if (save) {
+#pragma unroll
+      for (int r = 0; r < RPG; r++) store_row8<LPR>(slots + ((save - 1) * R + gi * RPG + r) * DK, st[r], j);
     }
     // one lane holding y of a row writes that row's output
 #pragma unroll
@@ -229,14 +267,6 @@ __global__ void __launch_bounds__(32 * GdnShape<LPR>::W) gdn_verify_kernel(const
           out[(static_cast<size_t>(off + node) * p.Hv + h) * p.dv + rb * R + gi * RPG + r] =
               from_f32<T>(gdn_o(cr, c4.z, c4.x, part[i], p.scale));
       }
-    }
-    if (has_children) {
-#pragma unroll
-      for (int r = 0; r < RPG; r++) gdn_update(st[r], k, c4.x, c[r]);
-    }
-    if (save) {
-#pragma unroll
-      for (int r = 0; r < RPG; r++) store_row8<LPR>(slots + ((save - 1) * R + gi * RPG + r) * DK, st[r], j);
     }
   }
 }
