@@ -234,7 +234,9 @@ def run_ours(args, rank, world, local_rank):
     torch.cuda.set_device(local_rank)
     dev = f"cuda:{local_rank}"
     cfg = synth.workload(args.config)
-    r = VerifyRound(cfg, device=dev, split=args.split)
+    pool = B.KVPool(local_rank) if args.kv_pool else None
+    extra = {} if args.kv_window is None else {"cap_extra": args.kv_window - max(cfg.ctx_lens)}
+    r = VerifyRound(cfg, device=dev, split=args.split, kv_pool=pool, **extra)
     n_nodes = r.n_nodes
     acc_lens = [len(p) for p in r.expected_paths]
     nodes_per_round = sum(n_nodes)
@@ -393,8 +395,12 @@ def run_ours(args, rank, world, local_rank):
                    "Hk_Hv_dk_dv": [cfg.shapes.Hk, cfg.shapes.Hv, cfg.shapes.dk, cfg.shapes.dv],
                    "split": r.split, "timing": "CUDA-graph replay of whole rounds, CUDA events",
                    "l2": "no flush: every round streams inputs far larger than L2 (KV context per round)",
-                   "parallelism": f"replicas x{world}"},
+                   "parallelism": f"replicas x{world}",
+                   "kv": ("pool: address space reserved for the whole cache, 2 MiB pages committed for rows below "
+                          f"L + {r.kv_margin}" if pool else "static buffers"), "kv_window": r.cap},
         "us_per_round": round(ms * 1e3, 2),
+        **({"kv_pool": {"committed_bytes": pool.committed_bytes, "reserved_bytes": pool.reserved_bytes,
+                        "page_bytes": pool.page_bytes}} if pool else {}),
         "hbm": {"algorithmic_bytes_per_round": bytes_round, "achieved_gbs": round(round_gbs, 1),
                 "frac_of_measured": round(round_gbs / hbm_peak, 4), "frac_of_8tbs": round(round_gbs / SPEC_HBM_GBS, 4)},
         "eager_ms_per_step": round(eager_ms, 4),
@@ -462,6 +468,9 @@ def main():
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-clocks", action="store_true")
+    ap.add_argument("--kv-pool", action="store_true", help="attention caches from the KV pool (tv_kvpool_*)")
+    ap.add_argument("--kv-window", type=int, default=None,
+                    help="cache rows per sequence (default: the context plus 64)")
     args = ap.parse_args()
     args.warmup = max(3, args.warmup)
     world = int(os.environ.get("WORLD_SIZE", "1"))

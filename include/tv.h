@@ -22,11 +22,14 @@
  *          axis sliced by length.
  *  [PAR]   "Parallel requests", "Joint verify": several sequences' trees in
  *          one pass, the mixers running per sequence.
+ *  [POOL]  "Parallel requests", "The shared KV pool": whole windows reserved
+ *          as address space, 2 MiB pages committed as rows are written.
  *
  * Conventions shared by every call
  *  - Ownership: the caller allocates and owns every buffer (device memory
  *    unless marked host).  The library allocates nothing in these calls and
- *    keeps no pointer after a call returns.  Verify inputs (k_t, v_t, k, v,
+ *    keeps no pointer after a call returns (the tv_kvpool_* calls, below, are
+ *    the exception: an allocator the caller may use for its caches).  Verify inputs (k_t, v_t, k, v,
  *    alpha, beta) must stay alive until tv_commit_path has run on the stream.
  *  - Streams: every call only enqueues work on `stream` (a cudaStream_t; NULL
  *    is the legacy default stream) and never synchronises, so a whole round
@@ -282,6 +285,64 @@ tv_status tv_decode_step(const tv_plan* plan, const tv_attn_layer* attn, const t
 /* len[s] += by[s] (device [n_seq]) if `by` is non-NULL, else len[s] += inc. */
 tv_status tv_len_advance(int32_t* len, const int32_t* by, int32_t inc, int32_t n_seq,
                          tv_stream stream);
+
+/* ------------------------------------------------------------------------
+ * KV pool: address space reserved for a whole window, pages committed as
+ * rows are written
+ * ------------------------------------------------------------------------
+ * [POOL] "Parallel requests", "The shared KV pool": each KV tensor's full
+ * size is reserved as virtual addresses and physical pages are mapped only
+ * for the rows a sequence writes; the tensor keeps the static buffer's shape,
+ * dtype and strides, so every call above, every view and every captured CUDA
+ * graph is unchanged and the results are the same bits by construction.
+ * Commit rows (plus a margin) before a round writes them; a fresh page is
+ * zeroed; pages wholly past the rows a sequence still holds can be given back.
+ *
+ * These are the library's only allocating calls.  They are host calls made
+ * between rounds (mapping is not a stream operation and cannot be captured);
+ * a pool is internally locked, so threads may share one.  The caller must
+ * not release or destroy pages that queued work still reads or writes.
+ *
+ * A tensor laid out as n_heads blocks of `head_stride` bytes, each holding
+ * rows of `row_bytes` (a cache [Hkv][cap][D] has head_stride = cap * D * esize
+ * and row_bytes = D * esize), is reserved as one range of
+ * n_heads * head_stride bytes rounded up to whole pages. */
+typedef struct tv_kv_pool tv_kv_pool; /* opaque */
+
+/* Physical page size the pool would use on `device` for a request of
+ * page_bytes (0: 2 MiB), rounded up to the device's allocation granularity;
+ * 0 when the device does not support virtual memory management. */
+size_t tv_kvpool_page_bytes(int32_t device, size_t page_bytes);
+
+/* New pool for `device` (host call, no stream work).  *pool receives the
+ * handle.  TV_ERR_ARG for a NULL out pointer, TV_ERR_CUDA when the device
+ * or driver lacks virtual memory management. */
+tv_status tv_kvpool_create(int32_t device, size_t page_bytes, tv_kv_pool** pool);
+
+/* Reserve address space for one tensor of `bytes` (rounded up to pages) and
+ * return its base in *base (aligned to a page).  Nothing is mapped yet: the
+ * device must not touch a row before it is committed. */
+tv_status tv_kvpool_reserve(tv_kv_pool* pool, size_t bytes, void** base);
+
+/* Map and zero (on `stream`, ordered before later work on it) the pages that
+ * hold rows [0, rows) of every head of the tensor reserved at `base`; pages
+ * already mapped are left as they are.  TV_ERR_ARG for an unknown base or a
+ * row range outside the reservation, TV_ERR_CAPACITY when the device is out
+ * of memory (the pages mapped so far stay mapped). */
+tv_status tv_kvpool_commit_rows(tv_kv_pool* pool, void* base, int32_t n_heads, size_t head_stride,
+                                size_t row_bytes, int64_t rows, tv_stream stream);
+
+/* Give back the pages of the tensor at `base` that hold no row below
+ * `keep_rows` of any head. */
+tv_status tv_kvpool_release_rows(tv_kv_pool* pool, void* base, int32_t n_heads, size_t head_stride,
+                                 size_t row_bytes, int64_t keep_rows);
+
+/* Bytes of physical pages mapped, and of address space reserved, by the pool. */
+size_t tv_kvpool_committed_bytes(const tv_kv_pool* pool);
+size_t tv_kvpool_reserved_bytes(const tv_kv_pool* pool);
+
+/* Unmap and free every page and reservation of the pool, then the pool. */
+tv_status tv_kvpool_destroy(tv_kv_pool* pool);
 
 #ifdef __cplusplus
 }

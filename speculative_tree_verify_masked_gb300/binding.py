@@ -95,13 +95,31 @@ def lib():
         L.tv_attn_static_scratch_bytes.argtypes = []
         L.tv_attn_tree_verify_static.restype = c_int32
         L.tv_attn_tree_verify_static.argtypes = [P, A, T, vp, c_int32, vp, vp, vp, vp, c_float, vp]
+        L.tv_kvpool_page_bytes.restype = c_size_t
+        L.tv_kvpool_page_bytes.argtypes = [c_int32, c_size_t]
+        L.tv_kvpool_create.restype = c_int32
+        L.tv_kvpool_create.argtypes = [c_int32, c_size_t, POINTER(vp)]
+        L.tv_kvpool_reserve.restype = c_int32
+        L.tv_kvpool_reserve.argtypes = [vp, c_size_t, POINTER(vp)]
+        L.tv_kvpool_commit_rows.restype = c_int32
+        L.tv_kvpool_commit_rows.argtypes = [vp, vp, c_int32, c_size_t, c_size_t, ctypes.c_int64, vp]
+        L.tv_kvpool_release_rows.restype = c_int32
+        L.tv_kvpool_release_rows.argtypes = [vp, vp, c_int32, c_size_t, c_size_t, ctypes.c_int64]
+        L.tv_kvpool_committed_bytes.restype = c_size_t
+        L.tv_kvpool_committed_bytes.argtypes = [vp]
+        L.tv_kvpool_reserved_bytes.restype = c_size_t
+        L.tv_kvpool_reserved_bytes.argtypes = [vp]
+        L.tv_kvpool_destroy.restype = c_int32
+        L.tv_kvpool_destroy.argtypes = [vp]
         _lib = L
     return _lib
 
 
 EXPORTED = ["tv_status_string", "tv_version", "tv_tree_meta_bytes", "tv_tree_prepare", "tv_attn_workspace_bytes",
             "tv_attn_tree_verify", "tv_gdn_tree_verify", "tv_accept_path", "tv_commit_path", "tv_decode_step",
-            "tv_len_advance", "tv_attn_static_scratch_bytes", "tv_attn_tree_verify_static"]
+            "tv_len_advance", "tv_attn_static_scratch_bytes", "tv_attn_tree_verify_static", "tv_kvpool_page_bytes",
+            "tv_kvpool_create", "tv_kvpool_reserve", "tv_kvpool_commit_rows", "tv_kvpool_release_rows",
+            "tv_kvpool_committed_bytes", "tv_kvpool_reserved_bytes", "tv_kvpool_destroy"]
 
 
 def _check(code: int, where: str):
@@ -271,3 +289,105 @@ def tv_decode_step(pl, attn: AttnLayer | None, gdn: GdnLayer | None, n_seq, len_
 
 def tv_len_advance(len_, by, inc: int, n_seq: int, stream=None):
     _check(lib().tv_len_advance(_ptr(len_), _ptr(by), inc, n_seq, _stream(stream)), "tv_len_advance")
+
+
+# ---------------------------------------------------------------------------
+# KV pool
+# ---------------------------------------------------------------------------
+def tv_kvpool_page_bytes(device: int, page_bytes: int = 0) -> int:
+    return int(lib().tv_kvpool_page_bytes(device, page_bytes))
+
+
+def tv_kvpool_create(device: int, page_bytes: int = 0) -> c_void_p:
+    h = c_void_p()
+    _check(lib().tv_kvpool_create(device, page_bytes, ctypes.byref(h)), "tv_kvpool_create")
+    return h
+
+
+def tv_kvpool_reserve(pool, nbytes: int) -> int:
+    base = c_void_p()
+    _check(lib().tv_kvpool_reserve(pool, nbytes, ctypes.byref(base)), "tv_kvpool_reserve")
+    return int(base.value)
+
+
+def tv_kvpool_commit_rows(pool, base: int, n_heads: int, head_stride: int, row_bytes: int, rows: int, stream=None):
+    _check(lib().tv_kvpool_commit_rows(pool, c_void_p(base), n_heads, head_stride, row_bytes, rows, _stream(stream)),
+           "tv_kvpool_commit_rows")
+
+
+def tv_kvpool_release_rows(pool, base: int, n_heads: int, head_stride: int, row_bytes: int, keep_rows: int):
+    _check(lib().tv_kvpool_release_rows(pool, c_void_p(base), n_heads, head_stride, row_bytes, keep_rows),
+           "tv_kvpool_release_rows")
+
+
+def tv_kvpool_committed_bytes(pool) -> int:
+    return int(lib().tv_kvpool_committed_bytes(pool))
+
+
+def tv_kvpool_reserved_bytes(pool) -> int:
+    return int(lib().tv_kvpool_reserved_bytes(pool))
+
+
+def tv_kvpool_destroy(pool):
+    _check(lib().tv_kvpool_destroy(pool), "tv_kvpool_destroy")
+
+
+class _DeviceRange:
+    """A device address range presented to torch through the CUDA array
+    interface (torch keeps this object alive with the tensor)."""
+
+    def __init__(self, ptr: int, numel: int, typestr: str, pool):
+        self.pool = pool
+        self.__cuda_array_interface__ = {"shape": (numel,), "typestr": typestr, "data": (ptr, False),
+                                         "version": 3, "strides": None, "stream": None}
+
+
+class KVPool:
+    """Caches [H][cap][D] whose address space is reserved whole and whose
+    pages are committed as rows are written (tv_kvpool_*)."""
+
+    _TYPESTR = {torch.float32: "<f4", torch.bfloat16: "<i2", torch.float16: "<f2"}
+
+    def __init__(self, device: int = 0, page_bytes: int = 0):
+        self.device = device
+        self.h = tv_kvpool_create(device, page_bytes)
+        self.page_bytes = tv_kvpool_page_bytes(device, page_bytes)
+
+    def cache(self, heads: int, cap: int, dim: int, dtype: torch.dtype) -> torch.Tensor:
+        """A [heads, cap, dim] tensor over a fresh reservation; row 0 of every
+        head is committed (zeroed), nothing else."""
+        esize = torch.empty((), dtype=dtype).element_size()
+        numel = heads * cap * dim
+        base = tv_kvpool_reserve(self.h, numel * esize)
+        tv_kvpool_commit_rows(self.h, base, heads, cap * dim * esize, dim * esize, 1)
+        t = torch.as_tensor(_DeviceRange(base, numel, self._TYPESTR[dtype], self), device=f"cuda:{self.device}")
+        return t.view(dtype).view(heads, cap, dim)
+
+    @staticmethod
+    def _geom(t: torch.Tensor):
+        heads, cap, dim = t.shape
+        es = t.element_size()
+        return t.data_ptr(), heads, cap * dim * es, dim * es
+
+    def commit_rows(self, t: torch.Tensor, rows: int, stream=None):
+        base, heads, hs, rb = self._geom(t)
+        tv_kvpool_commit_rows(self.h, base, heads, hs, rb, rows, stream)
+
+    def release_rows(self, t: torch.Tensor, keep_rows: int):
+        base, heads, hs, rb = self._geom(t)
+        tv_kvpool_release_rows(self.h, base, heads, hs, rb, keep_rows)
+
+    @property
+    def committed_bytes(self) -> int:
+        return tv_kvpool_committed_bytes(self.h)
+
+    @property
+    def reserved_bytes(self) -> int:
+        return tv_kvpool_reserved_bytes(self.h)
+
+    def close(self):
+        """Frees every page and reservation: tensors from cache() must not be
+        used afterwards."""
+        if self.h is not None:
+            tv_kvpool_destroy(self.h)
+            self.h = None

@@ -48,7 +48,8 @@ def auto_split(ctx_lens, n_nodes, Hq, Hkv, num_sms, lo=512, hi=16384):
 
 class VerifyRound:
     def __init__(self, cfg: synth.Workload, device="cuda", split: int | None = None, layers=None,
-                 cap_extra: int = 64, overlap: bool = True):
+                 cap_extra: int = 64, overlap: bool = True, kv_pool: B.KVPool | None = None,
+                 kv_margin: int = 256, max_len: int | None = None):
         self.cfg = cfg
         self.device = device
         s = cfg.shapes
@@ -64,7 +65,9 @@ class VerifyRound:
         self.expected_paths = [t[3] for t in self.trees]
         self.len0 = torch.tensor(cfg.ctx_lens, dtype=torch.int32, device=device)
         self.len = self.len0.clone()
-        self.max_len = max(cfg.ctx_lens)
+        # host bound on the context lengths (above the first round's when
+        # rounds run without resetting the lengths); caches hold cap_extra more rows
+        self.max_len = max(cfg.ctx_lens) if max_len is None else max_len
         self.cap = self.max_len + cap_extra
         if split is None:
             sms = torch.cuda.get_device_properties(device).multi_processor_count
@@ -73,12 +76,23 @@ class VerifyRound:
         self.plan = B.plan(split)
         self._attn_marks = None  # events around attention layers while capturing
         self._graph_marks = None
+        # With a KV pool the caches are reserved whole and only the rows below
+        # the context length plus kv_margin are committed; the committed rows
+        # hold the same values as the static caches'.
+        self.kv_pool, self.kv_margin = kv_pool, kv_margin
         self.attn_scale = 1.0 / math.sqrt(s.D)
         self.gdn_scale = 1.0 / math.sqrt(s.dk)
         self.attn, self.gdn = {}, {}
         for li in self.layers:
             if cfg.is_attn(li):
                 per = [synth.attn_layer_inputs(cfg, li, q, self.n_nodes[q], self.cap, device) for q in range(cfg.n_seq)]
+                if kv_pool is not None:
+                    for q, x in enumerate(per):
+                        for name in ("K", "V"):
+                            t = kv_pool.cache(s.Hkv, self.cap, s.D, s.kv_dtype)
+                            kv_pool.commit_rows(t, min(self.cap, cfg.ctx_lens[q] + kv_margin))
+                            t[:, :cfg.ctx_lens[q]].copy_(x[name][:, :cfg.ctx_lens[q]])
+                            x[name] = t
                 layer = B.AttnLayer([x["K"] for x in per], [x["V"] for x in per], s.Hq)
                 q_ = torch.cat([x["q"] for x in per]).contiguous()
                 k_t = torch.cat([x["k_t"] for x in per]).contiguous()
@@ -119,6 +133,19 @@ class VerifyRound:
         self.plan = B.plan(split)
         self.ws = None
         self._alloc_ws()
+
+    def commit_kv(self, lens=None):
+        """Commit cache rows up to each sequence's length (default: read from
+        the device) plus kv_margin, ahead of the rounds that will write them.
+        A host call between rounds; no-op without a KV pool."""
+        if self.kv_pool is None:
+            return
+        lens = self.len.tolist() if lens is None else list(lens)
+        for a in self.attn.values():
+            for q in range(self.cfg.n_seq):
+                rows = min(self.cap, int(lens[q]) + self.kv_margin)
+                self.kv_pool.commit_rows(a["layer"].K[q], rows)
+                self.kv_pool.commit_rows(a["layer"].V[q], rows)
 
     # -- steps of the round -------------------------------------------------
     def prepare(self, stream=None):

@@ -172,3 +172,21 @@ def test_synthetic_trees_are_well_formed(cfg_id):
         assert max(depth) < B.TV_MAX_PATH
         assert len(tok) == len(greedy) == n
         assert path[0] == 0 and all(parent[b] == a for a, b in zip(path, path[1:]))
+
+
+def test_kvpool_host_errors(L):
+    """KV pool calls reject bad handles and arguments on the host; without a
+    GPU driver a pool cannot be created."""
+    import torch
+    vp = ctypes.c_void_p
+    assert L.tv_kvpool_create(0, 0, None) == 1
+    assert L.tv_kvpool_create(-1, 0, ctypes.byref(vp())) == 1
+    assert L.tv_kvpool_reserve(None, 16, ctypes.byref(vp())) == 1
+    assert L.tv_kvpool_commit_rows(None, vp(16), 1, 16, 16, 1, None) == 1
+    assert L.tv_kvpool_release_rows(None, vp(16), 1, 16, 16, 1) == 1
+    assert L.tv_kvpool_committed_bytes(None) == 0 and L.tv_kvpool_reserved_bytes(None) == 0
+    assert L.tv_kvpool_destroy(None) == 1
+    if not torch.cuda.is_available():
+        assert L.tv_kvpool_page_bytes(0, 0) == 0
+        h = vp()
+        assert L.tv_kvpool_create(0, 0, ctypes.byref(h)) == 7 and not h.value
