@@ -83,7 +83,7 @@ struct GdnCommitParams {
 template <typename T, int LPR>
 __global__ void __launch_bounds__(128) gdn_commit_kernel(const GdnCommitParams p) {
   pdl_wait();
-  constexpr int DK = 16 * LPR;
+  constexpr int DK = 2 * kPairs * LPR;
   constexpr int R = 128 / LPR;
   const int s = blockIdx.y, li = blockIdx.z;
   const int rb_per_head = (p.dv + R - 1) / R;
@@ -119,19 +119,19 @@ __global__ void __launch_bounds__(128) gdn_commit_kernel(const GdnCommitParams p
   const int row = rb * R + r;
   const bool valid = row < p.dv;
   float* Srow = lay.S[s] + (static_cast<size_t>(h) * p.dv + (valid ? row : 0)) * DK;
-  f2_t st[8];
+  f2_t st[kPairs];
   if (valid) {
-    load_row8<LPR>(st, Srow, jl);
+    load_row<LPR>(st, Srow, jl);
   } else {
 #pragma unroll
-    for (int e = 0; e < 8; e++) st[e] = 0ull;
+    for (int e = 0; e < kPairs; e++) st[e] = 0ull;
   }
   for (int j = 0; j < a; j++) {
-    f2_t k[8];
-    load_row8<LPR>(k, kb[j], jl);
+    f2_t k[kPairs];
+    load_row<LPR>(k, kb[j], jl);
     gdn_row_step<LPR, false>(st, k, k, 0.f, vb[j][r], ab[j], bb[j], 0.f, true);
   }
-  if (valid) store_row8<LPR>(Srow, st, jl);
+  if (valid) store_row<LPR>(Srow, st, jl);
 }
 
 __global__ void commit_len_kernel(int32_t* len, const int32_t* acc_len, const int32_t* status, int n_seq) {
@@ -235,9 +235,11 @@ extern "C" tv_status tv_commit_path(const tv_tree* t, const int32_t* path, const
     p.dv = gdn[0].dv;
     const bool bf = gdn[0].dtype == TV_BF16;
     if (gdn[0].dk == 128) {
-      if (bf) launch_gdn_commit<__nv_bfloat16, 8>(p, n_seq, nl, st, ov); else launch_gdn_commit<float, 8>(p, n_seq, nl, st, ov);
+      constexpr int LPR = lanes_per_row<128>();
+      if (bf) launch_gdn_commit<__nv_bfloat16, LPR>(p, n_seq, nl, st, ov); else launch_gdn_commit<float, LPR>(p, n_seq, nl, st, ov);
     } else {
-      if (bf) launch_gdn_commit<__nv_bfloat16, 4>(p, n_seq, nl, st, ov); else launch_gdn_commit<float, 4>(p, n_seq, nl, st, ov);
+      constexpr int LPR = lanes_per_row<64>();
+      if (bf) launch_gdn_commit<__nv_bfloat16, LPR>(p, n_seq, nl, st, ov); else launch_gdn_commit<float, LPR>(p, n_seq, nl, st, ov);
     }
   }
   launch_k(ov, commit_len_kernel, dim3(1), dim3(32), 0, st, len, acc_len, static_cast<const int32_t*>(t->status),

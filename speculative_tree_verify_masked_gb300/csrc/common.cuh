@@ -33,6 +33,8 @@ struct SeqInfo {
   int32_t off;        // first global node index
   int32_t max_depth;  // deepest node
   int32_t max_slot;   // saved-state slots the recurrent traversal needs
+  int32_t n_seg;      // segments of the recurrent traversal (seg entries)
+  int32_t pad[3];
 };
 
 struct MetaView {
@@ -40,6 +42,7 @@ struct MetaView {
   uint64_t* anc;    // [n_total] ancestor-or-self bitmask (sequence-local bits)
   int32_t* depth;   // [n_total]
   int32_t* sched;   // [n_total] recurrent traversal, per sequence at off..off+n-1
+  int32_t* seg;     // [n_total] segments of the traversal, per sequence at off..off+n_seg-1
   int8_t* anc_at;   // [n_total][TV_MAX_PATH] local index of the ancestor at each depth
 };
 
@@ -47,7 +50,7 @@ __host__ __device__ inline size_t align16(size_t x) { return (x + 15) & ~static_
 
 __host__ __device__ inline size_t meta_bytes(int n_total) {
   const size_t n = static_cast<size_t>(n_total);
-  return align16(sizeof(SeqInfo) * TV_MAX_SEQ) + align16(8 * n) + 2 * align16(4 * n) +
+  return align16(sizeof(SeqInfo) * TV_MAX_SEQ) + align16(8 * n) + 3 * align16(4 * n) +
          align16(TV_MAX_PATH * n);
 }
 
@@ -63,16 +66,21 @@ __host__ __device__ inline MetaView meta_view(void* base, int n_total) {
   p += align16(4 * n);
   m.sched = reinterpret_cast<int32_t*>(p);
   p += align16(4 * n);
+  m.seg = reinterpret_cast<int32_t*>(p);
+  p += align16(4 * n);
   m.anc_at = reinterpret_cast<int8_t*>(p);
   return m;
 }
 
-// Recurrent traversal step: [0,8) local node, [8,16) source of the parent
-// state (0 = the state already in registers, 1+k = saved slot k),
-// [16,24) save after the step (0 = no, 1+k = slot k), bit 24 = node has children.
+// Recurrent traversal.  A visit: [0,8) local node, bit 24 = node has
+// children.  A segment of consecutive visits: [0,8) first visit, [8,16)
+// visits, [16,24) source of the state the segment starts from (0 = the state
+// already in registers, 1+k = saved slot k), [24,32) slot the state is saved
+// to after the segment's last visit (0 = none, 1+k = slot k).
 constexpr int kMaxSlots = 5;  // a tree of <= 64 nodes never needs more (see tree.cu)
-__host__ __device__ inline int32_t sched_encode(int node, int src, int save, int has_children) {
-  return node | (src << 8) | (save << 16) | (has_children << 24);
+__host__ __device__ inline int32_t visit_encode(int node, int has_children) { return node | (has_children << 24); }
+__host__ __device__ inline int32_t seg_encode(int first, int count, int src, int save) {
+  return first | (count << 8) | (src << 16) | (save << 24);
 }
 
 // ----------------------------------------------------------------------------
@@ -97,6 +105,12 @@ __device__ __forceinline__ float from_f32<float>(float x) { return x; }
 template <>
 __device__ __forceinline__ __nv_bfloat16 from_f32<__nv_bfloat16>(float x) {
   return __float2bfloat16_rn(x);
+}
+
+// Plain stores to global memory, as explicit global-space instructions.
+__device__ __forceinline__ void store_global(float* p, float v) { asm volatile("st.global.f32 [%0], %1;" ::"l"(p), "f"(v)); }
+__device__ __forceinline__ void store_global(__nv_bfloat16* p, __nv_bfloat16 v) {
+  asm volatile("st.global.b16 [%0], %1;" ::"l"(p), "h"(__bfloat16_as_ushort(v)));
 }
 
 // bf16 halves of a packed word, exactly

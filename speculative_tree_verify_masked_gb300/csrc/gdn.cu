@@ -1,21 +1,31 @@
 // Gated DeltaNet tree verify and single-token decode.
 //
 // Tree verify ("Adding a model", Gated DeltaNet layers; the gated delta rule
-// applied along every node's root path): a CTA of four warps owns
-// 4 * 4 * 32/LPR state rows of one value head of one sequence (the warps share
-// one staged copy of the tree's keys, queries and gates) and each warp walks
-// the tree in the order prepared by tv_tree_prepare.  A lane group of LPR lanes holds four
-// state rows, so each node's key and query, read once from shared memory (as
-// bf16), serve four rows, and the eight dot products of a step (s.k and s.q
-// of each row) are reduced together by one reduce-scatter.  The few states
-// that must outlive a subtree sit in shared-memory slots.  No per-node state
-// is written to memory: the kernel reads the committed state once and writes
-// one output value per (node, row).
+// applied along every node's root path).  A lane group of LPR lanes owns two
+// state rows of one value head of one sequence, each with the lane layout
+// and the step arithmetic of decode and commit (gdn_step.cuh), so a verified
+// row is the decoded row bit for bit by construction.  A CTA of two warps
+// owns 2 * 2 * 32/LPR consecutive rows of one value head and stages the
+// tree's keys and queries (bf16, by cp.async), gates and values once.  The
+// lane groups walk the tree in the order prepared by tv_tree_prepare, cut
+// into segments that restore a saved state only at their start and save one
+// only at their end, so the visits of a segment run without branches: a
+// leaf runs the same update with alpha = 1 and c = 0, which leaves the state
+// as it is (up to the sign of a zero element, which no later dot product can
+// see: every accumulator starts at +0), so its siblings still find their
+// parent's state in registers.  The few states that must outlive a subtree
+// sit in shared-memory slots.  No per-node state is written to memory: the
+// kernel reads the committed state once and writes one output value per
+// (node, row).
 //
-// Work per (node, row): two dot products of length dk and, for nodes with
-// children, one rank-1 update of the row, in packed fp32x2 arithmetic.  The
-// kernel is bound by the dependent chain of steps along the tree, not by the
-// 4 * Hv * dv * dk bytes of state it reads.
+// Bound.  The chain of steps along the tree, not the 4 * Hv * dv * dk bytes
+// of state, sets the layer's time.  A warp issues its step in order, so the
+// dependent pieces of a visit (shared-memory loads, packed fp32 FMAs at one
+// per two cycles, the butterfly over the group, the update) add up unless
+// the compiler can overlap them, which branches inside the loop prevent, or
+// another warp fills the gaps: eight rows per warp (16 columns per lane, two
+// rows per lane group, one 16-byte bf16 load per chunk serving both rows)
+// give a 48-head x 128-row layer 768 warps, about two per SM sub-partition.
 #include "common.cuh"
 #include "gdn_step.cuh"
 #include "host.hpp"
@@ -47,24 +57,22 @@ inline int slots_for(int n_max) {
 
 template <int LPR>
 struct GdnShape {
-  static constexpr int DK = 16 * LPR;  // key dim
-  static constexpr int NG = 32 / LPR;  // lane groups per warp
-  static constexpr int RPG = 4;        // state rows per lane group
-  static constexpr int W = 4;          // warps per CTA (one per SM sub-partition)
-  static constexpr int NGC = NG * W;   // lane groups per CTA
-  static constexpr int R = NGC * RPG;  // state rows per CTA
-  static constexpr int NV = 2 * RPG;   // dot products per step and group (s.k, s.q per row)
+  static constexpr int DK = 2 * kPairs * LPR;  // key dim
+  static constexpr int W = 2;                  // warps per CTA
+  static constexpr int NG = W * 32 / LPR;      // lane groups per CTA
+  static constexpr int RPG = 2;                // state rows per lane group
+  static constexpr int R = NG * RPG;           // state rows per CTA
 };
 
 // Shared memory: slots [n_slots][R][DK] f32 | keys, queries [n_max][DK] T |
-// (alpha, beta, k.q, -) [n_max] | v [n_max][R] f32 | schedule [n_max].
+// (alpha, beta, k.q, -) [n_max] | v [n_max][R] f32 | visits [n_max] | segments [n_max].
 template <typename T, int LPR>
 inline size_t gdn_verify_smem(int n_max, int n_slots) {
   using Sh = GdnShape<LPR>;
   const size_t n = static_cast<size_t>(n_max);
   size_t b = static_cast<size_t>(n_slots) * Sh::R * Sh::DK * 4;
   b += 2 * ((n * Sh::DK * sizeof(T) + 15) / 16 * 16);
-  b += n * 16 + n * Sh::R * 4 + n * 4;
+  b += n * 16 + n * Sh::R * 4 + 2 * n * 4;
   return b;
 }
 
@@ -75,28 +83,33 @@ __device__ __forceinline__ void cp_async16_g(void* dst, const void* src) {
 template <typename T, int LPR>
 __global__ void __launch_bounds__(32 * GdnShape<LPR>::W) gdn_verify_kernel(const GdnVerifyParams p) {
   using Sh = GdnShape<LPR>;
-  constexpr int DK = Sh::DK, R = Sh::R, RPG = Sh::RPG, NV = Sh::NV;
+  constexpr int DK = Sh::DK, R = Sh::R, NG = Sh::NG, NT = 32 * Sh::W;
   const int s = blockIdx.y;
   const int rb_per_head = (p.dv + R - 1) / R;
   const int h = blockIdx.x / rb_per_head;
   const int rb = blockIdx.x % rb_per_head;
-  const int tid = threadIdx.x, lane = tid & 31, j = lane % LPR;
-  const int gi = (tid >> 5) * Sh::NG + lane / LPR;  // lane group within the CTA
+  const int tid = threadIdx.x, j = tid % LPR;
+  const int gi = tid / LPR;                 // lane group within the CTA
+  const int row0 = rb * R + 2 * gi;         // the group's rows: row0, row0 + 1
+  const bool valid0 = row0 < p.dv, valid1 = row0 + 1 < p.dv;
 
-  // this group's four state rows first (they do not depend on the tree, and
-  // no kernel of the round before commit writes them), so their loads overlap
+  // this group's state rows first (they do not depend on the tree, and no
+  // kernel of the round before commit writes them), so their loads overlap
   // the previous kernel's end and everything up to the first step
-  f2_t st[RPG][8];
-  bool valid[RPG];
-#pragma unroll
-  for (int r = 0; r < RPG; r++) {
-    const int row = rb * R + gi * RPG + r;
-    valid[r] = row < p.dv;
-    if (valid[r]) {
-      load_row8<LPR>(st[r], p.S[s] + (static_cast<size_t>(h) * p.dv + row) * DK, j);
+  f2_t st0[kPairs], st1[kPairs];
+  {
+    const float* S = p.S[s] + static_cast<size_t>(h) * p.dv * DK;
+    if (valid0) {
+      load_row<LPR>(st0, S + static_cast<size_t>(row0) * DK, j);
     } else {
 #pragma unroll
-      for (int e = 0; e < 8; e++) st[r][e] = 0ull;
+      for (int e = 0; e < kPairs; e++) st0[e] = 0ull;
+    }
+    if (valid1) {
+      load_row<LPR>(st1, S + static_cast<size_t>(row0 + 1) * DK, j);
+    } else {
+#pragma unroll
+      for (int e = 0; e < kPairs; e++) st1[e] = 0ull;
     }
   }
   pdl_wait();  // tree tables, status and node inputs come from earlier kernels
@@ -104,8 +117,8 @@ __global__ void __launch_bounds__(32 * GdnShape<LPR>::W) gdn_verify_kernel(const
   MetaView mv = meta_view(const_cast<void*>(p.meta), p.n_total);
   const SeqInfo info = mv.seq[s];
   if (status_bad(p.status)) return;
-  const int n = info.n, off = info.off;
-  if (n <= 0 || n > p.n_max) return;
+  const int n = info.n, off = info.off, n_seg = info.n_seg;
+  if (n <= 0 || n > p.n_max || n_seg < 1 || n_seg > n) return;
   if (info.max_slot > p.n_slots) {
     if (tid == 0) set_status(p.status, TV_ERR_TREE);
     return;
@@ -119,154 +132,149 @@ __global__ void __launch_bounds__(32 * GdnShape<LPR>::W) gdn_verify_kernel(const
   T* qb = reinterpret_cast<T*>(reinterpret_cast<uint8_t*>(kb) + kq_bytes);
   float4* nc = reinterpret_cast<float4*>(reinterpret_cast<uint8_t*>(qb) + kq_bytes);  // [n_max]
   float* vb = reinterpret_cast<float*>(nc + p.n_max);                                // [n_max][R]
-  int* sch = reinterpret_cast<int*>(vb + static_cast<size_t>(p.n_max) * R);          // [n_max]
+  int* sch = reinterpret_cast<int*>(vb + static_cast<size_t>(p.n_max) * R);          // [n_max] visits
+  int* sgt = sch + p.n_max;                                                           // [n_max] segments
 
-  // stage the tree's keys and queries of this key head (raw, asynchronously),
-  // then the values of this CTA's rows, alpha, beta and the traversal, with
-  // every load issued before any is used
+  // Stage the tree's keys and queries of this key head (cp.async), the
+  // values of this CTA's rows, alpha, beta and the steps.  Every global load
+  // goes into registers (or a cp.async) before any shared-memory store, so
+  // the stage costs one memory round trip.
   {
-    constexpr int CPR = DK * static_cast<int>(sizeof(T)) / 16;  // 16-byte chunks per key row
-    const T* qg = static_cast<const T*>(p.q);
     const T* kg = static_cast<const T*>(p.k);
-    for (int idx = tid; idx < n * CPR; idx += blockDim.x) {
-      const size_t src = (static_cast<size_t>(off + idx / CPR) * p.Hk + g) * DK + (idx % CPR) * (16 / sizeof(T));
-      cp_async16_g(kb + static_cast<size_t>(idx / CPR) * DK + (idx % CPR) * (16 / sizeof(T)), kg + src);
-      cp_async16_g(qb + static_cast<size_t>(idx / CPR) * DK + (idx % CPR) * (16 / sizeof(T)), qg + src);
+    const T* qg = static_cast<const T*>(p.q);
+    const T* vg = static_cast<const T*>(p.v);
+    constexpr int CPR = DK * static_cast<int>(sizeof(T)) / 16;  // 16-byte chunks of a row
+    constexpr int EPC = 16 / static_cast<int>(sizeof(T));       // elements per chunk
+    for (int idx = tid; idx < n * CPR; idx += NT) {
+      const int node = idx / CPR, c = idx % CPR;
+      const size_t src = (static_cast<size_t>(off + node) * p.Hk + g) * DK + c * EPC;
+      cp_async16_g(kb + static_cast<size_t>(node) * DK + c * EPC, kg + src);
+      cp_async16_g(qb + static_cast<size_t>(node) * DK + c * EPC, qg + src);
     }
     asm volatile("cp.async.commit_group;" ::: "memory");
-    const T* vg = static_cast<const T*>(p.v);
-    for (int base = tid; base < n * R; base += 16 * blockDim.x) {
-      float vv[16];
+    constexpr int UV = (32 * R + NT - 1) / NT;  // values of a 32-node tree in one batch
+    float vv[UV];
 #pragma unroll
-      for (int u = 0; u < 16; u++) {
-        const int idx = base + u * blockDim.x;
-        const int row = rb * R + idx % R;
-        vv[u] = (idx < n * R && row < p.dv)
-                    ? to_f32(vg[(static_cast<size_t>(off + idx / R) * p.Hv + h) * p.dv + row])
-                    : 0.f;
-      }
-#pragma unroll
-      for (int u = 0; u < 16; u++)
-        if (base + u * blockDim.x < n * R) vb[base + u * blockDim.x] = vv[u];
+    for (int u = 0; u < UV; u++) {
+      const int idx = tid + u * NT;
+      const int rr = rb * R + idx % R;
+      vv[u] = (idx < n * R && rr < p.dv) ? to_f32(vg[(static_cast<size_t>(off + idx / R) * p.Hv + h) * p.dv + rr])
+                                         : 0.f;
     }
-    for (int idx = tid; idx < n; idx += blockDim.x) {
+    float a = 0.f, b = 0.f;
+    int e = 0, rde = 0;
+    if (tid < n) {
+      const size_t ah = static_cast<size_t>(off + tid) * p.Hv + h;
+      a = p.alpha[ah];
+      b = p.beta[ah];
+      e = mv.sched[off + tid];
+      rde = mv.seg[off + tid];
+    }
+#pragma unroll
+    for (int u = 0; u < UV; u++)
+      if (tid + u * NT < n * R) vb[tid + u * NT] = vv[u];
+    if (tid < n) {
+      nc[tid] = make_float4(a, b, 0.f, 0.f);
+      sch[tid] = e;
+      sgt[tid] = rde;
+    }
+    // values and gates of larger trees
+    for (int idx = UV * NT + tid; idx < n * R; idx += NT) {
+      const int rr = rb * R + idx % R;
+      vb[idx] = rr < p.dv ? to_f32(vg[(static_cast<size_t>(off + idx / R) * p.Hv + h) * p.dv + rr]) : 0.f;
+    }
+    for (int idx = NT + tid; idx < n; idx += NT) {
       const size_t ah = static_cast<size_t>(off + idx) * p.Hv + h;
-      const float a = p.alpha[ah], b = p.beta[ah];
+      nc[idx] = make_float4(p.alpha[ah], p.beta[ah], 0.f, 0.f);
       sch[idx] = mv.sched[off + idx];
-      nc[idx] = make_float4(a, b, 0.f, 0.f);
+      sgt[idx] = mv.seg[off + idx];
     }
     asm volatile("cp.async.wait_all;" ::: "memory");
     __syncthreads();
   }
-  // k . q of every node: each group takes eight nodes at a time, and one
-  // reduce-scatter finishes all of them
-  for (int base = 0; base < n; base += 8 * Sh::NGC) {
-    float part[8];
-#pragma unroll
-    for (int m = 0; m < 8; m++) {
-      const int node = base + gi * 8 + m;
-      part[m] = 0.f;
-      if (node < n) {
-        f2_t kk[8], qq[8];
-        load_row8_any<LPR>(kk, kb + static_cast<size_t>(node) * DK, j);
-        load_row8_any<LPR>(qq, qb + static_cast<size_t>(node) * DK, j);
-        part[m] = row_partial(kk, qq);
-      }
-    }
-    reduce_scatter<LPR, 8>(part, j);
-#pragma unroll
-    for (int i = 0; i < rs_count<LPR, 8>(); i++) {
-      const int m = rs_value<LPR, 8>(j, i);
-      const int node = base + gi * 8 + m;
-      const bool writer = rs_first<LPR, 8>(j);
-      if (writer && node < n) nc[node].z = part[i];
-    }
+  // k . q of every node, one node per lane group at a time (warp-uniform
+  // trip count, so every lane of a warp takes part in each butterfly)
+  for (int base = 0; base < n; base += NG) {
+    const int node = base + gi;
+    f2_t kk[kPairs], qq[kPairs];
+    const int src = node < n ? node : 0;
+    load_row_any<LPR>(kk, kb + static_cast<size_t>(src) * DK, j);
+    load_row_any<LPR>(qq, qb + static_cast<size_t>(src) * DK, j);
+    const float kq = kq_group<LPR>(kk, qq);
+    __syncwarp();
+    if (node < n && j == 0) nc[node].z = kq;
   }
   __syncthreads();
 
-  T* out = static_cast<T*>(p.out);
-  // The next node's schedule entry, key, query, gates and values do not depend
-  // on the state: each step loads them for the step after, so only the state
-  // chain (dots, reduce-scatter, update) is on the critical path.
-  int e_nx = sch[0];
-  f2_t k_nx[8], q_nx[8];
-  float4 c_nx;
-  float v_nx[RPG];
-  {
-    const int node = e_nx & 0xFF;
-    load_row8_any<LPR>(k_nx, kb + static_cast<size_t>(node) * DK, j);
-    load_row8_any<LPR>(q_nx, qb + static_cast<size_t>(node) * DK, j);
-    c_nx = nc[node];
-#pragma unroll
-    for (int r = 0; r < RPG; r++) v_nx[r] = vb[node * R + gi * RPG + r];
-  }
-  for (int step = 0; step < n; step++) {
-    const int e = e_nx;
-    const int node = e & 0xFF, src = (e >> 8) & 0xFF, save = (e >> 16) & 0xFF;
-    const bool has_children = (e >> 24) & 1;
-    f2_t k[8], q[8];
-#pragma unroll
-    for (int i = 0; i < 8; i++) {
-      k[i] = k_nx[i];
-      q[i] = q_nx[i];
+  T* out = static_cast<T*>(p.out) + (static_cast<size_t>(off) * p.Hv + h) * p.dv + row0;
+  float* slot0 = slots + static_cast<size_t>(2 * gi) * DK;  // the group's rows in slot 0
+  const size_t out_stride = static_cast<size_t>(p.Hv) * p.dv;
+  const bool pair_store = sizeof(T) == 2 && valid1 && (p.dv % 2) == 0;
+  // Outputs go out as explicit global stores: the compiler then knows they
+  // cannot alias the shared-memory tables and may issue the next visit's
+  // loads ahead of them.
+  auto put = [&](int node, float o0, float o1) {
+    T* dst = out + static_cast<size_t>(node) * out_stride;
+    if (pair_store) {
+      const uint32_t w = static_cast<uint32_t>(__bfloat16_as_ushort(__float2bfloat16_rn(o0))) |
+                         (static_cast<uint32_t>(__bfloat16_as_ushort(__float2bfloat16_rn(o1))) << 16);
+      asm volatile("st.global.b32 [%0], %1;" ::"l"(dst), "r"(w));
+    } else {
+      if (valid0) store_global(dst, from_f32<T>(o0));
+      if (valid1) store_global(dst + 1, from_f32<T>(o1));
     }
-    const float4 c4 = c_nx;
-    float v[RPG];
-#pragma unroll
-    for (int r = 0; r < RPG; r++) v[r] = v_nx[r];
-    if (step + 1 < n) {
-      e_nx = sch[step + 1];
-      const int nn = e_nx & 0xFF;
-      load_row8_any<LPR>(k_nx, kb + static_cast<size_t>(nn) * DK, j);
-      load_row8_any<LPR>(q_nx, qb + static_cast<size_t>(nn) * DK, j);
-      c_nx = nc[nn];
-#pragma unroll
-      for (int r = 0; r < RPG; r++) v_nx[r] = vb[nn * R + gi * RPG + r];
-    }
+  };
+  const float scale = p.scale;
+  for (int sg = 0; sg < n_seg; sg++) {
+    const int sw = sgt[sg];
+    const int first = sw & 0xFF, cnt = (sw >> 8) & 0xFF, src = (sw >> 16) & 0xFF, save = (sw >> 24) & 0xFF;
     if (src) {
-#pragma unroll
-      for (int r = 0; r < RPG; r++) load_row8<LPR>(st[r], slots + ((src - 1) * R + gi * RPG + r) * DK, j);
+      const float* sl = slot0 + static_cast<size_t>(src - 1) * R * DK;
+      load_row<LPR>(st0, sl, j);
+      load_row<LPR>(st1, sl + DK, j);
     }
-    float part[NV];
+    // the visits of the segment: no branch but the lane-0 store.  Each sum,
+    // c and o is formed exactly as gdn_row_step forms it.  The next visit's
+    // entry, key, query, gates and value are loaded during this one (the
+    // index clamped at the segment's end, so the loads need no branch).
+    const int last = first + cnt - 1;
+    int e = sch[first];
+    f2_t k[kPairs], q[kPairs];
+    load_row_any<LPR>(k, kb + static_cast<size_t>(e & 0xFF) * DK, j);
+    load_row_any<LPR>(q, qb + static_cast<size_t>(e & 0xFF) * DK, j);
+    float4 c4 = nc[e & 0xFF];
+    float2 v2 = *reinterpret_cast<const float2*>(vb + (e & 0xFF) * R + 2 * gi);
+#pragma unroll 2
+    for (int v = first; v <= last; v++) {
+      const int node = e & 0xFF;
+      const bool hc = (e >> 24) & 1;
+      const int en = sch[v < last ? v + 1 : last];
+      f2_t kn[kPairs], qn[kPairs];
+      load_row_any<LPR>(kn, kb + static_cast<size_t>(en & 0xFF) * DK, j);
+      load_row_any<LPR>(qn, qb + static_cast<size_t>(en & 0xFF) * DK, j);
+      const float4 c4n = nc[en & 0xFF];
+      const float2 v2n = *reinterpret_cast<const float2*>(vb + (en & 0xFF) * R + 2 * gi);
+      float d[4] = {row_partial(st0, k), row_partial(st0, q), row_partial(st1, k), row_partial(st1, q)};
+      group_sum_n<LPR, 4>(d);
+      const float c0 = gdn_c(d[0], v2.x, c4.x, c4.y), c1 = gdn_c(d[2], v2.y, c4.x, c4.y);
+      const float o0 = gdn_o(c0, c4.z, c4.x, d[1], scale), o1 = gdn_o(c1, c4.z, c4.x, d[3], scale);
+      const float au = hc ? c4.x : 1.f;
+      gdn_update(st0, k, au, hc ? c0 : 0.f);
+      gdn_update(st1, k, au, hc ? c1 : 0.f);
+      if (j == 0) put(node, o0, o1);
+      e = en;
 #pragma unroll
-    for (int r = 0; r < RPG; r++) {
-      part[2 * r] = row_partial(st[r], k);
-      part[2 * r + 1] = row_partial(st[r], q);
-    }
-    reduce_scatter<LPR, NV>(part, j);
-    float c[RPG];
-#pragma unroll
-    for (int r = 0; r < RPG; r++) {
-      const float x = __shfl_sync(0xffffffffu, part[rs_index<LPR, NV>(2 * r)], rs_lane<LPR, NV>(2 * r), LPR);
-      c[r] = gdn_c(x, v[r], c4.x, c4.y);
-    }
-    if (has_children) {
-#pragma unroll
-      for (int r = 0; r < RPG; r++) gdn_update(st[r], k, c4.x, c[r]);
+      for (int i = 0; i < kPairs; i++) {
+        k[i] = kn[i];
+        q[i] = qn[i];
+      }
+      c4 = c4n;
+      v2 = v2n;
     }
     if (save) {
-#pragma unroll
-      for (int r = 0; r < RPG; r++) store_row8<LPR>(slots + ((save - 1) * R + gi * RPG + r) * DK, st[r], j);
-    }
-    // one lane holding y of a row writes that row's output
-#pragma unroll
-    for (int i = 0; i < rs_count<LPR, NV>(); i++) {
-      const int m = rs_value<LPR, NV>(j, i);
-      const bool writer = rs_first<LPR, NV>(j);
-      if (writer && (m & 1)) {
-        const int r = m >> 1;
-        float cr = c[0];
-#pragma unroll
-        for (int rr = 1; rr < RPG; rr++)
-          if (rr == r) cr = c[rr];
-        bool vr = valid[0];
-#pragma unroll
-        for (int rr = 1; rr < RPG; rr++)
-          if (rr == r) vr = valid[rr];
-        if (vr)
-          out[(static_cast<size_t>(off + node) * p.Hv + h) * p.dv + rb * R + gi * RPG + r] =
-              from_f32<T>(gdn_o(cr, c4.z, c4.x, part[i], p.scale));
-      }
+      float* sl = slot0 + static_cast<size_t>(save - 1) * R * DK;
+      store_row<LPR>(sl, st0, j);
+      store_row<LPR>(sl + DK, st1, j);
     }
   }
 }
@@ -286,7 +294,7 @@ struct GdnDecodeParams {
 
 template <typename T, int LPR>
 __global__ void __launch_bounds__(128) gdn_decode_kernel(const GdnDecodeParams p) {
-  constexpr int DK = 16 * LPR;
+  constexpr int DK = 2 * kPairs * LPR;
   constexpr int R = 128 / LPR;
   const int s = blockIdx.y;
   const int rb_per_head = (p.dv + R - 1) / R;
@@ -308,22 +316,22 @@ __global__ void __launch_bounds__(128) gdn_decode_kernel(const GdnDecodeParams p
   const int row = rb * R + r;
   const bool valid = row < p.dv;
   float* Srow = p.S[s] + (static_cast<size_t>(h) * p.dv + (valid ? row : 0)) * DK;
-  f2_t st[8];
+  f2_t st[kPairs];
   if (valid) {
-    load_row8<LPR>(st, Srow, j);
+    load_row<LPR>(st, Srow, j);
   } else {
 #pragma unroll
-    for (int e = 0; e < 8; e++) st[e] = 0ull;
+    for (int e = 0; e < kPairs; e++) st[e] = 0ull;
   }
-  f2_t kk[8], qq[8];
-  load_row8<LPR>(kk, kb, j);
-  load_row8<LPR>(qq, qb, j);
+  f2_t kk[kPairs], qq[kPairs];
+  load_row<LPR>(kk, kb, j);
+  load_row<LPR>(qq, qb, j);
   const float kq = kq_group<LPR>(kk, qq);
   const size_t hi = static_cast<size_t>(s) * p.Hv + h;
   const float vv = valid ? to_f32(static_cast<const T*>(p.v)[hi * p.dv + row]) : 0.f;
   const float o = gdn_row_step<LPR, true>(st, kk, qq, kq, vv, p.alpha[hi], p.beta[hi], p.scale, true);
   if (valid) {
-    store_row8<LPR>(Srow, st, j);
+    store_row<LPR>(Srow, st, j);
     if (j == 0) static_cast<T*>(p.out)[hi * p.dv + row] = from_f32<T>(o);
   }
 }
@@ -343,8 +351,8 @@ static void launch_verify(const GdnVerifyParams& p, int n_seq, cudaStream_t st, 
     attrs = true;
   }
   const dim3 grid(p.Hv * ((p.dv + R - 1) / R), n_seq);
-  launch_k(ov, gdn_verify_kernel<T, LPR>, grid, dim3(32 * GdnShape<LPR>::W), gdn_verify_smem<T, LPR>(p.n_max, p.n_slots),
-           st, p);
+  launch_k(ov, gdn_verify_kernel<T, LPR>, grid, dim3(32 * GdnShape<LPR>::W),
+           gdn_verify_smem<T, LPR>(p.n_max, p.n_slots), st, p);
 }
 
 template <typename T, int LPR>
@@ -371,9 +379,11 @@ tv_status gdn_decode_launch(const tv_gdn_layer* l, int32_t n_seq, const void* q,
   p.Hk = l->Hk; p.Hv = l->Hv; p.dv = l->dv; p.scale = scale;
   const bool bf = l->dtype == TV_BF16;
   if (l->dk == 128) {
-    if (bf) launch_decode<__nv_bfloat16, 8>(p, n_seq, st); else launch_decode<float, 8>(p, n_seq, st);
+    constexpr int LPR = lanes_per_row<128>();
+    if (bf) launch_decode<__nv_bfloat16, LPR>(p, n_seq, st); else launch_decode<float, LPR>(p, n_seq, st);
   } else {
-    if (bf) launch_decode<__nv_bfloat16, 4>(p, n_seq, st); else launch_decode<float, 4>(p, n_seq, st);
+    constexpr int LPR = lanes_per_row<64>();
+    if (bf) launch_decode<__nv_bfloat16, LPR>(p, n_seq, st); else launch_decode<float, LPR>(p, n_seq, st);
   }
   return launch_status();
 }
@@ -406,9 +416,11 @@ extern "C" tv_status tv_gdn_tree_verify(const tv_gdn_layer* l, const tv_tree* t,
   const bool bf = l->dtype == TV_BF16;
   const bool ov = tree_overlap(t);
   if (l->dk == 128) {
-    if (bf) launch_verify<__nv_bfloat16, 8>(p, t->n_seq, st, ov); else launch_verify<float, 8>(p, t->n_seq, st, ov);
+    constexpr int LPR = lanes_per_row<128>();
+    if (bf) launch_verify<__nv_bfloat16, LPR>(p, t->n_seq, st, ov); else launch_verify<float, LPR>(p, t->n_seq, st, ov);
   } else {
-    if (bf) launch_verify<__nv_bfloat16, 4>(p, t->n_seq, st, ov); else launch_verify<float, 4>(p, t->n_seq, st, ov);
+    constexpr int LPR = lanes_per_row<64>();
+    if (bf) launch_verify<__nv_bfloat16, LPR>(p, t->n_seq, st, ov); else launch_verify<float, LPR>(p, t->n_seq, st, ov);
   }
   return launch_status();
 }

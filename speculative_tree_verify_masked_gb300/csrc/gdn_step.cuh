@@ -7,23 +7,29 @@
 //     c  = beta * (v_r - alpha * x)
 //     s' = alpha * s + c * k          (= alpha s (I - beta k k^T) + beta v_r k^T)
 //     o  = scale * (alpha * y + c * (k . q))   (= scale * s' . q)
-// A row is spread over LPR lanes, 16 elements each, held as 8 packed fp32
-// pairs: pair e of lane j covers columns ((e / 2) * LPR + j) * 4 + 2 (e % 2)
-// and the next one, so a lane group reads whole 16-byte chunks of the row.
-// The arithmetic uses the packed fp32x2 FMA / MUL instructions (two
+// A row is spread over LPR = dk / 16 lanes (a lane group), 16 elements each,
+// held as kPairs = 8 packed fp32 pairs: chunk c (pairs 4c .. 4c+3) of lane j
+// covers columns (c * LPR + j) * 8 .. +7, so a lane group reads LPR * 32
+// contiguous bytes of an fp32 row per chunk, and one 16-byte load brings a
+// lane a whole chunk of a bf16 key or query.
+//
+// The arithmetic uses the packed fp32x2 FMA / MUL / ADD instructions (two
 // independent IEEE round-to-nearest operations each); every operation is
-// explicit and in a fixed order.  A dot product is each lane's partial sum
-// followed by a butterfly over the group's lanes, lane distance LPR/2 first,
-// then halving; pairwise sums are commutative, so every lane of the group
-// gets the same bits.  reduce_scatter forms the same sums for several values
-// at once (each lane ends up with its share of the results) with one eighth
-// of the shuffles, and gives the same bits as eight separate butterflies.
+// explicit and in a fixed order.  A lane's partial dot product runs four
+// accumulators over its pairs (pair e into accumulator e % 4), adds them as
+// (a0 + a1) + (a2 + a3) and then the two halves of the pair; the group sum
+// is a butterfly over the group's lanes, lane distance LPR/2 first, then
+// halving.  Pairwise sums are commutative, so every lane of the group gets
+// the same bits.
 #pragma once
 #include "common.cuh"
 
 namespace tv {
 
 typedef unsigned long long f2_t;  // two fp32 values in one 64-bit register
+
+constexpr int kPairs = 8;            // packed pairs of a row per lane (16 elements)
+constexpr int kChunks = kPairs / 4;  // chunks of 8 columns of a row per lane
 
 __device__ __forceinline__ f2_t f2_fma(f2_t a, f2_t b, f2_t c) {
   f2_t d;
@@ -33,6 +39,11 @@ __device__ __forceinline__ f2_t f2_fma(f2_t a, f2_t b, f2_t c) {
 __device__ __forceinline__ f2_t f2_mul(f2_t a, f2_t b) {
   f2_t d;
   asm("mul.rn.f32x2 %0, %1, %2;" : "=l"(d) : "l"(a), "l"(b));
+  return d;
+}
+__device__ __forceinline__ f2_t f2_add(f2_t a, f2_t b) {
+  f2_t d;
+  asm("add.rn.f32x2 %0, %1, %2;" : "=l"(d) : "l"(a), "l"(b));
   return d;
 }
 __device__ __forceinline__ f2_t f2_dup(float x) {
@@ -53,93 +64,69 @@ __device__ __forceinline__ float group_sum(float x) {
   return x;
 }
 
-// Group sums of NV values v[0..NV) (each a per-lane partial), NV a power of
-// two.  At lane distance o, while a lane still holds more than one value, the
-// lanes with bit o set keep the upper half of their current values and the
-// others the lower half, each adding its partner's partial of the kept
-// values; once one value is left the step is a plain butterfly add.  Every
-// sum is formed exactly as group_sum forms it.  Afterwards lane j holds
-// rs_count<LPR, NV>() sums in v[0 ..): values j * (NV / LPR) + i when
-// NV >= LPR, else value j >> log2(LPR / NV).
-template <int LPR, int NV>
-__device__ __forceinline__ void reduce_scatter(float (&v)[NV], int j) {
-  int cnt = NV;
+// This lane's pairs of a dk-long fp32 row (global or shared memory).
+template <int LPR>
+__device__ __forceinline__ void load_row(f2_t (&d)[kPairs], const float* src, int j) {
 #pragma unroll
-  for (int o = LPR / 2; o >= 1; o >>= 1) {
-    if (cnt > 1) {
-      const int half = cnt / 2;
-      const bool up = (j & o) != 0;
-#pragma unroll
-      for (int m = 0; m < NV / 2; m++) {
-        if (m < half) {
-          const float send = up ? v[m] : v[m + half];
-          const float keep = up ? v[m + half] : v[m];
-          v[m] = __fadd_rn(keep, __shfl_xor_sync(0xffffffffu, send, o, LPR));
-        }
-      }
-      cnt = half;
-    } else {
-      v[0] = __fadd_rn(v[0], __shfl_xor_sync(0xffffffffu, v[0], o, LPR));
-    }
+  for (int c = 0; c < kChunks; c++) {
+    const ulonglong2* p = reinterpret_cast<const ulonglong2*>(src + (c * LPR + j) * 8);
+    const ulonglong2 v0 = p[0], v1 = p[1];
+    d[4 * c] = v0.x;
+    d[4 * c + 1] = v0.y;
+    d[4 * c + 2] = v1.x;
+    d[4 * c + 3] = v1.y;
   }
 }
-template <int LPR, int NV>
-__device__ __forceinline__ constexpr int rs_count() {
-  return NV >= LPR ? NV / LPR : 1;
-}
-// Lane (within the group) that holds value m after reduce_scatter, and the
-// index of that value in its v[].
-template <int LPR, int NV>
-__device__ __forceinline__ int rs_lane(int m) {
-  if constexpr (NV >= LPR) return m / (NV / LPR);
-  else return m * (LPR / NV);
-}
-template <int LPR, int NV>
-__device__ __forceinline__ int rs_index(int m) {
-  if constexpr (NV >= LPR) return m % (NV / LPR);
-  else return 0;
-}
-// Value held in v[i] by lane j after reduce_scatter, and whether lane j is
-// the first of the lanes that hold it.
-template <int LPR, int NV>
-__device__ __forceinline__ int rs_value(int j, int i) {
-  if constexpr (NV >= LPR) return j * (NV / LPR) + i;
-  else return j / (LPR / NV);
-}
-template <int LPR, int NV>
-__device__ __forceinline__ bool rs_first(int j) {
-  if constexpr (NV >= LPR) return true;
-  else return (j % (LPR / NV)) == 0;
+template <int LPR>
+__device__ __forceinline__ void store_row(float* dst, const f2_t (&s)[kPairs], int j) {
+#pragma unroll
+  for (int c = 0; c < kChunks; c++) {
+    ulonglong2* p = reinterpret_cast<ulonglong2*>(dst + (c * LPR + j) * 8);
+    p[0] = make_ulonglong2(s[4 * c], s[4 * c + 1]);
+    p[1] = make_ulonglong2(s[4 * c + 2], s[4 * c + 3]);
+  }
 }
 
-// This lane's 8 pairs of a dk-long fp32 row (global or shared memory).
+// Two bf16 (low half first) as a packed fp32 pair, exactly.
+__device__ __forceinline__ f2_t f2_from_bf16x2(uint32_t w) {
+  return (static_cast<f2_t>(w & 0xffff0000u) << 32) | static_cast<f2_t>(w << 16);
+}
+// This lane's pairs of a dk-long row stored as bf16 (same columns as load_row).
 template <int LPR>
-__device__ __forceinline__ void load_row8(f2_t (&d)[8], const float* src, int j) {
-  const ulonglong2* p = reinterpret_cast<const ulonglong2*>(src);
+__device__ __forceinline__ void load_row_bf16(f2_t (&d)[kPairs], const __nv_bfloat16* src, int j) {
 #pragma unroll
-  for (int c = 0; c < 4; c++) {
-    const ulonglong2 v = p[c * LPR + j];
-    d[2 * c] = v.x;
-    d[2 * c + 1] = v.y;
+  for (int c = 0; c < kChunks; c++) {
+    const uint4 v = *reinterpret_cast<const uint4*>(src + (c * LPR + j) * 8);
+    d[4 * c] = f2_from_bf16x2(v.x);
+    d[4 * c + 1] = f2_from_bf16x2(v.y);
+    d[4 * c + 2] = f2_from_bf16x2(v.z);
+    d[4 * c + 3] = f2_from_bf16x2(v.w);
   }
 }
 template <int LPR>
-__device__ __forceinline__ void store_row8(float* dst, const f2_t (&s)[8], int j) {
-  ulonglong2* p = reinterpret_cast<ulonglong2*>(dst);
-#pragma unroll
-  for (int c = 0; c < 4; c++) p[c * LPR + j] = make_ulonglong2(s[2 * c], s[2 * c + 1]);
+__device__ __forceinline__ void load_row_any(f2_t (&d)[kPairs], const float* src, int j) {
+  load_row<LPR>(d, src, j);
+}
+template <int LPR>
+__device__ __forceinline__ void load_row_any(f2_t (&d)[kPairs], const __nv_bfloat16* src, int j) {
+  load_row_bf16<LPR>(d, src, j);
 }
 
 // This lane's partial of s . w.
-__device__ __forceinline__ float row_partial(const f2_t (&s)[8], const f2_t (&w)[8]) {
-  f2_t acc = 0ull;  // (+0.0f, +0.0f)
+__device__ __forceinline__ float row_partial(const f2_t (&s)[kPairs], const f2_t (&w)[kPairs]) {
+  f2_t a0 = 0ull, a1 = 0ull, a2 = 0ull, a3 = 0ull;  // (+0.0f, +0.0f)
 #pragma unroll
-  for (int e = 0; e < 8; e++) acc = f2_fma(s[e], w[e], acc);
-  return f2_hsum(acc);
+  for (int e = 0; e < kPairs; e += 4) {
+    a0 = f2_fma(s[e], w[e], a0);
+    a1 = f2_fma(s[e + 1], w[e + 1], a1);
+    a2 = f2_fma(s[e + 2], w[e + 2], a2);
+    a3 = f2_fma(s[e + 3], w[e + 3], a3);
+  }
+  return f2_hsum(f2_add(f2_add(a0, a1), f2_add(a2, a3)));
 }
 
 template <int LPR>
-__device__ __forceinline__ float row_dot(const f2_t (&s)[8], const f2_t (&w)[8]) {
+__device__ __forceinline__ float row_dot(const f2_t (&s)[kPairs], const f2_t (&w)[kPairs]) {
   return group_sum<LPR>(row_partial(s, w));
 }
 
@@ -150,45 +137,43 @@ __device__ __forceinline__ float gdn_c(float x, float v, float alpha, float beta
 __device__ __forceinline__ float gdn_o(float c, float kq, float alpha, float y, float scale) {
   return __fmul_rn(scale, __fmaf_rn(c, kq, __fmul_rn(alpha, y)));
 }
-__device__ __forceinline__ void gdn_update(f2_t (&s)[8], const f2_t (&k)[8], float alpha, float c) {
+__device__ __forceinline__ void gdn_update(f2_t (&s)[kPairs], const f2_t (&k)[kPairs], float alpha, float c) {
   const f2_t a2 = f2_dup(alpha), c2 = f2_dup(c);
 #pragma unroll
-  for (int e = 0; e < 8; e++) s[e] = f2_fma(c2, k[e], f2_mul(a2, s[e]));
+  for (int e = 0; e < kPairs; e++) s[e] = f2_fma(c2, k[e], f2_mul(a2, s[e]));
 }
 
-// Two bf16 (low half first) as a packed fp32 pair, exactly.
-__device__ __forceinline__ f2_t f2_from_bf16x2(uint32_t w) {
-  return (static_cast<f2_t>(w & 0xffff0000u) << 32) | static_cast<f2_t>(w << 16);
-}
-// This lane's 8 pairs of a dk-long row stored as bf16 (same columns as load_row8).
-template <int LPR>
-__device__ __forceinline__ void load_row8_bf16(f2_t (&d)[8], const __nv_bfloat16* src, int j) {
-  const uint2* p = reinterpret_cast<const uint2*>(src);
+// Group sums of N values, their butterflies interleaved level by level
+// (each sum formed exactly as group_sum forms it).
+template <int LPR, int N>
+__device__ __forceinline__ void group_sum_n(float (&x)[N]) {
 #pragma unroll
-  for (int c = 0; c < 4; c++) {
-    const uint2 v = p[c * LPR + j];
-    d[2 * c] = f2_from_bf16x2(v.x);
-    d[2 * c + 1] = f2_from_bf16x2(v.y);
+  for (int o = LPR / 2; o >= 1; o >>= 1) {
+    float t[N];
+#pragma unroll
+    for (int i = 0; i < N; i++) t[i] = __shfl_xor_sync(0xffffffffu, x[i], o, LPR);
+#pragma unroll
+    for (int i = 0; i < N; i++) x[i] = __fadd_rn(x[i], t[i]);
   }
-}
-template <int LPR>
-__device__ __forceinline__ void load_row8_any(f2_t (&d)[8], const float* src, int j) {
-  load_row8<LPR>(d, src, j);
-}
-template <int LPR>
-__device__ __forceinline__ void load_row8_any(f2_t (&d)[8], const __nv_bfloat16* src, int j) {
-  load_row8_bf16<LPR>(d, src, j);
 }
 
 // One token for one state row, with this lane's pairs of the token's key k
 // and query q already in registers and kq = k . q (from kq_group).  Returns
-// o when WITH_OUT; advances s when `update`.
+// o when WITH_OUT; advances s when `update`.  Both dot products are formed
+// before either butterfly.
 template <int LPR, bool WITH_OUT>
-__device__ __forceinline__ float gdn_row_step(f2_t (&s)[8], const f2_t (&k)[8], const f2_t (&q)[8], float kq, float v,
-                                              float alpha, float beta, float scale, bool update) {
-  const float x = row_dot<LPR>(s, k);
+__device__ __forceinline__ float gdn_row_step(f2_t (&s)[kPairs], const f2_t (&k)[kPairs], const f2_t (&q)[kPairs],
+                                              float kq, float v, float alpha, float beta, float scale, bool update) {
+  float x = row_partial(s, k);
   float y = 0.f;
-  if (WITH_OUT) y = row_dot<LPR>(s, q);
+  if (WITH_OUT) {
+    float xy[2] = {x, row_partial(s, q)};
+    group_sum_n<LPR, 2>(xy);
+    x = xy[0];
+    y = xy[1];
+  } else {
+    x = group_sum<LPR>(x);
+  }
   const float c = gdn_c(x, v, alpha, beta);
   float o = 0.f;
   if (WITH_OUT) o = gdn_o(c, kq, alpha, y, scale);
@@ -199,8 +184,14 @@ __device__ __forceinline__ float gdn_row_step(f2_t (&s)[8], const f2_t (&k)[8], 
 // k . q of one token, by one lane group with the row layout (the same
 // reduction as a row dot), so every caller gets the same bits.
 template <int LPR>
-__device__ __forceinline__ float kq_group(const f2_t (&k)[8], const f2_t (&q)[8]) {
+__device__ __forceinline__ float kq_group(const f2_t (&k)[kPairs], const f2_t (&q)[kPairs]) {
   return row_dot<LPR>(k, q);
+}
+
+// Lanes per row for a key dimension (dk = 64 or 128): 4 or 8.
+template <int DK>
+__host__ __device__ constexpr int lanes_per_row() {
+  return DK / (2 * kPairs);
 }
 
 }  // namespace tv

@@ -20,6 +20,12 @@
 // nodes needs at most floor(log2(n / 5)) + 1 slots: 4 for 64 nodes.  The order
 // never changes any node's arithmetic: each state is exactly one step from its
 // parent's.
+//
+// Segments.  The walk is cut into runs of visits that neither restore nor
+// save a state inside: a run starts at a visit whose parent state comes from
+// a slot and ends after a visit whose state must be saved, so a kernel
+// walking the tree handles slots only between runs and runs the visits of a
+// run without branches.
 #include "common.cuh"
 #include "host.hpp"
 
@@ -33,7 +39,7 @@ __device__ __forceinline__ int child_class(int c, const int* nch, const int* hea
 
 __device__ __forceinline__ void tree_invalid(MetaView& mv, int s, int off, int32_t* status) {
   set_status(status, TV_ERR_TREE);
-  mv.seq[s] = SeqInfo{0, off, 0, 0};
+  mv.seq[s] = SeqInfo{0, off, 0, 0, 0, {0, 0, 0}};
 }
 
 __global__ void __launch_bounds__(32) tree_prepare_kernel(const int32_t* __restrict__ node_off,
@@ -44,6 +50,7 @@ __global__ void __launch_bounds__(32) tree_prepare_kernel(const int32_t* __restr
   const int lane = threadIdx.x;
   __shared__ int par[TV_MAX_NODES], nch[TV_MAX_NODES], nnl[TV_MAX_NODES], size[TV_MAX_NODES];
   __shared__ int hkey[TV_MAX_NODES], heavy[TV_MAX_NODES], rel[TV_MAX_NODES], first_light[TV_MAX_NODES];
+  __shared__ int vsrc[TV_MAX_NODES], vsave[TV_MAX_NODES];  // the walk's slot use, in visit order
   MetaView mv = meta_view(meta, n_total);
   const int off = node_off[s];
   const int end = node_off[s + 1];
@@ -150,17 +157,33 @@ __global__ void __launch_bounds__(32) tree_prepare_kernel(const int32_t* __restr
       my_slot = lv > my_slot ? lv : my_slot;
     }
     if (lv >= kMaxSlots) good = false;
-    mv.sched[off + pos] = sched_encode(i, src, save, nch[i] > 0 ? 1 : 0);
+    mv.sched[off + pos] = visit_encode(i, nch[i] > 0 ? 1 : 0);
+    vsrc[pos] = src;
+    vsave[pos] = save;
   }
   if (!__all_sync(0xffffffffu, good)) {
     if (lane == 0) tree_invalid(mv, s, off, status);
     return;
   }
+  __syncwarp();
+  // cut the walk into segments (one lane; at most 64 visits)
+  int n_seg = 0;
+  if (lane == 0) {
+    int first = 0;
+    for (int v = 1; v <= n; v++) {
+      if (v == n || vsrc[v] != 0 || vsave[v - 1] != 0) {
+        mv.seg[off + n_seg] = seg_encode(first, v - first, vsrc[first], vsave[v - 1]);
+        n_seg++;
+        first = v;
+      }
+    }
+  }
+  n_seg = __shfl_sync(0xffffffffu, n_seg, 0);
   for (int o = 16; o >= 1; o >>= 1) {
     my_depth = max(my_depth, __shfl_xor_sync(0xffffffffu, my_depth, o));
     my_slot = max(my_slot, __shfl_xor_sync(0xffffffffu, my_slot, o));
   }
-  if (lane == 0) mv.seq[s] = SeqInfo{n, off, my_depth, my_slot + 1};
+  if (lane == 0) mv.seq[s] = SeqInfo{n, off, my_depth, my_slot + 1, n_seg, {0, 0, 0}};
 }
 
 // Longest agreeing path plus one token ("One request, end to end" 2.6).
