@@ -208,6 +208,53 @@ tv_status tv_attn_tree_verify_static(const tv_plan* plan, const tv_attn_layer* l
                                      const void* v_t, void* out, float scale, tv_stream stream);
 
 /* ------------------------------------------------------------------------
+ * Attention front end: partial rotary embedding and the gated output
+ * ------------------------------------------------------------------------
+ * "Adding a model", "What is still specific to Qwen3.8": the model's
+ * attention has a gated output and partial rotary.  The pages give neither
+ * formula; the library takes the plainest reading:
+ *   rotary: the first rot_dims dimensions of every query and key head turn
+ *     as rot_dims/2 planes, plane j pairing dimension j with j + rot_dims/2
+ *     and turning by pos * theta^(-2j/rot_dims); the rest pass through;
+ *   position: a tree node at depth d sits at L + d, where decoding its root
+ *     path would put it (a decode token at L), so the key rows a commit
+ *     copies into the cache are rotated at their final positions;
+ *   gate: out = attention * sigmoid(gate), elementwise over [Hq][D].
+ * A row's bits depend only on its own inputs and position, so verified rows
+ * still equal decoded rows bit for bit. */
+
+/* Rotate the rows of one attention layer's queries and keys.
+ *  tree      verify: every node of the tree, at len[s] + depth(i); the
+ *            tree's status word receives device errors (n_seq, status unused)
+ *            or NULL: decode, one token per sequence at len[s] (n_seq tokens,
+ *            errors to *status)
+ *  len       device [n_seq] committed rows; max_len host bound (a larger
+ *            length sets TV_ERR_LEN and leaves the row unwritten)
+ *  q_raw     [rows][Hq][D], k_raw [rows][Hkv][D] in the layer's dtype;
+ *  q, k      outputs of the same shapes (may alias q_raw, k_raw)
+ *  rot_dims  even, 0 <= rot_dims <= D; theta > 1 finite
+ * Values need no rotation: pass the projection's values as v_t.
+ * Host-checkable errors return without enqueueing anything. */
+tv_status tv_attn_rope(const tv_attn_layer* layer, const tv_tree* tree, int32_t n_seq, const int32_t* len,
+                       int32_t max_len, int32_t rot_dims, float theta, const void* q_raw, const void* k_raw,
+                       void* q, void* k, int32_t* status, tv_stream stream);
+
+/* tv_attn_tree_verify with the output gate applied in the same kernel:
+ * out[i,h,:] = attention row * sigmoid(gate[i,h,:]); gate [n_total][Hq][D]
+ * in the layer's dtype, 16-byte aligned.  Other arguments as there. */
+tv_status tv_attn_tree_verify_gated(const tv_plan* plan, const tv_attn_layer* layer, const tv_tree* tree,
+                                    const int32_t* len, int32_t max_len, const void* q, const void* k_t,
+                                    const void* v_t, const void* gate, void* out, float scale, void* workspace,
+                                    size_t workspace_bytes, tv_stream stream);
+
+/* The attention half of tv_decode_step with the output gate applied in the
+ * same kernel (gate [n_seq][Hq][D]); appends each token's k, v at row len[s]. */
+tv_status tv_attn_decode_gated(const tv_plan* plan, const tv_attn_layer* attn, int32_t n_seq, const int32_t* len,
+                               int32_t max_len, const void* q, const void* k, const void* v, const void* gate,
+                               void* out, float scale, void* workspace, size_t workspace_bytes, int32_t* status,
+                               tv_stream stream);
+
+/* ------------------------------------------------------------------------
  * Gated DeltaNet: the gated delta rule along every node's ancestor path
  * ------------------------------------------------------------------------
  * [MODEL].  For value head h (key head g = h / (Hv/Hk)) and node i, with

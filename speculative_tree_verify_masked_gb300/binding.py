@@ -95,6 +95,13 @@ def lib():
         L.tv_attn_static_scratch_bytes.argtypes = []
         L.tv_attn_tree_verify_static.restype = c_int32
         L.tv_attn_tree_verify_static.argtypes = [P, A, T, vp, c_int32, vp, vp, vp, vp, c_float, vp]
+        L.tv_attn_rope.restype = c_int32
+        L.tv_attn_rope.argtypes = [A, T, c_int32, vp, c_int32, c_int32, c_float, vp, vp, vp, vp, vp, vp]
+        L.tv_attn_tree_verify_gated.restype = c_int32
+        L.tv_attn_tree_verify_gated.argtypes = [P, A, T, vp, c_int32, vp, vp, vp, vp, vp, c_float, vp, c_size_t, vp]
+        L.tv_attn_decode_gated.restype = c_int32
+        L.tv_attn_decode_gated.argtypes = [P, A, c_int32, vp, c_int32, vp, vp, vp, vp, vp, c_float, vp, c_size_t, vp,
+                                           vp]
         L.tv_kvpool_page_bytes.restype = c_size_t
         L.tv_kvpool_page_bytes.argtypes = [c_int32, c_size_t]
         L.tv_kvpool_create.restype = c_int32
@@ -119,7 +126,8 @@ EXPORTED = ["tv_status_string", "tv_version", "tv_tree_meta_bytes", "tv_tree_pre
             "tv_attn_tree_verify", "tv_gdn_tree_verify", "tv_accept_path", "tv_commit_path", "tv_decode_step",
             "tv_len_advance", "tv_attn_static_scratch_bytes", "tv_attn_tree_verify_static", "tv_kvpool_page_bytes",
             "tv_kvpool_create", "tv_kvpool_reserve", "tv_kvpool_commit_rows", "tv_kvpool_release_rows",
-            "tv_kvpool_committed_bytes", "tv_kvpool_reserved_bytes", "tv_kvpool_destroy"]
+            "tv_kvpool_committed_bytes", "tv_kvpool_reserved_bytes", "tv_kvpool_destroy", "tv_attn_rope",
+            "tv_attn_tree_verify_gated", "tv_attn_decode_gated"]
 
 
 def _check(code: int, where: str):
@@ -233,6 +241,33 @@ def tv_attn_tree_verify(pl, layer: AttnLayer, tree: Tree, len_, max_len, q, k_t,
                                      ctypes.byref(tree.c), _ptr(len_), max_len, _ptr(q), _ptr(k_t), _ptr(v_t),
                                      _ptr(out), scale, _ptr(ws), 0 if ws is None else ws.numel() * ws.element_size(),
                                      _stream(stream)), "tv_attn_tree_verify")
+
+
+def tv_attn_rope(layer: AttnLayer, tree: Tree | None, n_seq, len_, max_len, rot_dims, theta, q_raw, k_raw, q, k,
+                 status=None, stream=None):
+    """Rotary embedding of one layer's query and key rows at each row's
+    logical position (tree: L + depth; tree None: one decode token per
+    sequence at L)."""
+    _check(lib().tv_attn_rope(ctypes.byref(layer.c), ctypes.byref(tree.c) if tree is not None else None, n_seq,
+                              _ptr(len_), max_len, rot_dims, theta, _ptr(q_raw), _ptr(k_raw), _ptr(q), _ptr(k),
+                              _ptr(status), _stream(stream)), "tv_attn_rope")
+
+
+def tv_attn_tree_verify_gated(pl, layer: AttnLayer, tree: Tree, len_, max_len, q, k_t, v_t, gate, out, scale, ws,
+                              stream=None):
+    _check(lib().tv_attn_tree_verify_gated(ctypes.byref(pl) if pl is not None else None, ctypes.byref(layer.c),
+                                           ctypes.byref(tree.c), _ptr(len_), max_len, _ptr(q), _ptr(k_t), _ptr(v_t),
+                                           _ptr(gate), _ptr(out), scale, _ptr(ws),
+                                           0 if ws is None else ws.numel() * ws.element_size(), _stream(stream)),
+           "tv_attn_tree_verify_gated")
+
+
+def tv_attn_decode_gated(pl, attn: AttnLayer, n_seq, len_, max_len, q, k, v, gate, out, scale, ws, status,
+                         stream=None):
+    _check(lib().tv_attn_decode_gated(ctypes.byref(pl) if pl is not None else None, ctypes.byref(attn.c), n_seq,
+                                      _ptr(len_), max_len, _ptr(q), _ptr(k), _ptr(v), _ptr(gate), _ptr(out), scale,
+                                      _ptr(ws), 0 if ws is None else ws.numel() * ws.element_size(), _ptr(status),
+                                      _stream(stream)), "tv_attn_decode_gated")
 
 
 def tv_attn_static_scratch_bytes() -> int:

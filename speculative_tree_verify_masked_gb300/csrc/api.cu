@@ -84,3 +84,37 @@ extern "C" tv_status tv_decode_step(const tv_plan* plan, const tv_attn_layer* at
   if (attn->dtype == TV_F32) return attn_f32_launch(c, st);
   return attn_tc_launch(plan, c, ws, ws_bytes, st);
 }
+
+extern "C" tv_status tv_attn_tree_verify_gated(const tv_plan* plan, const tv_attn_layer* l, const tv_tree* t,
+                                               const int32_t* len, int32_t max_len, const void* q, const void* k_t,
+                                               const void* v_t, const void* gate, void* out, float scale, void* ws,
+                                               size_t ws_bytes, tv_stream stream) {
+  if (!tree_ok(t) || !len || !q || !k_t || !v_t || !gate || !out) return TV_ERR_ARG;
+  const tv_status ls = attn_layer_check(l, t->n_seq);
+  if (ls != TV_OK) return ls;
+  if (max_len < 0 || max_len > l->cap || !(scale > 0.f) || !std::isfinite(scale)) return TV_ERR_ARG;
+  if (!aligned16(len) || !aligned16(q) || !aligned16(k_t) || !aligned16(v_t) || !aligned16(gate) || !aligned16(out))
+    return TV_ERR_ALIGN;
+  AttnCall c{l, t->n_seq, t->n_total, t->n_max, t->node_off, t->meta, len, max_len, q, k_t, v_t, out, scale,
+             t->status, 0, tree_overlap(t), gate};
+  cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
+  if (l->dtype == TV_F32) return attn_f32_launch(c, st);
+  return attn_tc_launch(plan, c, ws, ws_bytes, st);
+}
+
+extern "C" tv_status tv_attn_decode_gated(const tv_plan* plan, const tv_attn_layer* attn, int32_t n_seq,
+                                          const int32_t* len, int32_t max_len, const void* q, const void* k,
+                                          const void* v, const void* gate, void* out, float scale, void* ws,
+                                          size_t ws_bytes, int32_t* status, tv_stream stream) {
+  if (n_seq < 1 || n_seq > TV_MAX_SEQ || !status || !q || !k || !v || !gate || !out || !len) return TV_ERR_ARG;
+  if (!aligned16(status)) return TV_ERR_ALIGN;
+  const tv_status ls = attn_layer_check(attn, n_seq);
+  if (ls != TV_OK) return ls;
+  if (max_len < 0 || max_len > attn->cap || !(scale > 0.f) || !std::isfinite(scale)) return TV_ERR_ARG;
+  if (!aligned16(len) || !aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(gate) || !aligned16(out))
+    return TV_ERR_ALIGN;
+  AttnCall c{attn, n_seq, n_seq, 1, nullptr, nullptr, len, max_len, q, k, v, out, scale, status, 1, false, gate};
+  cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
+  if (attn->dtype == TV_F32) return attn_f32_launch(c, st);
+  return attn_tc_launch(plan, c, ws, ws_bytes, st);
+}

@@ -24,6 +24,7 @@ struct AttnF32Params {
   const float* kt;
   const float* vt;
   float* out;
+  const float* gate;  // output gate of the front end, or null
   const int32_t* len;
   const int32_t* node_off;
   const void* meta;
@@ -113,7 +114,11 @@ __global__ void __launch_bounds__(128) attn_f32_kernel(const AttnF32Params p) {
     m = m_new;
   }
 #pragma unroll
-  for (int c = 0; c < CPL; c++) p.out[static_cast<size_t>(row) * D + lane + 32 * c] = __fdiv_rn(acc[c], l);
+  for (int c = 0; c < CPL; c++) {
+    const size_t oi = static_cast<size_t>(row) * D + lane + 32 * c;
+    const float y = __fdiv_rn(acc[c], l);
+    p.out[oi] = p.gate ? gate_mul(y, p.gate[oi]) : y;
+  }
   if (p.decode && h % p.G == 0) {
     // append this token's key/value at row L of its KV head
     float* kd = p.K[s] + (static_cast<size_t>(g) * p.cap + L) * D;
@@ -141,6 +146,7 @@ tv_status attn_f32_launch(const AttnCall& a, cudaStream_t st) {
   p.kt = static_cast<const float*>(a.kt);
   p.vt = static_cast<const float*>(a.vt);
   p.out = static_cast<float*>(a.out);
+  p.gate = static_cast<const float*>(a.gate);
   p.len = a.len;
   p.node_off = a.node_off;
   p.meta = a.meta;

@@ -91,6 +91,7 @@ struct TcParams {
   const __nv_bfloat16* kt;
   const __nv_bfloat16* vt;
   __nv_bfloat16* out;
+  const __nv_bfloat16* gate;  // output gate of the front end, or null
   const int32_t* len;
   const int32_t* node_off;
   const void* meta;
@@ -1055,10 +1056,17 @@ __global__ void __launch_bounds__(256, 1) attn_tail_kernel(const __grid_constant
             o.w = __fmaf_rn(wgt, v.w, o.w);
           }
         }
+        const size_t oi = (static_cast<size_t>(node_g) * p.Hq + g * G + r) * D + 4 * c4;
+        float4 y = make_float4(__fdiv_rn(o.x, ls), __fdiv_rn(o.y, ls), __fdiv_rn(o.z, ls), __fdiv_rn(o.w, ls));
+        if (p.gate) {
+          const uint2 gw = *reinterpret_cast<const uint2*>(p.gate + oi);
+          y = make_float4(gate_mul(y.x, bf16_lo(gw.x)), gate_mul(y.y, bf16_hi(gw.x)), gate_mul(y.z, bf16_lo(gw.y)),
+                          gate_mul(y.w, bf16_hi(gw.y)));
+        }
         uint2 packed;
-        packed.x = pack_bf16x2(__fdiv_rn(o.x, ls), __fdiv_rn(o.y, ls));
-        packed.y = pack_bf16x2(__fdiv_rn(o.z, ls), __fdiv_rn(o.w, ls));
-        *reinterpret_cast<uint2*>(p.out + (static_cast<size_t>(node_g) * p.Hq + g * G + r) * D + 4 * c4) = packed;
+        packed.x = pack_bf16x2(y.x, y.y);
+        packed.y = pack_bf16x2(y.z, y.w);
+        *reinterpret_cast<uint2*>(p.out + oi) = packed;
       }
       if (p.decode) {
         // append the token's own key/value at row L
@@ -1200,6 +1208,7 @@ tv_status attn_tc_launch(const tv_plan* plan, const AttnCall& a, void* ws, size_
   p.kt = static_cast<const __nv_bfloat16*>(a.kt);
   p.vt = static_cast<const __nv_bfloat16*>(a.vt);
   p.out = static_cast<__nv_bfloat16*>(a.out);
+  p.gate = static_cast<const __nv_bfloat16*>(a.gate);
   p.len = a.len;
   p.node_off = a.node_off;
   p.meta = a.meta;

@@ -107,6 +107,13 @@ __device__ __forceinline__ __nv_bfloat16 from_f32<__nv_bfloat16>(float x) {
   return __float2bfloat16_rn(x);
 }
 
+// Output gate of the attention front end: x * sigmoid(g), with the sigmoid
+// as 1 / (1 + e^-g) (CUDA's expf, IEEE add and divide); the same function for
+// verify and decode rows.
+__device__ __forceinline__ float gate_mul(float x, float g) {
+  return __fmul_rn(x, __fdiv_rn(1.f, __fadd_rn(1.f, expf(-g))));
+}
+
 // Plain stores to global memory, as explicit global-space instructions.
 __device__ __forceinline__ void store_global(float* p, float v) { asm volatile("st.global.f32 [%0], %1;" ::"l"(p), "f"(v)); }
 __device__ __forceinline__ void store_global(__nv_bfloat16* p, __nv_bfloat16 v) {

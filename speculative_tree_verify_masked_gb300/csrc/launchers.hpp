@@ -26,6 +26,7 @@ struct AttnCall {
   int32_t* status;
   int decode;
   bool overlap;  // programmatic dependent launch (TV_TREE_OVERLAP)
+  const void* gate = nullptr;  // [rows][Hq][D] in the KV type: out *= sigmoid(gate), or none
 };
 
 tv_status attn_f32_launch(const AttnCall& c, cudaStream_t st);

@@ -123,6 +123,31 @@ def test_host_argument_errors_need_no_device(L):
                             0.1, None, 0, vp(16), None) == 1
 
 
+def test_front_end_host_argument_errors(L):
+    """tv_attn_rope / the gated calls reject bad arguments before any launch."""
+    vp = ctypes.c_void_p
+    layer, keep = _bf16_layer()
+    st = vp(16)
+
+    def rope(lay, tree, n=1, ln=vp(16), ml=10, rot=64, th=1e7, q=vp(16), status=st):
+        return L.tv_attn_rope(lay, tree, n, ln, ml, rot, th, q, vp(16), vp(16), vp(16), status, None)
+
+    lay = ctypes.byref(layer)
+    assert rope(None, None) == 1
+    assert rope(lay, None, rot=63) == 1        # odd rotated dimensions
+    assert rope(lay, None, rot=512) == 1       # more than the head dimension
+    assert rope(lay, None, th=1.0) == 1        # base must exceed 1
+    assert rope(lay, None, status=None) == 1   # decode mode reports to a status word
+    assert rope(lay, None, n=0) == 1
+    assert rope(lay, None, q=vp(24)) == 4      # misaligned row
+    pl = B.tv_plan(512)
+    t = B.tv_tree(1, 4, 4, 0x1000, 0x2000, 0x3000, 0x4000)
+    assert L.tv_attn_tree_verify_gated(ctypes.byref(pl), lay, ctypes.byref(t), vp(16), 10, vp(16), vp(16), vp(16),
+                                       None, vp(16), 0.1, vp(16), 1 << 20, None) == 1   # gate required
+    assert L.tv_attn_decode_gated(ctypes.byref(pl), lay, 1, vp(16), 10, vp(16), vp(16), vp(16), vp(24), vp(16), 0.1,
+                                  vp(16), 1 << 20, vp(16), None) == 4
+
+
 def test_static_scratch_rejects_oversized_request_on_host(L):
     """The size check comes before any device call, so it runs here."""
     layer, keep = _bf16_layer(cap=40000)
