@@ -744,13 +744,60 @@ __global__ void __launch_bounds__(256, 1) attn_tail_kernel(const __grid_constant
     if (threadIdx.x < TV_MAX_PATH) anc_s[threadIdx.x] = threadIdx.x > depth ? node_g : off + a;
   }
   const int local = node_g - off;
-  // the split kernel before this one writes the workspace and may set the status
-  pdl_wait();
+  const int G = p.G;
+  // Set-up that needs nothing the split kernel writes: barriers, TMEM and,
+  // when they fit in the P tile area, the node's query rows and its first
+  // own tile (cache rows and tree rows), so that their loads overlap the
+  // split kernel's last CTAs.  The carried split state waits for it.
   if (threadIdx.x == 0) {
     mbar_init(BAR, 1);
     mbar_init(DRAIN, 1);
     mbar_init(MBAR, 1);
     fence_mbar_init();
+  }
+  if (warp == 0) {
+    tmem_alloc(smem_u32(tmem_slot), C::COLS);
+    tmem_relinquish();
+  }
+  const bool lok = L >= 0 && L <= p.max_len && !(p.decode && L >= p.cap);
+  const uint32_t qbytes = static_cast<uint32_t>(G * D * 2 + 15) & ~15u;
+  const bool early = lok && qbytes + static_cast<uint32_t>(G * C::REC * 4) <= static_cast<uint32_t>(C::PTILE);
+  const uint32_t qstage = early ? pbase : sb + C::TILE, ostage = early ? pbase + qbytes : sb;
+  const int P = L + depth + 1;
+  const int tsh = lok ? L / kTile : 0;
+  // the node's K/V tile t: cache rows below L, ancestors at L..L+d, zeros after
+  auto gather = [&](int t) {
+    for (int idx = threadIdx.x; idx < kTile * (D / 8); idx += blockDim.x) {
+      const int j = idx / (D / 8), cc = idx % (D / 8), pos = t * kTile + j;
+      const __nv_bfloat16* ksrc = p.kt;
+      const __nv_bfloat16* vsrc = p.vt;
+      bool have = false;
+      if (pos < L) {
+        const size_t r = (static_cast<size_t>(g) * p.cap + pos) * D + cc * 8;
+        ksrc = p.K[s] + r;
+        vsrc = p.V[s] + r;
+        have = true;
+      } else if (pos < P) {
+        const size_t r = (static_cast<size_t>(anc_s[pos - L]) * p.Hkv + g) * D + cc * 8;
+        ksrc = p.kt + r;
+        vsrc = p.vt + r;
+        have = true;
+      }
+      const int kb = cc >> 3, c = cc & 7;
+      const uint32_t o = kb * kBox + (j >> 3) * 1024 + (j & 7) * 128 + ((c ^ (j & 7)) << 4);
+      cp_async16(sb + o, ksrc, have);
+      cp_async16(sb + C::TILE + o, vsrc, have);
+    }
+  };
+  if (early) {
+    __syncthreads();  // anc_s
+    const __nv_bfloat16* qsrc = p.q + (static_cast<size_t>(node_g) * p.Hq + g * G) * D;
+    for (int idx = threadIdx.x; idx < G * D / 8; idx += blockDim.x) cp_async16(qstage + idx * 16, qsrc + idx * 8, true);
+    gather(tsh);
+  }
+  // the split kernel before this one writes the workspace and may set the status
+  pdl_wait();
+  if (threadIdx.x == 0) {
     int bad = status_bad(p.status) ? 1 : 0;
     if (!bad && (L < 0 || L > p.max_len)) {
       set_status(p.status, TV_ERR_LEN);
@@ -762,34 +809,30 @@ __global__ void __launch_bounds__(256, 1) attn_tail_kernel(const __grid_constant
     }
     skip = bad;
   }
-  if (warp == 0) {
-    tmem_alloc(smem_u32(tmem_slot), C::COLS);
-    tmem_relinquish();
-  }
   tc_fence_before();
   __syncthreads();
   tc_fence_after();
   const uint32_t tbase = *tmem_slot;
   const uint32_t tl = tbase + (static_cast<uint32_t>((warp & 3) * 32) << 16);
 
+  if (skip) cp_async_wait_all();  // copies issued before the wait land before the CTA leaves
   if (!skip) {
-    const int G = p.G;
-    const int P = L + depth + 1;
-    const int tsh = L / kTile, tlast = (L + depth) / kTile;
+    const int tlast = (L + depth) / kTile;
     const int ST = p.split_tiles;
     const bool vrow = lrow < G;
     const int row_seq = local * G + lrow;
     int cur = tsh / ST;
     const bool cont = (tsh % ST) != 0;  // the split kernel started this split
 
-    // stage this node's G query rows (V tile area) and, when continuing, the
-    // carried state records (K tile area) with cp.async
-    const uint32_t qstage = sb + C::TILE, ostage = sb;
-    const bool ostaged = G * C::REC * 4 <= C::TILE;
+    // stage this node's G query rows (unless staged early) and, when
+    // continuing, the carried state records with cp.async
+    const bool ostaged = early || G * C::REC * 4 <= C::TILE;
     {
-      const __nv_bfloat16* qsrc = p.q + (static_cast<size_t>(node_g) * p.Hq + g * G) * D;
-      for (int idx = threadIdx.x; idx < G * D / 8; idx += blockDim.x)
-        cp_async16(qstage + idx * 16, qsrc + idx * 8, true);
+      if (!early) {
+        const __nv_bfloat16* qsrc = p.q + (static_cast<size_t>(node_g) * p.Hq + g * G) * D;
+        for (int idx = threadIdx.x; idx < G * D / 8; idx += blockDim.x)
+          cp_async16(qstage + idx * 16, qsrc + idx * 8, true);
+      }
       if (cont && ostaged) {
         for (int idx = threadIdx.x; idx < G * C::REC / 4; idx += blockDim.x) {
           const int r = idx / (C::REC / 4), cc = idx % (C::REC / 4);
@@ -801,7 +844,7 @@ __global__ void __launch_bounds__(256, 1) attn_tail_kernel(const __grid_constant
     }
     // Q and the carried O into TMEM (each half its own columns)
     {
-      const uint4* qs = reinterpret_cast<const uint4*>(gb + C::TILE) + lrow * (D / 8);
+      const uint4* qs = reinterpret_cast<const uint4*>(gb + (qstage - sb)) + lrow * (D / 8);
 #pragma unroll 1
       for (int c0 = hf * (D / 4); c0 < (hf + 1) * (D / 4); c0 += 32) {
         uint32_t r[32];
@@ -819,7 +862,7 @@ __global__ void __launch_bounds__(256, 1) attn_tail_kernel(const __grid_constant
     float m = -INFINITY, lh = 0.f;
     bool fresh = true;
     if (cont) {
-      const float* rec = vrow ? (ostaged ? reinterpret_cast<const float*>(gb) + lrow * C::REC
+      const float* rec = vrow ? (ostaged ? reinterpret_cast<const float*>(gb + (ostage - sb)) + lrow * C::REC
                                          : ws_rec(p, s, g, cur, row_seq, D))
                               : nullptr;
 #pragma unroll 1
@@ -872,28 +915,8 @@ __global__ void __launch_bounds__(256, 1) attn_tail_kernel(const __grid_constant
         m = -INFINITY;
         lh = 0.f;
       }
-      // gather the node's K/V tile: cache rows below L, ancestors at L..L+d, zeros after
-      for (int idx = threadIdx.x; idx < kTile * (D / 8); idx += blockDim.x) {
-        const int j = idx / (D / 8), cc = idx % (D / 8), pos = t * kTile + j;
-        const __nv_bfloat16* ksrc = p.kt;
-        const __nv_bfloat16* vsrc = p.vt;
-        bool have = false;
-        if (pos < L) {
-          const size_t r = (static_cast<size_t>(g) * p.cap + pos) * D + cc * 8;
-          ksrc = p.K[s] + r;
-          vsrc = p.V[s] + r;
-          have = true;
-        } else if (pos < P) {
-          const size_t r = (static_cast<size_t>(anc_s[pos - L]) * p.Hkv + g) * D + cc * 8;
-          ksrc = p.kt + r;
-          vsrc = p.vt + r;
-          have = true;
-        }
-        const int kb = cc >> 3, c = cc & 7;
-        const uint32_t o = kb * kBox + (j >> 3) * 1024 + (j & 7) * 128 + ((c ^ (j & 7)) << 4);
-        cp_async16(sb + o, ksrc, have);
-        cp_async16(sb + C::TILE + o, vsrc, have);
-      }
+      // the node's K/V tile (the first one may have been gathered before the wait)
+      if (!(early && t == tsh)) gather(t);
       cp_async_wait_all();
       fence_proxy_async_smem();
       tc_fence_before();
@@ -1024,7 +1047,29 @@ __global__ void __launch_bounds__(256, 1) attn_tail_kernel(const __grid_constant
           for (int sp = 0; sp < ns; sp++) mm = fmaxf(mm, rec4(sp, r, D / 4).x);
         }
         float4 o = make_float4(0.f, 0.f, 0.f, 0.f);
-        if (wstaged) {
+        if (wstaged && nst == cur) {
+          // every split's record is in shared memory (the common case): plain
+          // shared loads the compiler can batch, accumulated in split order
+          const float4* st4 = reinterpret_cast<const float4*>(gb + (C::TAIL_FIXED - 1024)) + r * (C::REC / 4) + c4;
+#pragma unroll 4
+          for (int sp = 0; sp < cur; sp++) {
+            const float4 v = st4[static_cast<size_t>(sp) * G * (C::REC / 4)];
+            const float wgt = wsm[sp * G + r];
+            o.x = __fmaf_rn(wgt, v.x, o.x);
+            o.y = __fmaf_rn(wgt, v.y, o.y);
+            o.z = __fmaf_rn(wgt, v.z, o.z);
+            o.w = __fmaf_rn(wgt, v.w, o.w);
+          }
+          {
+            const float4 v = reinterpret_cast<const float4*>(mown + r * C::REC)[c4];
+            const float wgt = wsm[cur * G + r];
+            o.x = __fmaf_rn(wgt, v.x, o.x);
+            o.y = __fmaf_rn(wgt, v.y, o.y);
+            o.z = __fmaf_rn(wgt, v.z, o.z);
+            o.w = __fmaf_rn(wgt, v.w, o.w);
+          }
+          ls = ltot[r];
+        } else if (wstaged) {
           // up to 16 splits' partial rows in flight at a time, accumulated in split order
           for (int sp0 = 0; sp0 < ns; sp0 += 16) {
             float4 v[16];
