@@ -115,8 +115,10 @@ typedef struct {
  * verify, at exit elsewhere),
  * so everything older than the predecessor has completed.  Before waiting, a
  * kernel reads only the recurrent states (GDN verify), the lengths and
- * node_off (attention), and the tree tables (the attention tail, whose
- * predecessor is always its own split kernel); no kernel of a verify round
+ * node_off (attention; the split kernel also prefetches K/V tiles into L2,
+ * which is only a cache hint), and the tree tables, the query rows, the
+ * tree's K/V rows and the cache rows of its own tile (the attention tail,
+ * whose predecessor is always its own split kernel); no kernel of a verify round
  * (prepare, per-layer verify, accept, commit, in that order on one stream)
  * writes these directly before such a read.  The caller must not enqueue its
  * own kernel that writes them directly before a call with this flag. */

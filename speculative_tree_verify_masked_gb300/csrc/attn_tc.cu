@@ -485,6 +485,17 @@ __global__ void __launch_bounds__(384, 1) attn_split_kernel(const __grid_constan
   if (pair) cluster_sync();  // both CTAs' barriers exist before either signals the other
   const uint32_t tbase = *tmem_slot;
   const int total = is.cum[p.n_seq];
+  // L2 prefetch of the first item's first tiles while the previous kernel
+  // finishes: a prefetch only warms L2 (the point of coherence), so it is
+  // safe whatever the previous kernel writes, and the ring's first loads
+  // then hit L2.
+  if ((warp == 0 || warp == 10) && lane == 0 && cid < total) {
+    const Item I = item_at(is, p, cid, rank);
+    const CUtensorMap* maps = warp == 0 ? p.tmK : p.tmV;
+    const int nfirst = min(I.t1 - I.t0, (warp == 0 ? C::NK : C::NV) + kL2Ahead);
+    for (int t = I.t0; t < I.t0 + nfirst; t++)
+      for (int kb = kb0; kb < kb1; kb++) tma_prefetch_l2_2d(&maps[I.s], kb * 64, I.g * p.cap + t * kTile);
+  }
   pdl_wait();  // queries, status and the workspace (read by the previous tail) from here on
   pdl_trigger();
   if (threadIdx.x == 0) skip = status_bad(p.status) ? 1 : 0;
