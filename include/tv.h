@@ -279,6 +279,55 @@ tv_status tv_gdn_tree_verify(const tv_gdn_layer* layer, const tv_tree* tree, con
                              void* out, float scale, tv_stream stream);
 
 /* ------------------------------------------------------------------------
+ * Gated DeltaNet front end and gated output norm
+ * ------------------------------------------------------------------------
+ * "Adding a model", "What is still specific to Qwen3.8": the Gated DeltaNet
+ * layer with its gated norm; "The model layer": the per-sequence state
+ * includes the convolution tails.  The pages give no formula; the library
+ * takes the plainest reading:
+ *   channels: the raw query, key and value projections side by side,
+ *     C = 2 Hk dk + Hv dv per token;
+ *   short convolution: depthwise and causal, width W; a token's output at
+ *     channel c is sum_j wconv[c][j] x[t - (W-1) + j][c] over its root path,
+ *     continuing past the root into the committed tail; then SiLU;
+ *   q, k: divided per head by sqrt(sum of squares + 1e-6);
+ *   gates: beta = sigmoid(b_raw), alpha = exp(-softplus(a_raw));
+ *   output: o / sqrt(mean(o^2) + 1e-6) * w_norm * SiLU(z).
+ * Values are formed in fp32 in a fixed order, so verified rows equal decoded
+ * rows bit for bit. */
+typedef struct {
+  tv_dtype dtype;      /* x, tails, q/k/v, o, z, out: TV_BF16 or TV_F32 */
+  int32_t Hk, Hv, dk, dv; /* dk = dv in {64, 128} */
+  int32_t width;       /* convolution width W, 1..8 */
+  const float* wconv;  /* device [C][W] fp32 */
+  void* const* tail;   /* host array [n_seq] of device pointers, each [W-1][C]: the
+                          last W-1 committed raw inputs, oldest first (unused if W = 1) */
+} tv_gdn_front_layer;
+
+/* Convolution, SiLU, q/k norm and gates for every tree node (tree) or one
+ * decode token per sequence (tree NULL: n_seq tokens, errors to *status).
+ *  x      [rows][C] raw projections (layer dtype)
+ *  a_raw, b_raw [rows][Hv] fp32
+ *  q, k   [rows][Hk][dk]; v [rows][Hv][dv] (layer dtype); alpha, beta [rows][Hv] fp32:
+ *         the inputs of tv_gdn_tree_verify / tv_decode_step.
+ * The tails are read only. */
+tv_status tv_gdn_front(const tv_gdn_front_layer* layer, const tv_tree* tree, int32_t n_seq, const void* x,
+                       const float* a_raw, const float* b_raw, void* q, void* k, void* v, float* alpha,
+                       float* beta, int32_t* status, tv_stream stream);
+
+/* Gated RMS norm of rows outputs [rows][Hv][dv]: out = o / rms(o) * w_norm * SiLU(z);
+ * o, z, out in the layer dtype (out may alias o); w_norm [dv] fp32. */
+tv_status tv_gdn_out_norm(const tv_gdn_front_layer* layer, int32_t rows, const void* o, const void* z,
+                          const float* w_norm, void* out, tv_stream stream);
+
+/* Commit of the convolution tails: each sequence's tail becomes the last W-1
+ * of (tail, x[path[0..a-1]]) for the accepted path of tv_accept_path (tree),
+ * or of (tail, x[s]) for a decoded token (tree NULL, n_seq tokens).  Run it
+ * after every call that reads the tails for this round. */
+tv_status tv_gdn_conv_commit(const tv_gdn_front_layer* layer, const tv_tree* tree, int32_t n_seq, const void* x,
+                             const int32_t* path, const int32_t* acc_len, int32_t* status, tv_stream stream);
+
+/* ------------------------------------------------------------------------
  * Accept walk: longest agreeing path plus one token
  * ------------------------------------------------------------------------
  * [TOUR].  A node agrees when every node on its root path below the root

@@ -51,6 +51,11 @@ class tv_gdn_layer(ctypes.Structure):
                 ("S", POINTER(c_void_p))]
 
 
+class tv_gdn_front_layer(ctypes.Structure):
+    _fields_ = [("dtype", c_int32), ("Hk", c_int32), ("Hv", c_int32), ("dk", c_int32), ("dv", c_int32),
+                ("width", c_int32), ("wconv", c_void_p), ("tail", POINTER(c_void_p))]
+
+
 class tv_plan(ctypes.Structure):
     _fields_ = [("split", c_int32)]
 
@@ -102,6 +107,13 @@ def lib():
         L.tv_attn_decode_gated.restype = c_int32
         L.tv_attn_decode_gated.argtypes = [P, A, c_int32, vp, c_int32, vp, vp, vp, vp, vp, c_float, vp, c_size_t, vp,
                                            vp]
+        F = POINTER(tv_gdn_front_layer)
+        L.tv_gdn_front.restype = c_int32
+        L.tv_gdn_front.argtypes = [F, T, c_int32, vp, vp, vp, vp, vp, vp, vp, vp, vp, vp]
+        L.tv_gdn_out_norm.restype = c_int32
+        L.tv_gdn_out_norm.argtypes = [F, c_int32, vp, vp, vp, vp, vp]
+        L.tv_gdn_conv_commit.restype = c_int32
+        L.tv_gdn_conv_commit.argtypes = [F, T, c_int32, vp, vp, vp, vp, vp]
         L.tv_kvpool_page_bytes.restype = c_size_t
         L.tv_kvpool_page_bytes.argtypes = [c_int32, c_size_t]
         L.tv_kvpool_create.restype = c_int32
@@ -127,7 +139,8 @@ EXPORTED = ["tv_status_string", "tv_version", "tv_tree_meta_bytes", "tv_tree_pre
             "tv_len_advance", "tv_attn_static_scratch_bytes", "tv_attn_tree_verify_static", "tv_kvpool_page_bytes",
             "tv_kvpool_create", "tv_kvpool_reserve", "tv_kvpool_commit_rows", "tv_kvpool_release_rows",
             "tv_kvpool_committed_bytes", "tv_kvpool_reserved_bytes", "tv_kvpool_destroy", "tv_attn_rope",
-            "tv_attn_tree_verify_gated", "tv_attn_decode_gated"]
+            "tv_attn_tree_verify_gated", "tv_attn_decode_gated", "tv_gdn_front", "tv_gdn_out_norm",
+            "tv_gdn_conv_commit"]
 
 
 def _check(code: int, where: str):
@@ -268,6 +281,35 @@ def tv_attn_decode_gated(pl, attn: AttnLayer, n_seq, len_, max_len, q, k, v, gat
                                       _ptr(len_), max_len, _ptr(q), _ptr(k), _ptr(v), _ptr(gate), _ptr(out), scale,
                                       _ptr(ws), 0 if ws is None else ws.numel() * ws.element_size(), _ptr(status),
                                       _stream(stream)), "tv_attn_decode_gated")
+
+
+class GdnFrontLayer:
+    """A tv_gdn_front_layer over torch tensors: wconv [C][W] fp32, one tail
+    [W-1][C] per sequence."""
+
+    def __init__(self, Hk: int, Hv: int, dk: int, dv: int, wconv, tails, dtype: torch.dtype):
+        self.wconv, self.tails = wconv, list(tails)
+        self._tail = _ptr_array(self.tails)
+        self.c = tv_gdn_front_layer(_dtype_code(dtype), Hk, Hv, dk, dv, wconv.shape[1], _ptr(wconv), self._tail)
+
+
+def tv_gdn_front(layer: GdnFrontLayer, tree: Tree | None, n_seq, x, a_raw, b_raw, q, k, v, alpha, beta, status=None,
+                 stream=None):
+    _check(lib().tv_gdn_front(ctypes.byref(layer.c), ctypes.byref(tree.c) if tree is not None else None, n_seq,
+                              _ptr(x), _ptr(a_raw), _ptr(b_raw), _ptr(q), _ptr(k), _ptr(v), _ptr(alpha), _ptr(beta),
+                              _ptr(status), _stream(stream)), "tv_gdn_front")
+
+
+def tv_gdn_out_norm(layer: GdnFrontLayer, rows, o, z, w_norm, out, stream=None):
+    _check(lib().tv_gdn_out_norm(ctypes.byref(layer.c), rows, _ptr(o), _ptr(z), _ptr(w_norm), _ptr(out),
+                                 _stream(stream)), "tv_gdn_out_norm")
+
+
+def tv_gdn_conv_commit(layer: GdnFrontLayer, tree: Tree | None, n_seq, x, path=None, acc_len=None, status=None,
+                       stream=None):
+    _check(lib().tv_gdn_conv_commit(ctypes.byref(layer.c), ctypes.byref(tree.c) if tree is not None else None, n_seq,
+                                    _ptr(x), _ptr(path), _ptr(acc_len), _ptr(status), _stream(stream)),
+           "tv_gdn_conv_commit")
 
 
 def tv_attn_static_scratch_bytes() -> int:

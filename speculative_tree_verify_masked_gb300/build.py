@@ -18,7 +18,7 @@ CSRC = os.path.join(HERE, "csrc")
 INCLUDE = os.path.join(ROOT, "include")
 BUILD = os.path.join(HERE, "_build")
 LIB = os.path.join(HERE, "libtreeverify.so")
-SOURCES = ["tree.cu", "gdn.cu", "attn_f32.cu", "attn_tc.cu", "commit.cu", "api.cu", "attn_static.cu", "kvpool.cu", "front.cu"]
+SOURCES = ["tree.cu", "gdn.cu", "attn_f32.cu", "attn_tc.cu", "commit.cu", "api.cu", "attn_static.cu", "kvpool.cu", "front.cu", "front_gdn.cu"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 FLAGS = ARCH + ["-O3", "-lineinfo", "-std=c++17", "-Xcompiler", "-fPIC", "-I", INCLUDE, "-I", CSRC]
 

@@ -50,7 +50,7 @@ def test_every_declared_function_is_exported(L):
 def test_struct_layout_matches_c():
     """sizeof/offsetof of every ABI struct from gcc against ctypes."""
     structs = {"tv_tree": B.tv_tree, "tv_attn_layer": B.tv_attn_layer, "tv_gdn_layer": B.tv_gdn_layer,
-               "tv_plan": B.tv_plan}
+               "tv_plan": B.tv_plan, "tv_gdn_front_layer": B.tv_gdn_front_layer}
     lines = ['#include <stdio.h>', '#include <stddef.h>', '#include "tv.h"', "int main(void) {"]
     for name, cls in structs.items():
         lines.append(f'  printf("{name} size %zu\\n", sizeof({name}));')
@@ -146,6 +146,30 @@ def test_front_end_host_argument_errors(L):
                                        None, vp(16), 0.1, vp(16), 1 << 20, None) == 1   # gate required
     assert L.tv_attn_decode_gated(ctypes.byref(pl), lay, 1, vp(16), 10, vp(16), vp(16), vp(16), vp(24), vp(16), 0.1,
                                   vp(16), 1 << 20, vp(16), None) == 4
+
+
+def test_gdn_front_host_argument_errors(L):
+    """tv_gdn_front / tv_gdn_out_norm / tv_gdn_conv_commit reject bad
+    arguments before any launch."""
+    vp = ctypes.c_void_p
+    tails = (vp * 1)(vp(0x1000))
+    f = B.tv_gdn_front_layer(B.TV_BF16, 16, 48, 128, 128, 4, vp(0x2000), tails)
+    st = vp(16)
+    args = [vp(16)] * 8
+    assert L.tv_gdn_front(None, None, 1, *args, st, None) == 1
+    bad_w = B.tv_gdn_front_layer(B.TV_BF16, 16, 48, 128, 128, 9, vp(0x2000), tails)   # width above 8
+    assert L.tv_gdn_front(ctypes.byref(bad_w), None, 1, *args, st, None) == 2
+    bad_d = B.tv_gdn_front_layer(B.TV_BF16, 16, 48, 96, 96, 4, vp(0x2000), tails)     # head dim
+    assert L.tv_gdn_front(ctypes.byref(bad_d), None, 1, *args, st, None) == 2
+    bad_t = B.tv_gdn_front_layer(7, 16, 48, 128, 128, 4, vp(0x2000), tails)           # dtype
+    assert L.tv_gdn_front(ctypes.byref(bad_t), None, 1, *args, st, None) == 3
+    assert L.tv_gdn_front(ctypes.byref(f), None, 1, *args, None, None) == 1          # decode needs a status word
+    assert L.tv_gdn_front(ctypes.byref(f), None, 9, *args, st, None) == 1            # too many sequences
+    assert L.tv_gdn_out_norm(ctypes.byref(f), -1, vp(16), vp(16), vp(16), vp(16), None) == 1
+    assert L.tv_gdn_out_norm(ctypes.byref(f), 0, vp(16), vp(16), vp(16), vp(16), None) == 0  # nothing to do
+    assert L.tv_gdn_conv_commit(ctypes.byref(f), None, 1, None, None, None, st, None) == 1
+    t = B.tv_tree(1, 4, 4, 0x1000, 0x2000, 0x3000, 0x4000)
+    assert L.tv_gdn_conv_commit(ctypes.byref(f), ctypes.byref(t), 1, vp(16), None, vp(16), None, None) == 1
 
 
 def test_static_scratch_rejects_oversized_request_on_host(L):
