@@ -114,7 +114,8 @@ typedef struct {
  * returned (right after that wait in the attention split kernel and GDN
  * verify, at exit elsewhere),
  * so everything older than the predecessor has completed.  Before waiting, a
- * kernel reads only the recurrent states (GDN verify), the lengths and
+ * kernel reads only the recurrent states (GDN verify; GDN commit, whose
+ * predecessor is always a kernel of the same commit call), the lengths and
  * node_off (attention; the split kernel also prefetches K/V tiles into L2,
  * which is only a cache hint), and the tree tables, the query rows, the
  * tree's K/V rows and the cache rows of its own tile (the attention tail,

@@ -80,58 +80,96 @@ struct GdnCommitParams {
   int n_total, Hk, Hv, dv;
 };
 
+// Two state rows per lane group (the rows the GDN verify kernel pairs), so
+// a CTA of 128 threads replays 2 * 128/LPR rows: half the CTAs of one row
+// per group, and two independent replays to overlap.  The rows are loaded
+// before the wait: no kernel of the round directly before a commit writes
+// the recurrent states.
 template <typename T, int LPR>
 __global__ void __launch_bounds__(128) gdn_commit_kernel(const GdnCommitParams p) {
-  pdl_wait();
   constexpr int DK = 2 * kPairs * LPR;
-  constexpr int R = 128 / LPR;
+  constexpr int R = 2 * (128 / LPR);
   const int s = blockIdx.y, li = blockIdx.z;
   const int rb_per_head = (p.dv + R - 1) / R;
   const int h = blockIdx.x / rb_per_head, rb = blockIdx.x % rb_per_head;
+  const GdnCommitLayer& lay = p.L[li];
+  const int gi = threadIdx.x / LPR, jl = threadIdx.x % LPR;
+  const int row0 = rb * R + 2 * gi;
+  const bool valid0 = row0 < p.dv, valid1 = row0 + 1 < p.dv;
+  float* S0 = lay.S[s] + (static_cast<size_t>(h) * p.dv + (valid0 ? row0 : 0)) * DK;
+  float* S1 = lay.S[s] + (static_cast<size_t>(h) * p.dv + (valid1 ? row0 + 1 : 0)) * DK;
+  f2_t st0[kPairs], st1[kPairs];
+  if (valid0) {
+    load_row<LPR>(st0, S0, jl);
+  } else {
+#pragma unroll
+    for (int e = 0; e < kPairs; e++) st0[e] = 0ull;
+  }
+  if (valid1) {
+    load_row<LPR>(st1, S1, jl);
+  } else {
+#pragma unroll
+    for (int e = 0; e < kPairs; e++) st1[e] = 0ull;
+  }
+  pdl_wait();
   if (status_bad(p.status)) return;
   const int g = h / (p.Hv / p.Hk);
   const int a = p.acc_len[s];
+  if (a < 1 || a > TV_MAX_PATH) return;
   const MetaView mv = meta_view(const_cast<void*>(p.meta), p.n_total);
   const int off = mv.seq[s].off;
-  const GdnCommitLayer& lay = p.L[li];
   __shared__ __align__(16) float kb[TV_MAX_PATH][DK];
-  __shared__ float vb[TV_MAX_PATH][R];
+  __shared__ __align__(8) float vb[TV_MAX_PATH][R];
   __shared__ float ab[TV_MAX_PATH], bb[TV_MAX_PATH];
   const T* k = static_cast<const T*>(lay.k);
   const T* v = static_cast<const T*>(lay.v);
-  for (int idx = threadIdx.x; idx < a * DK; idx += blockDim.x) {
-    const int j = idx / DK, e = idx % DK;
-    const size_t node = static_cast<size_t>(off + p.path[s * TV_MAX_PATH + j]);
-    kb[j][e] = to_f32(k[(node * p.Hk + g) * DK + e]);
-  }
-  for (int idx = threadIdx.x; idx < a * R; idx += blockDim.x) {
-    const int j = idx / R, r = idx % R, row = rb * R + r;
-    const size_t node = static_cast<size_t>(off + p.path[s * TV_MAX_PATH + j]);
-    vb[j][r] = row < p.dv ? to_f32(v[(node * p.Hv + h) * p.dv + row]) : 0.f;
-  }
-  for (int j = threadIdx.x; j < a; j += blockDim.x) {
-    const size_t node = static_cast<size_t>(off + p.path[s * TV_MAX_PATH + j]);
-    ab[j] = lay.alpha[node * p.Hv + h];
-    bb[j] = lay.beta[node * p.Hv + h];
+  // the path's keys, values, gates: every load issued before any store
+  {
+    constexpr int UK = TV_MAX_PATH * DK / 128, UV = TV_MAX_PATH * R / 128;
+    float kv[UK], vv[UV];
+#pragma unroll
+    for (int u = 0; u < UK; u++) {
+      const int idx = threadIdx.x + 128 * u, j = idx / DK, e = idx % DK;
+      kv[u] = j < a ? to_f32(k[(static_cast<size_t>(off + p.path[s * TV_MAX_PATH + j]) * p.Hk + g) * DK + e]) : 0.f;
+    }
+#pragma unroll
+    for (int u = 0; u < UV; u++) {
+      const int idx = threadIdx.x + 128 * u, j = idx / R, r = idx % R, row = rb * R + r;
+      vv[u] = j < a && row < p.dv
+                  ? to_f32(v[(static_cast<size_t>(off + p.path[s * TV_MAX_PATH + j]) * p.Hv + h) * p.dv + row])
+                  : 0.f;
+    }
+    float av = 0.f, bv = 0.f;
+    if (threadIdx.x < a) {
+      const size_t node = static_cast<size_t>(off + p.path[s * TV_MAX_PATH + threadIdx.x]);
+      av = lay.alpha[node * p.Hv + h];
+      bv = lay.beta[node * p.Hv + h];
+    }
+#pragma unroll
+    for (int u = 0; u < UK; u++) {
+      const int idx = threadIdx.x + 128 * u;
+      kb[idx / DK][idx % DK] = kv[u];
+    }
+#pragma unroll
+    for (int u = 0; u < UV; u++) {
+      const int idx = threadIdx.x + 128 * u;
+      vb[idx / R][idx % R] = vv[u];
+    }
+    if (threadIdx.x < a) {
+      ab[threadIdx.x] = av;
+      bb[threadIdx.x] = bv;
+    }
   }
   __syncthreads();
-  const int r = threadIdx.x / LPR, jl = threadIdx.x % LPR;
-  const int row = rb * R + r;
-  const bool valid = row < p.dv;
-  float* Srow = lay.S[s] + (static_cast<size_t>(h) * p.dv + (valid ? row : 0)) * DK;
-  f2_t st[kPairs];
-  if (valid) {
-    load_row<LPR>(st, Srow, jl);
-  } else {
-#pragma unroll
-    for (int e = 0; e < kPairs; e++) st[e] = 0ull;
-  }
   for (int j = 0; j < a; j++) {
-    f2_t k[kPairs];
-    load_row<LPR>(k, kb[j], jl);
-    gdn_row_step<LPR, false>(st, k, k, 0.f, vb[j][r], ab[j], bb[j], 0.f, true);
+    f2_t kk[kPairs];
+    load_row<LPR>(kk, kb[j], jl);
+    const float2 v2 = *reinterpret_cast<const float2*>(&vb[j][2 * gi]);
+    gdn_row_step<LPR, false>(st0, kk, kk, 0.f, v2.x, ab[j], bb[j], 0.f, true);
+    gdn_row_step<LPR, false>(st1, kk, kk, 0.f, v2.y, ab[j], bb[j], 0.f, true);
   }
-  if (valid) store_row<LPR>(Srow, st, jl);
+  if (valid0) store_row<LPR>(S0, st0, jl);
+  if (valid1) store_row<LPR>(S1, st1, jl);
 }
 
 __global__ void commit_len_kernel(int32_t* len, const int32_t* acc_len, const int32_t* status, int n_seq) {
@@ -142,7 +180,7 @@ __global__ void commit_len_kernel(int32_t* len, const int32_t* acc_len, const in
 
 template <typename T, int LPR>
 static void launch_gdn_commit(const GdnCommitParams& p, int n_seq, int nl, cudaStream_t st, bool ov) {
-  constexpr int R = 128 / LPR;
+  constexpr int R = 2 * (128 / LPR);
   const dim3 grid(p.Hv * ((p.dv + R - 1) / R), n_seq, nl);
   launch_k(ov, gdn_commit_kernel<T, LPR>, grid, dim3(128), 0, st, p);
 }
