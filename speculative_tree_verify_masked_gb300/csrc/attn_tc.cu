@@ -847,6 +847,23 @@ __global__ void __launch_bounds__(256, 1) attn_tail_kernel(const __grid_constant
     int cur = tsh / ST;
     const bool cont = (tsh % ST) != 0;  // the split kernel started this split
 
+    // The finished splits' states (the node's G rows of a split are one
+    // contiguous block) come in by bulk copies issued first thing after the
+    // wait, so their latency hides behind the carried state, the queries and
+    // the node's own tiles; the node's final split state is kept in shared
+    // memory too.  Shared layout: [nst][G][REC], then [G][REC].
+    const uint32_t mst_s = sb + (C::TAIL_FIXED - 1024);
+    const int nst = min(cur, p.n_mstage);
+    const uint32_t mown_s = mst_s + static_cast<uint32_t>(nst * G * C::REC * 4);
+    float* const mown = reinterpret_cast<float*>(gb + (C::TAIL_FIXED - 1024) + nst * G * C::REC * 4);
+    if (warp == 0 && nst > 0) {
+      // one lane sets the byte count first; the copies are spread over the warp
+      const uint32_t bytes = static_cast<uint32_t>(G * C::REC * 4);
+      if (lane == 0) mbar_arrive_expect_tx(MBAR, bytes * nst);
+      __syncwarp();
+      for (int sp = lane; sp < nst; sp += 32)
+        bulk_g2s(mst_s + sp * bytes, ws_rec(p, s, g, sp, local * G, D), bytes, MBAR);
+    }
     // stage this node's G query rows (unless staged early) and, when
     // continuing, the carried state records with cp.async
     const bool ostaged = early || G * C::REC * 4 <= C::TILE;
@@ -911,22 +928,6 @@ __global__ void __launch_bounds__(256, 1) attn_tail_kernel(const __grid_constant
     tc_fence_before();
     __syncthreads();
     tc_fence_after();
-    // The finished splits' states (the node's G rows of a split are one
-    // contiguous block) come in by bulk copies issued now, so their latency
-    // hides behind the node's own tiles; the node's final split state is
-    // kept in shared memory too.  Shared layout: [nst][G][REC], then [G][REC].
-    const uint32_t mst_s = sb + (C::TAIL_FIXED - 1024);
-    const int nst = min(cur, p.n_mstage);
-    const uint32_t mown_s = mst_s + static_cast<uint32_t>(nst * G * C::REC * 4);
-    float* const mown = reinterpret_cast<float*>(gb + (C::TAIL_FIXED - 1024) + nst * G * C::REC * 4);
-    if (warp == 0 && nst > 0) {
-      // one lane sets the byte count first; the copies are spread over the warp
-      const uint32_t bytes = static_cast<uint32_t>(G * C::REC * 4);
-      if (lane == 0) mbar_arrive_expect_tx(MBAR, bytes * nst);
-      __syncwarp();
-      for (int sp = lane; sp < nst; sp += 32)
-        bulk_g2s(mst_s + sp * bytes, ws_rec(p, s, g, sp, local * G, D), bytes, MBAR);
-    }
 
     uint32_t ph = 0;
     bool ok = true;
@@ -1046,6 +1047,7 @@ __global__ void __launch_bounds__(256, 1) attn_tail_kernel(const __grid_constant
         float* mref = lsm + static_cast<size_t>(ns) * G;  // [G]
         for (int r = threadIdx.x; r < G; r += blockDim.x) {
           float mm = -INFINITY;
+#pragma unroll 8
           for (int sp = 0; sp < ns; sp++) mm = fmaxf(mm, wsm[sp * G + r]);
           mref[r] = mm;
         }
@@ -1057,6 +1059,7 @@ __global__ void __launch_bounds__(256, 1) attn_tail_kernel(const __grid_constant
         __syncthreads();
         for (int r = threadIdx.x; r < G; r += blockDim.x) {
           float ls = 0.f;
+#pragma unroll 8
           for (int sp = 0; sp < ns; sp++) ls = __fmaf_rn(wsm[sp * G + r], lsm[sp * G + r], ls);
           ltot[r] = ls;
         }
