@@ -82,7 +82,7 @@ def round_bytes(cfg, n_nodes_per_seq, acc_lens):
 # workload name; the capture command and the figures are in
 # profiles/attn_traffic_64layer_128k.md.  Update together with the kernels.
 MEASURED_TRAFFIC = {
-    "64-layer mixer stack (48 GDN + 16 attention), L 131072, 32-node tree": 537335040 + 21220864 + 1061376,
+    "64-layer mixer stack (48 GDN + 16 attention), L 131072, 32-node tree": 537351424 + 21152768 + 1061888,
 }
 
 
