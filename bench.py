@@ -224,6 +224,23 @@ def blas_threads():
 # ---------------------------------------------------------------------------
 # our arm
 # ---------------------------------------------------------------------------
+def max_over_ranks(x: float, world: int, device) -> float:
+    """The largest of every rank's value: a replicated job is as slow as its
+    slowest replica.  One rank: the value itself."""
+    if world <= 1:
+        return x
+    t = torch.tensor([x], dtype=torch.float64, device=device)
+    torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
+    return float(t.item())
+
+
+def job_throughput(nodes_per_round: int, world: int, ms_per_round: float) -> float:
+    """Whole-job tree nodes per second: each of the `world` replicas verifies
+    its own round of `nodes_per_round` nodes in `ms_per_round` (the slowest
+    rank's time), weak scaling."""
+    return world * nodes_per_round / (ms_per_round / 1e3)
+
+
 def run_ours(args, rank, world, local_rank):
     from speculative_tree_verify_masked_gb300 import binding as B
     from speculative_tree_verify_masked_gb300 import build as _build
@@ -265,11 +282,7 @@ def run_ours(args, rank, world, local_rank):
     if world > 1:
         torch.distributed.barrier()
     clk = clocks.stop(t_wall0, t_wall1) if clocks else None
-    ms = ev0.elapsed_time(ev1) / args.steps
-    if world > 1:
-        t = torch.tensor([ms], device=dev)
-        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
-        ms = float(t.item())
+    ms = max_over_ranks(ev0.elapsed_time(ev1) / args.steps, world, dev)
     assert r.status() == 0, f"device status {r.status()}"
     # the dominant call, one attention layer's verify: CUDA events captured
     # around each attention layer in a second graph of the same round (event
@@ -334,13 +347,9 @@ def run_ours(args, rank, world, local_rank):
         for _ in range(n_e2e):
             e2e_step()
         torch.cuda.synchronize()
-        e2e_ms = (time.perf_counter() - t0) * 1e3 / n_e2e
-        if world > 1:
-            t = torch.tensor([e2e_ms], device=dev)
-            torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
-            e2e_ms = float(t.item())
+        e2e_ms = max_over_ranks((time.perf_counter() - t0) * 1e3 / n_e2e, world, dev)
         assert r.status() == 0
-        e2e = {"value": round(world * nodes_per_round / (e2e_ms / 1e3), 1), "unit": UNIT,
+        e2e = {"value": round(job_throughput(nodes_per_round, world, e2e_ms), 1), "unit": UNIT,
                "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "ms_per_step": round(e2e_ms, 4),
                "steps": n_e2e, "path": "eager C-ABI calls (ctypes), pinned host inputs in, accepted path out"}
 
@@ -386,7 +395,7 @@ def run_ours(args, rank, world, local_rank):
     n_gdn = len(r.gdn)
     launches_per_round = 1 + 2 * n_attn + n_gdn + 1 + (1 + math.ceil(n_attn / 16) + math.ceil(n_gdn / 32) + 1)
     line = {
-        "metric": METRIC, "value": round(world * nodes_per_round / (ms / 1e3), 1), "unit": UNIT, "n_gpus": world,
+        "metric": METRIC, "value": round(job_throughput(nodes_per_round, world, ms), 1), "unit": UNIT, "n_gpus": world,
         "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(ms, 5), "higher_is_better": True,
         "scaling": "weak", "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
         "config": {"workload": cfg.name, "layers": cfg.n_layers, "attention_layers": n_attn, "gdn_layers": n_gdn,
