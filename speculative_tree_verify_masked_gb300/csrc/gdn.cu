@@ -225,6 +225,15 @@ __global__ void __launch_bounds__(32 * GdnShape<LPR>::W) gdn_verify_kernel(const
     }
   };
   const float scale = p.scale;
+  // the first visit's entry, key, query, gates and value; each visit then
+  // loads the next one in visit order, across segment ends too (segments are
+  // consecutive runs of the visits)
+  int e = sch[0];
+  f2_t k[kPairs], q[kPairs];
+  load_row_any<LPR>(k, kb + static_cast<size_t>(e & 0xFF) * DK, j);
+  load_row_any<LPR>(q, qb + static_cast<size_t>(e & 0xFF) * DK, j);
+  float4 c4 = nc[e & 0xFF];
+  float2 v2 = *reinterpret_cast<const float2*>(vb + (e & 0xFF) * R + 2 * gi);
   for (int sg = 0; sg < n_seg; sg++) {
     const int sw = sgt[sg];
     const int first = sw & 0xFF, cnt = (sw >> 8) & 0xFF, src = (sw >> 16) & 0xFF, save = (sw >> 24) & 0xFF;
@@ -236,19 +245,13 @@ __global__ void __launch_bounds__(32 * GdnShape<LPR>::W) gdn_verify_kernel(const
     // the visits of the segment: no branch but the lane-0 store.  Each sum,
     // c and o is formed exactly as gdn_row_step forms it.  The next visit's
     // entry, key, query, gates and value are loaded during this one (the
-    // index clamped at the segment's end, so the loads need no branch).
+    // index clamped at the last visit, so the loads need no branch).
     const int last = first + cnt - 1;
-    int e = sch[first];
-    f2_t k[kPairs], q[kPairs];
-    load_row_any<LPR>(k, kb + static_cast<size_t>(e & 0xFF) * DK, j);
-    load_row_any<LPR>(q, qb + static_cast<size_t>(e & 0xFF) * DK, j);
-    float4 c4 = nc[e & 0xFF];
-    float2 v2 = *reinterpret_cast<const float2*>(vb + (e & 0xFF) * R + 2 * gi);
 #pragma unroll 2
     for (int v = first; v <= last; v++) {
       const int node = e & 0xFF;
       const bool hc = (e >> 24) & 1;
-      const int en = sch[v < last ? v + 1 : last];
+      const int en = sch[v + 1 < n ? v + 1 : v];
       f2_t kn[kPairs], qn[kPairs];
       load_row_any<LPR>(kn, kb + static_cast<size_t>(en & 0xFF) * DK, j);
       load_row_any<LPR>(qn, qb + static_cast<size_t>(en & 0xFF) * DK, j);
