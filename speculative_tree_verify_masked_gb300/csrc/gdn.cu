@@ -4,8 +4,8 @@
 // applied along every node's root path).  A lane group of LPR lanes owns two
 // state rows of one value head of one sequence, each with the lane layout
 // and the step arithmetic of decode and commit (gdn_step.cuh), so a verified
-// row is the decoded row bit for bit by construction.  A CTA of two warps
-// owns 2 * 2 * 32/LPR consecutive rows of one value head and stages the
+// row is the decoded row bit for bit by construction.  A CTA of four warps
+// owns 4 * 2 * 32/LPR consecutive rows of one value head and stages the
 // tree's keys and queries (bf16, by cp.async), gates and values once.  The
 // lane groups walk the tree in the order prepared by tv_tree_prepare, cut
 // into segments that restore a saved state only at their start and save one
@@ -25,7 +25,9 @@
 // the compiler can overlap them, which branches inside the loop prevent, or
 // another warp fills the gaps: eight rows per warp (16 columns per lane, two
 // rows per lane group, one 16-byte bf16 load per chunk serving both rows)
-// give a 48-head x 128-row layer 768 warps, about two per SM sub-partition.
+// give a 48-head x 128-row layer 768 warps, about two per SM sub-partition;
+// four warps per CTA share one staged copy of the tree's inputs (two warps:
+// the 64-layer round 39 us slower, 64-node trees of 4 sequences 5 % slower).
 #include "common.cuh"
 #include "gdn_step.cuh"
 #include "host.hpp"
@@ -58,7 +60,7 @@ inline int slots_for(int n_max) {
 template <int LPR>
 struct GdnShape {
   static constexpr int DK = 2 * kPairs * LPR;  // key dim
-  static constexpr int W = 2;                  // warps per CTA
+  static constexpr int W = 4;                  // warps per CTA
   static constexpr int NG = W * 32 / LPR;      // lane groups per CTA
   static constexpr int RPG = 2;                // state rows per lane group
   static constexpr int R = NG * RPG;           // state rows per CTA
