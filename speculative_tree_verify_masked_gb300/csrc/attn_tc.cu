@@ -19,7 +19,9 @@
 //  split kernel (persistent, one CTA per SM): the tiles that every node of a
 //    sequence shares (positions below 64*floor(L/64), all cache rows) for up to
 //    128 query rows (node x head of one KV head) at once.  Warps 0 and 10
-//    stream K and V tiles with TMA (128B-swizzled boxes) through two rings;
+//    stream K and V tiles with TMA (128B-swizzled boxes) through two rings,
+//    prefetching into L2 the tile two ahead (and, before the wait for the
+//    previous kernel, the first tiles);
 //    warp 1 issues QK^T (Q in TMEM, K in
 //    shared memory, S double-buffered in TMEM) and warp 11 issues PV (P in a
 //    ring of shared-memory slots, V in shared memory, O in TMEM); warps 2-5
@@ -33,9 +35,10 @@
 //    once.  Each split's state goes to the workspace.
 //  tail kernel (one CTA per node and KV head): the node's own tiles (cache
 //    rows past the last shared tile plus its ancestors at their logical
-//    slots, gathered into shared memory with cp.async), continuing the split
-//    state the split kernel left, then the in-order merge of all splits and
-//    the bf16 output.
+//    slots, gathered into shared memory with cp.async, the first one before
+//    the wait for the split kernel), continuing the split state the split
+//    kernel left, then the in-order merge of all splits and the bf16 output
+//    (times the front end's sigmoid gate when one is given).
 //  Decode runs the same two kernels with a one-node tree per sequence and
 //  appends its own K/V row.
 #include <cmath>
