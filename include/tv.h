@@ -198,8 +198,14 @@ size_t tv_attn_static_scratch_bytes(void);
  *  Limit: requests whose tv_attn_workspace_bytes(plan, layer, tree->n_seq,
  *    tree->n_max, max_len) exceeds TV_STATIC_SCRATCH_BYTES return
  *    TV_ERR_SCRATCH before anything is enqueued.
+ *  Errors: TV_ERR_ARG for a NULL or ill-formed tree descriptor or a negative
+ *    max_len (checked before the size), then everything tv_attn_tree_verify
+ *    returns.
  *  Setup: the first call on each device looks up the array's device address
  *    (this loads the module); make that first call before any stream capture.
+ *    The address is cached per device and looked up again when the device's
+ *    context changes (after cudaDeviceReset), so the first call after a reset
+ *    must also come before any capture.
  *  Start values: none needed; every scratch record a call reads was written
  *    earlier in the same call.
  *  Concurrency: all calls on one device share the one array, so two calls
@@ -442,6 +448,25 @@ size_t tv_kvpool_reserved_bytes(const tv_kv_pool* pool);
 
 /* Unmap and free every page and reservation of the pool, then the pool. */
 tv_status tv_kvpool_destroy(tv_kv_pool* pool);
+
+/* ------------------------------------------------------------------------
+ * Diagnostics
+ * ------------------------------------------------------------------------
+ * Every wait inside the pipelined kernels (the attention split and tail
+ * kernels) is bounded: after a limit it raises a give-up flag the other
+ * roles see, lets its own copies land, and the kernel writes TV_ERR_TIMEOUT
+ * into the status word instead of hanging.  This call runs those same wait
+ * routines against barriers that nothing arrives at, with a caller-chosen
+ * limit, so that the give-up path can be checked on a device without
+ * faulting or hanging it.  One CTA; the pages have no counterpart (the
+ * load-time self-check of "Adding a model", step 4, is the nearest).
+ *  status  device [1] word: TV_ERR_TIMEOUT is written when a wait gave up
+ *  result  device int32 [4]: 1 = the wait succeeded, 0 = it gave up, for
+ *          [0] a barrier that has completed (expect 1), [1] the warp-wide
+ *          wait, [2] the single-thread wait, [3] the plain wait on barriers
+ *          that never complete (expect 0 each)
+ *  limit_cycles  1 .. 2^31 SM clocks per wait (the kernels use 2^31) */
+tv_status tv_wait_selftest(int32_t* status, int32_t* result, int64_t limit_cycles, tv_stream stream);
 
 #ifdef __cplusplus
 }

@@ -130,6 +130,8 @@ def lib():
         L.tv_kvpool_reserved_bytes.argtypes = [vp]
         L.tv_kvpool_destroy.restype = c_int32
         L.tv_kvpool_destroy.argtypes = [vp]
+        L.tv_wait_selftest.restype = c_int32
+        L.tv_wait_selftest.argtypes = [vp, vp, ctypes.c_int64, vp]
         _lib = L
     return _lib
 
@@ -140,7 +142,7 @@ EXPORTED = ["tv_status_string", "tv_version", "tv_tree_meta_bytes", "tv_tree_pre
             "tv_kvpool_create", "tv_kvpool_reserve", "tv_kvpool_commit_rows", "tv_kvpool_release_rows",
             "tv_kvpool_committed_bytes", "tv_kvpool_reserved_bytes", "tv_kvpool_destroy", "tv_attn_rope",
             "tv_attn_tree_verify_gated", "tv_attn_decode_gated", "tv_gdn_front", "tv_gdn_out_norm",
-            "tv_gdn_conv_commit"]
+            "tv_gdn_conv_commit", "tv_wait_selftest"]
 
 
 def _check(code: int, where: str):
@@ -371,6 +373,10 @@ def tv_len_advance(len_, by, inc: int, n_seq: int, stream=None):
 # ---------------------------------------------------------------------------
 # KV pool
 # ---------------------------------------------------------------------------
+def tv_wait_selftest(status, result, limit_cycles: int, stream=None):
+    _check(lib().tv_wait_selftest(_ptr(status), _ptr(result), int(limit_cycles), _stream(stream)), "tv_wait_selftest")
+
+
 def tv_kvpool_page_bytes(device: int, page_bytes: int = 0) -> int:
     return int(lib().tv_kvpool_page_bytes(device, page_bytes))
 

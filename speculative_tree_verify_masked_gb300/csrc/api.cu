@@ -6,9 +6,46 @@
 #include "host.hpp"
 #include "launchers.hpp"
 
+#include "ptx.cuh"
+
 using namespace tv;
 
 namespace {
+
+// The bounded waits of the pipelined kernels, run against barriers that
+// nothing arrives at: each must give up after `limit` clocks, raise the
+// shared give-up flag and let the kernel report TV_ERR_TIMEOUT.  Warp 0
+// first waits on a barrier that has completed (must succeed), then on one
+// that never completes with the warp-wide wait; thread 32 does the same
+// with the single-thread wait; thread 64 uses the plain wait.
+__global__ void __launch_bounds__(96) wait_selftest_kernel(int32_t* status, int32_t* result, long long limit) {
+  __shared__ __align__(8) uint64_t bars[4];
+  __shared__ int abort_flag;
+  const uint32_t done_bar = smem_u32(&bars[0]), never0 = smem_u32(&bars[1]), never1 = smem_u32(&bars[2]),
+                 never2 = smem_u32(&bars[3]);
+  if (threadIdx.x == 0) {
+    for (int i = 0; i < 4; i++) mbar_init(smem_u32(&bars[i]), 1);
+    abort_flag = 0;
+    fence_mbar_init();
+    mbar_arrive(done_bar);  // phase 0 of this one completes
+  }
+  __syncthreads();
+  volatile int* flag = &abort_flag;
+  if (threadIdx.x < 32) {
+    const bool a = wait_warp(done_bar, 0, flag, limit);
+    const bool b = wait_warp(never0, 0, flag, limit);
+    if (threadIdx.x == 0) {
+      result[0] = a ? 1 : 0;
+      result[1] = b ? 1 : 0;
+    }
+  } else if (threadIdx.x == 32) {
+    result[2] = wait_role(never1, 0, flag, limit) ? 1 : 0;
+  } else if (threadIdx.x == 64) {
+    result[3] = mbar_wait(never2, 0, limit) ? 1 : 0;
+  }
+  __syncthreads();
+  if (threadIdx.x == 0 && (result[1] == 0 || result[2] == 0 || result[3] == 0)) set_status(status, TV_ERR_TIMEOUT);
+}
 
 tv_status attn_layer_check(const tv_attn_layer* l, int n_seq) {
   if (!l || !l->K || !l->V) return TV_ERR_ARG;
@@ -117,4 +154,11 @@ extern "C" tv_status tv_attn_decode_gated(const tv_plan* plan, const tv_attn_lay
   cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
   if (attn->dtype == TV_F32) return attn_f32_launch(c, st);
   return attn_tc_launch(plan, c, ws, ws_bytes, st);
+}
+
+extern "C" tv_status tv_wait_selftest(int32_t* status, int32_t* result, int64_t limit_cycles, tv_stream stream) {
+  if (!status || !result || limit_cycles < 1 || limit_cycles > kWaitCycles) return TV_ERR_ARG;
+  if (!aligned16(status) || !aligned16(result)) return TV_ERR_ALIGN;
+  wait_selftest_kernel<<<1, 96, 0, reinterpret_cast<cudaStream_t>(stream)>>>(status, result, limit_cycles);
+  return launch_status();
 }

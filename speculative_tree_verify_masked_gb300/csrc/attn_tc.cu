@@ -30,9 +30,9 @@
 //    QK^T runs ahead of the softmax and the tensor pipe overlaps the narrow
 //    QK^T steps with the wide PV steps.  When the largest tree spans two
 //    128-row blocks, the two row blocks of a (sequence, KV head, split) run
-//    as a 2-CTA cluster that shares one K/V stream: each CTA loads half of
-//    every tile's boxes and multicasts them to both, so each tile leaves DRAM
-//    once.  Each split's state goes to the workspace.
+//    on neighbouring CTAs that stream the same tiles side by side, so the
+//    second read of a tile is served by L2; each of the two prefetches half
+//    of every tile's boxes into L2.  Each split's state goes to the workspace.
 //  tail kernel (one CTA per node and KV head): the node's own tiles (cache
 //    rows past the last shared tile plus its ancestors at their logical
 //    slots, gathered into shared memory with cp.async, the first one before
@@ -57,14 +57,9 @@ constexpr int kHalf = 32;       // positions per softmax half
 constexpr int kBox = 64 * 128;  // one [64 rows x 128 B] 128B-swizzled box
 constexpr int kMaxGroup = 64;   // query heads per KV head on this path
 // The K/V producers also prefetch into L2 the boxes of the tile this many
-// tiles ahead.  A 2-CTA cluster holds at most 5 tiles (160 KiB) in its rings,
-// short of the ~176 KiB per cluster that 76 clusters need in flight to keep
-// HBM busy at ~2 us of loaded latency.  Measured per attention layer (64-layer
-// workload / 4-sequence workload): none 119.2 / -, 2 ahead 112.2 / 98.6 us,
-// 3 ahead 114.0 / 101.6, 4 ahead 117.1 / 105.3, 5 ahead no gain; 8 ahead (an
-// earlier build) read 26 % more DRAM bytes, the prefetched lines evicted
-// before their loads.  At 3 ahead the split kernel still reads each KV byte
-// once (537.96 MB for 536.87 MB of KV).
+// tiles ahead: a CTA's rings hold at most 5 tiles (160 KiB), fewer bytes
+// than HBM needs in flight per SM at ~2 us of loaded latency.  Prefetching
+// much further ahead lets the prefetched lines be evicted before their loads.
 constexpr int kL2Ahead = 2;
 
 template <int D>
@@ -112,7 +107,7 @@ struct TcParams {
   float* ws;
   int n_seq, n_total, Hq, Hkv, G, cap, max_len, split_tiles, max_splits, rows_max, decode;
   int n_mstage;  // tail kernel: finished splits whose states are staged in shared memory
-  int pair;      // split kernel: 2-CTA clusters, one per (sequence, KV head, split), CTA rank = row block
+  int pair;      // split kernel: CTAs 2c, 2c+1 run row blocks 0, 1 of the same (sequence, KV head, split)
   float c;  // scale * log2(e)
 };
 
@@ -353,9 +348,15 @@ __device__ inline void item_space(const TcParams& p, ItemSpace& is) {
   for (int s = 0; s < p.n_seq; s++) {
     int L = p.len[s];
     if (L < 0 || L > p.max_len) L = 0;  // reported by the tail kernel
-    int nodes = p.decode ? 1 : p.node_off[s + 1] - p.node_off[s];
+    // offsets and counts clamped to the node buffers: a malformed tree is
+    // reported by tv_tree_prepare, and the query rows of the first item are
+    // read before the status word is
+    int off = p.decode ? s : p.node_off[s];
+    off = off < 0 ? 0 : (off > p.n_total ? p.n_total : off);
+    int nodes = p.decode ? 1 : p.node_off[s + 1] - off;
     nodes = nodes < 0 ? 0 : (nodes > TV_MAX_NODES ? TV_MAX_NODES : nodes);
-    is.off[s] = p.decode ? s : p.node_off[s];
+    if (off + nodes > p.n_total) nodes = p.n_total - off;
+    is.off[s] = off;
     is.rows[s] = nodes * p.G;
     is.nrb[s] = p.pair ? 1 : (is.rows[s] + 127) / 128;  // a pair covers row blocks 0 and 1
     is.tsh[s] = L / kTile;
@@ -377,41 +378,6 @@ __device__ inline Item item_at(const ItemSpace& is, const TcParams& p, int w, in
   it.t0 = it.split * p.split_tiles;
   it.t1 = min(it.t0 + p.split_tiles, is.tsh[s]);
   return it;
-}
-
-// Warp-wide bounded wait: a non-blocking test first (the common case in a
-// full pipeline), then polling; gives up with the other roles.  The outcome
-// is the same in every lane.
-__device__ __forceinline__ bool wait_warp(uint32_t bar, uint32_t parity, volatile int* abort_flag) {
-  if (__all_sync(0xffffffffu, mbar_test(bar, parity))) return true;
-  const long long t0 = clock64();
-  while (true) {
-    const bool done = mbar_try_wait(bar, parity);
-    if (__all_sync(0xffffffffu, done)) return true;
-    int give_up = 0;
-    if (lane_id() == 0) {
-      if (*abort_flag) give_up = 1;
-      else if (clock64() - t0 > kWaitCycles) {
-        *abort_flag = 1;
-        give_up = 1;
-      }
-    }
-    if (__shfl_sync(0xffffffffu, give_up, 0)) return false;
-  }
-}
-
-// Bounded wait that also gives up as soon as another role has given up.
-__device__ __forceinline__ bool wait_role(uint32_t bar, uint32_t parity, volatile int* abort_flag) {
-  if (mbar_try_wait(bar, parity)) return true;
-  const long long t0 = clock64();
-  while (true) {
-    if (mbar_try_wait(bar, parity)) return true;
-    if (*abort_flag) return false;
-    if (clock64() - t0 > kWaitCycles) {
-      *abort_flag = 1;
-      return false;
-    }
-  }
 }
 
 template <int D>
@@ -442,25 +408,23 @@ __global__ void __launch_bounds__(384, 1) attn_split_kernel(const __grid_constan
   const uint32_t XBAR0 = DRAIN + 16u;  // [2] half-max exchange, by tile parity
   const uint32_t kring = sb, vring = sb + C::NK * C::TILE, pring = vring + C::NV * C::TILE;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  // Pair mode: a 2-CTA cluster shares the K/V stream of one (sequence, KV
-  // head, split); CTA rank r computes row block r, loads half of each tile's
-  // boxes and multicasts them to both CTAs, and a ring slot is refilled only
-  // after both CTAs' QK^T / PV have read it.
+  // Pair mode: CTAs 2c and 2c+1 run row blocks 0 and 1 of the same items,
+  // loading the same tiles at nearly the same time, so one of the two reads
+  // of a tile comes from L2.  Each prefetches only its half of the boxes.
   const bool pair = p.pair != 0;
-  const int rank = pair ? static_cast<int>(cluster_ctarank()) : 0;
+  const int rank = pair ? static_cast<int>(blockIdx.x & 1u) : 0;
   const int cid = pair ? static_cast<int>(blockIdx.x) / 2 : static_cast<int>(blockIdx.x);
   const int ncl = pair ? static_cast<int>(gridDim.x) / 2 : static_cast<int>(gridDim.x);
-  const int kb0 = pair ? rank * (C::KB / 2) : 0, kb1 = pair ? kb0 + C::KB / 2 : C::KB;
-  constexpr uint16_t kBoth = 3;
+  const int kb0 = pair ? rank * (C::KB / 2) : 0, kb1 = pair ? kb0 + C::KB / 2 : C::KB;  // L2 prefetch share
 
   if (threadIdx.x == 0) {
     for (int i = 0; i < C::NK; i++) {
       mbar_init(KFULL0 + 8u * i, 1);
-      mbar_init(KEMPTY0 + 8u * i, pair ? 2 : 1);
+      mbar_init(KEMPTY0 + 8u * i, 1);
     }
     for (int i = 0; i < C::NV; i++) {
       mbar_init(VFULL0 + 8u * i, 1);
-      mbar_init(VEMPTY0 + 8u * i, pair ? 2 : 1);
+      mbar_init(VEMPTY0 + 8u * i, 1);
     }
     for (int b = 0; b < 2; b++) {
       mbar_init(SFULL0 + 8u * b, 1);
@@ -485,7 +449,6 @@ __global__ void __launch_bounds__(384, 1) attn_split_kernel(const __grid_constan
   tc_fence_before();
   __syncthreads();
   tc_fence_after();
-  if (pair) cluster_sync();  // both CTAs' barriers exist before either signals the other
   const uint32_t tbase = *tmem_slot;
   const int total = is.cum[p.n_seq];
   // L2 prefetch of the first item's first tiles while the previous kernel
@@ -531,7 +494,7 @@ __global__ void __launch_bounds__(384, 1) attn_split_kernel(const __grid_constan
       const int ybase = I.g * p.cap;
       for (int t = I.t0; t < I.t1; t++) {
         const int st = it % nslot;
-        if (!wait_role(empty0 + 8u * st, ((it / nslot) & 1) ^ 1, abort_flag)) {
+        if (!wait_role(empty0 + 8u * st, ((it / nslot) & 1) ^ 1, abort_flag, kWaitCycles)) {
           ok = false;
           break;
         }
@@ -541,14 +504,8 @@ __global__ void __launch_bounds__(384, 1) attn_split_kernel(const __grid_constan
         const int y = ybase + t * kTile;
         if (t + kL2Ahead < I.t1)
           for (int kb = kb0; kb < kb1; kb++) tma_prefetch_l2_2d(&maps[I.s], kb * 64, y + kL2Ahead * kTile);
-        if (pair) {
-          // this CTA's half of the boxes, into both CTAs (each CTA's full
-          // barrier expects the whole tile)
-          for (int kb = kb0; kb < kb1; kb++) tma_load_2d_mc(dst + kb * kBox, &maps[I.s], full, kb * 64, y, kBoth);
-        } else {
 #pragma unroll
-          for (int kb = 0; kb < C::KB; kb++) tma_load_2d(dst + kb * kBox, &maps[I.s], full, kb * 64, y);
-        }
+        for (int kb = 0; kb < C::KB; kb++) tma_load_2d(dst + kb * kBox, &maps[I.s], full, kb * 64, y);
         it++;
       }
     }
@@ -572,7 +529,7 @@ __global__ void __launch_bounds__(384, 1) attn_split_kernel(const __grid_constan
       const Item I = item_at(is, p, w, rank);
       const int n = I.t1 - I.t0;
       if (is_qk) {
-        if (!wait_warp(QREADY, q_ph, abort_flag)) {
+        if (!wait_warp(QREADY, q_ph, abort_flag, kWaitCycles)) {
           ok = false;
           break;
         }
@@ -581,8 +538,8 @@ __global__ void __launch_bounds__(384, 1) attn_split_kernel(const __grid_constan
       for (int k = 0; k < n; k++, t++) {
         if (is_qk) {
           const int ks = t % C::NK, b = t & 1;
-          if (!wait_warp(KFULL0 + 8u * ks, (t / C::NK) & 1, abort_flag) ||
-              (t >= 2 && !wait_warp(SFREE0 + 8u * b, ((t - 2) >> 1) & 1, abort_flag))) {
+          if (!wait_warp(KFULL0 + 8u * ks, (t / C::NK) & 1, abort_flag, kWaitCycles) ||
+              (t >= 2 && !wait_warp(SFREE0 + 8u * b, ((t - 2) >> 1) & 1, abort_flag, kWaitCycles))) {
             ok = false;
             break;
           }
@@ -593,20 +550,20 @@ __global__ void __launch_bounds__(384, 1) attn_split_kernel(const __grid_constan
 #pragma unroll
             for (int kk = 0; kk < D / 16; kk++) issue_qk_step_from<D>(tS, tQ, kd, kk);
             tc_commit(SFULL0 + 8u * b);
-            if (pair) tc_commit_mc(KEMPTY0 + 8u * ks, kBoth); else tc_commit(KEMPTY0 + 8u * ks);
+            tc_commit(KEMPTY0 + 8u * ks);
           }
           __syncwarp();
         } else {
           const int ps = t % C::NP, vs = t % C::NV;
-          if (!wait_warp(PFULL0 + 8u * ps, (t / C::NP) & 1, abort_flag) ||
-              !wait_warp(VFULL0 + 8u * vs, (t / C::NV) & 1, abort_flag)) {
+          if (!wait_warp(PFULL0 + 8u * ps, (t / C::NP) & 1, abort_flag, kWaitCycles) ||
+              !wait_warp(VFULL0 + 8u * vs, (t / C::NV) & 1, abort_flag, kWaitCycles)) {
             ok = false;
             break;
           }
           tc_fence_after();
           if (elect_one_sync()) {
             issue_pv_ss<D>(tbase + C::T_O, pring + ps * C::PTILE, desc_v(vring + vs * C::TILE, 0), k > 0);
-            if (pair) tc_commit_mc(VEMPTY0 + 8u * vs, kBoth); else tc_commit(VEMPTY0 + 8u * vs);
+            tc_commit(VEMPTY0 + 8u * vs);
             tc_commit(ODONE0 + 8u * ps);
           }
           __syncwarp();
@@ -637,7 +594,7 @@ __global__ void __launch_bounds__(384, 1) attn_split_kernel(const __grid_constan
       float m = -INFINITY, lh = 0.f;
       for (int k = 0; k < n; k++) {
         const int b = t & 1;
-        if (!wait_role(SFULL0 + 8u * b, (t >> 1) & 1, abort_flag)) {
+        if (!wait_role(SFULL0 + 8u * b, (t >> 1) & 1, abort_flag, kWaitCycles)) {
           ok = false;
           break;
         }
@@ -649,7 +606,7 @@ __global__ void __launch_bounds__(384, 1) attn_split_kernel(const __grid_constan
         const float mh = half_max(sv, kHalf);
         xmax[b][hf][lrow] = mh;
         mbar_arrive(XBAR0 + 8u * b);
-        if (!wait_role(XBAR0 + 8u * b, (t >> 1) & 1, abort_flag)) {
+        if (!wait_role(XBAR0 + 8u * b, (t >> 1) & 1, abort_flag, kWaitCycles)) {
           ok = false;
           break;
         }
@@ -662,14 +619,14 @@ __global__ void __launch_bounds__(384, 1) attn_split_kernel(const __grid_constan
         m = m_new;
         const int ps = t % C::NP;
         if (t >= static_cast<uint32_t>(C::NP) &&
-            !wait_role(ODONE0 + 8u * ps, ((t - C::NP) / C::NP) & 1, abort_flag)) {  // slot's previous PV done
+            !wait_role(ODONE0 + 8u * ps, ((t - C::NP) / C::NP) & 1, abort_flag, kWaitCycles)) {  // slot's previous PV done
           ok = false;
           break;
         }
         store_p_half(pring + ps * C::PTILE, lrow, hf, P);
         if (k > 0 && __any_sync(0xffffffffu, alpha != 1.f)) {
           const uint32_t tp = t - 1;  // PV of the previous tile must be complete
-          if (!wait_role(ODONE0 + 8u * (tp % C::NP), (tp / C::NP) & 1, abort_flag)) {
+          if (!wait_role(ODONE0 + 8u * (tp % C::NP), (tp / C::NP) & 1, abort_flag, kWaitCycles)) {
             ok = false;
             break;
           }
@@ -685,7 +642,7 @@ __global__ void __launch_bounds__(384, 1) attn_split_kernel(const __grid_constan
       if (!ok) break;
       {
         const uint32_t tp = t - 1;  // the item's last PV
-        if (!wait_role(ODONE0 + 8u * (tp % C::NP), (tp / C::NP) & 1, abort_flag)) {
+        if (!wait_role(ODONE0 + 8u * (tp % C::NP), (tp / C::NP) & 1, abort_flag, kWaitCycles)) {
           ok = false;
           break;
         }
@@ -706,7 +663,6 @@ __global__ void __launch_bounds__(384, 1) attn_split_kernel(const __grid_constan
   tc_fence_before();
   __syncthreads();
   tc_fence_after();
-  if (pair) cluster_sync();  // the peer no longer writes into this CTA's shared memory or barriers
   if (warp == 1) tmem_dealloc(tbase, C::COLS);
 }
 
@@ -756,6 +712,7 @@ __global__ void __launch_bounds__(256, 1) attn_tail_kernel(const __grid_constant
     const int off0 = p.node_off[0];
     MetaView mv = meta_view(const_cast<void*>(p.meta), p.n_total);
     depth = mv.depth[node_g];
+    depth = depth < 0 ? 0 : (depth >= TV_MAX_PATH ? TV_MAX_PATH - 1 : depth);
     const int a = threadIdx.x < TV_MAX_PATH ? mv.anc_at[static_cast<size_t>(node_g) * TV_MAX_PATH + threadIdx.x] : 0;
     off = off0;
     L = lens[0];
@@ -767,7 +724,11 @@ __global__ void __launch_bounds__(256, 1) attn_tail_kernel(const __grid_constant
         L = lens[i + 1];
       }
     }
-    if (threadIdx.x < TV_MAX_PATH) anc_s[threadIdx.x] = threadIdx.x > depth ? node_g : off + a;
+    // clamped to the node buffers: with a malformed tree (reported by
+    // tv_tree_prepare) the tables may be stale, and the first tile is
+    // gathered before the status word is read
+    const int an = threadIdx.x > depth ? node_g : off + a;
+    if (threadIdx.x < TV_MAX_PATH) anc_s[threadIdx.x] = an < 0 ? 0 : (an >= p.n_total ? p.n_total - 1 : an);
   }
   const int local = node_g - off;
   const int G = p.G;
@@ -1227,31 +1188,10 @@ static tv_status launch_tc(TcParams& p, int n_items_bound, int n_tail, cudaStrea
     attrs = true;
   }
   if (n_items_bound > 0) {
-    if (p.pair) {
-      // one 2-CTA cluster per item, at most one cluster per pair of SMs
-      const int pairs = n_items_bound < num_sms() / 2 ? n_items_bound : num_sms() / 2;
-      cudaLaunchConfig_t cfg = {};
-      cfg.gridDim = dim3(2 * pairs);
-      cfg.blockDim = dim3(384);
-      cfg.dynamicSmemBytes = C::SMEM_SPLIT;
-      cfg.stream = st;
-      cudaLaunchAttribute attr[2];
-      attr[0].id = cudaLaunchAttributeClusterDimension;
-      attr[0].val.clusterDim.x = 2;
-      attr[0].val.clusterDim.y = 1;
-      attr[0].val.clusterDim.z = 1;
-      cfg.attrs = attr;
-      cfg.numAttrs = 1;
-      if (ov) {
-        attr[1].id = cudaLaunchAttributeProgrammaticStreamSerialization;
-        attr[1].val.programmaticStreamSerializationAllowed = 1;
-        cfg.numAttrs = 2;
-      }
-      cudaLaunchKernelEx(&cfg, attn_split_kernel<D>, p);
-    } else {
-      const int grid = n_items_bound < num_sms() ? n_items_bound : num_sms();
-      launch_k(ov, attn_split_kernel<D>, dim3(grid), dim3(384), C::SMEM_SPLIT, st, p);
-    }
+    // pair mode: two CTAs per item (row blocks 0 and 1), at most one CTA per SM
+    const int per = p.pair ? 2 : 1;
+    const int units = n_items_bound < num_sms() / per ? n_items_bound : num_sms() / per;
+    launch_k(ov, attn_split_kernel<D>, dim3(per * units), dim3(384), C::SMEM_SPLIT, st, p);
   }
   launch_k(ov, attn_tail_kernel<D>, dim3(n_tail), dim3(256), smem_tail, st, p);
   return launch_status();

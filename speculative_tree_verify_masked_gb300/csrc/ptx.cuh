@@ -103,6 +103,42 @@ __device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity, long lo
   return true;
 }
 
+// Warp-wide bounded wait: a non-blocking test first (the common case in a
+// full pipeline), then polling; gives up after `limit` SM clocks, or as soon
+// as another role has given up (*abort_flag), and then raises the flag for
+// the others.  The outcome is the same in every lane.
+__device__ __forceinline__ bool wait_warp(uint32_t bar, uint32_t parity, volatile int* abort_flag, long long limit) {
+  if (__all_sync(0xffffffffu, mbar_test(bar, parity))) return true;
+  const long long t0 = clock64();
+  while (true) {
+    const bool done = mbar_try_wait(bar, parity);
+    if (__all_sync(0xffffffffu, done)) return true;
+    int give_up = 0;
+    if (lane_id() == 0) {
+      if (*abort_flag) give_up = 1;
+      else if (clock64() - t0 > limit) {
+        *abort_flag = 1;
+        give_up = 1;
+      }
+    }
+    if (__shfl_sync(0xffffffffu, give_up, 0)) return false;
+  }
+}
+
+// Single-thread bounded wait with the same give-up rules.
+__device__ __forceinline__ bool wait_role(uint32_t bar, uint32_t parity, volatile int* abort_flag, long long limit) {
+  if (mbar_try_wait(bar, parity)) return true;
+  const long long t0 = clock64();
+  while (true) {
+    if (mbar_try_wait(bar, parity)) return true;
+    if (*abort_flag) return false;
+    if (clock64() - t0 > limit) {
+      *abort_flag = 1;
+      return false;
+    }
+  }
+}
+
 // ----------------------------------------------------------------------------
 // TMA
 // ----------------------------------------------------------------------------
@@ -119,37 +155,6 @@ __device__ __forceinline__ void tma_load_2d(uint32_t dst, const CUtensorMap* map
       "l"(reinterpret_cast<uint64_t>(map)), "r"(bar), "r"(x), "r"(y)
       : "memory");
 }
-// ----------------------------------------------------------------------------
-// Thread-block clusters
-// ----------------------------------------------------------------------------
-__device__ __forceinline__ uint32_t cluster_ctarank() {
-  uint32_t r;
-  asm volatile("mov.u32 %0, %%cluster_ctarank;" : "=r"(r));
-  return r;
-}
-// Every thread of every CTA of the cluster (release / acquire).
-__device__ __forceinline__ void cluster_sync() {
-  asm volatile("barrier.cluster.arrive.release.aligned;\n\tbarrier.cluster.wait.acquire.aligned;" ::: "memory");
-}
-// TMA 2-D load written to the same shared-memory offset of every CTA in
-// `mask`, each CTA's mbarrier at `bar`'s offset counting the bytes it gets.
-__device__ __forceinline__ void tma_load_2d_mc(uint32_t dst, const CUtensorMap* map, uint32_t bar, int x, int y,
-                                               uint16_t mask) {
-  asm volatile(
-      "cp.async.bulk.tensor.2d.shared::cluster.global.tile.mbarrier::complete_tx::bytes.multicast::cluster"
-      " [%0], [%1, {%3, %4}], [%2], %5;" ::"r"(dst),
-      "l"(reinterpret_cast<uint64_t>(map)), "r"(bar), "r"(x), "r"(y), "h"(mask)
-      : "memory");
-}
-// Arrive on the mbarrier at `bar`'s offset in every CTA of `mask` once this
-// thread's tcgen05 operations so far have completed.
-__device__ __forceinline__ void tc_commit_mc(uint32_t bar, uint16_t mask) {
-  asm volatile(
-      "tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.multicast::cluster.b64 [%0], %1;" ::"r"(bar),
-      "h"(mask)
-      : "memory");
-}
-
 // Contiguous global -> shared copy on the TMA engine (addresses and size
 // multiples of 16 bytes), completing on an mbarrier transaction count.
 __device__ __forceinline__ void bulk_g2s(uint32_t dst, const void* src, uint32_t bytes, uint32_t bar) {

@@ -185,6 +185,33 @@ def test_static_scratch_rejects_oversized_request_on_host(L):
     assert rc == 11  # TV_ERR_SCRATCH
 
 
+def test_static_scratch_rejects_ill_formed_tree_on_host(L):
+    """An ill-formed tree descriptor or a negative length bound is an argument
+    error (1) for the static call, as for the workspace call, even when the
+    counts would wrap the scratch size computation."""
+    layer, keep = _bf16_layer(cap=40000)
+    pl = B.tv_plan(4096)
+    vp = ctypes.c_void_p
+    args = (vp(16), vp(16), vp(16), vp(16), 0.0625, None)
+    bad_trees = [
+        B.tv_tree(-1, 4, 4, 0x1000, 0x2000, 0x3000, 0x4000),   # negative sequence count
+        B.tv_tree(1, 4, -3, 0x1000, 0x2000, 0x3000, 0x4000),   # negative tree bound
+        B.tv_tree(1, 4, 65, 0x1000, 0x2000, 0x3000, 0x4000),   # tree bound above 64 nodes
+        B.tv_tree(9, 9, 1, 0x1000, 0x2000, 0x3000, 0x4000),    # more than 8 sequences
+        B.tv_tree(1, 4, 4, 0x1000, 0x2000, 0x3000, 0x4008),    # status word not 16-byte aligned
+        B.tv_tree(1, 4, 4, 0, 0x2000, 0x3000, 0x4000),         # no node offsets
+    ]
+    for t in bad_trees:
+        rc = L.tv_attn_tree_verify_static(ctypes.byref(pl), ctypes.byref(layer), ctypes.byref(t), vp(16), 32768,
+                                          *args)
+        assert rc == 1, (t.n_seq, t.n_total, t.n_max, rc)
+    good = B.tv_tree(1, 4, 4, 0x1000, 0x2000, 0x3000, 0x4000)
+    assert L.tv_attn_tree_verify_static(ctypes.byref(pl), ctypes.byref(layer), ctypes.byref(good), vp(16), -1,
+                                        *args) == 1
+    assert L.tv_attn_tree_verify_static(ctypes.byref(pl), ctypes.byref(layer), None, vp(16), 32768, *args) == 1
+    assert L.tv_attn_tree_verify_static(ctypes.byref(pl), None, ctypes.byref(good), vp(16), 32768, *args) == 1
+
+
 def test_auto_split_is_the_makespan_minimum():
     """Brute force over every split on a small case, with the stated cost model."""
     lens, nodes, Hq, Hkv, sms = [8192, 1024], [16, 5], 8, 2, 7

@@ -111,6 +111,16 @@ def test_verify_rows_equal_decode_rows_full_size():
     check_rows_equal_decode(r, paths_per_seq=3, rng=np.random.default_rng(0))
 
 
+def test_verify_rows_equal_decode_rows_four_sequences():
+    """Four sequences in one launch (contexts 65,536 / 8,192 x 3, 16-node
+    trees): for every sequence, its accepted path and three random root
+    paths, decoded on that sequence's own cache and state, give the verified
+    rows bit for bit on one attention and one GDN layer of the stack."""
+    cfg = synth.workload(4)
+    r = VerifyRound(cfg, layers=[2, 3])
+    check_rows_equal_decode(r, paths_per_seq=3, rng=np.random.default_rng(1))
+
+
 def test_commit_equals_decode_replay():
     """The committed state is the decode replay of the accepted path, bit for bit."""
     r = VerifyRound(synth.workload(2))
@@ -243,7 +253,8 @@ def test_overlapped_launch_gives_same_bits(cfg_id):
     """A round launched with TV_TREE_OVERLAP (programmatic dependent launch)
     gives the same bits as the same round launched plainly: outputs of every
     verified layer, the accepted path, and the committed caches and states.
-    On the 64-layer workload the attention layers also run as 2-CTA clusters."""
+    On the 64-layer workload the attention layers also run as CTA pairs
+    (two 128-row blocks streaming the same tiles)."""
     cfg = synth.workload(cfg_id)
     layers = None if cfg.n_layers <= 2 else [0, 1, 2, 3, 7]
     runs = []

@@ -6,13 +6,16 @@
 * A node's rows do not depend on the rest of its tree (each row is a function
   of its own query and its ancestors), so the graph for a prefix of a tree
   gives exactly the full tree's rows for those nodes -- across the widths
-  where the attention path changes its launch (one 128-row block, a 2-CTA
-  cluster for two blocks, three blocks).
+  where the attention path changes its launch (one 128-row block, a CTA
+  pair for two blocks, three blocks).  Some of those replays are also checked
+  against the oracle directly.
 * The accept walk on the prefix stops where the full tree's path leaves it.
 """
 import pytest
 import torch
 
+import oracle.tree_verify as O
+from gpu_helpers import check_close, f64
 from speculative_tree_verify_masked_gb300 import binding as B
 from speculative_tree_verify_masked_gb300 import synth
 from speculative_tree_verify_masked_gb300.graphs import ShapeGraphs, prefix_trees, shape_key
@@ -97,6 +100,16 @@ def test_prefix_graphs_give_the_full_trees_rows():
         got = outputs(r, w)
         for li in got:
             assert torch.equal(got[li], full[li][:w]), f"width {w}, layer {li}"
+        if w in (5, 22, 43):  # one width per attention launch form, against the oracle
+            pw = parents[:w]
+            for li, a in r.attn.items():
+                ref = O.attn_tree_verify(f64(a["layer"].K[0][:, :3000]), f64(a["layer"].V[0][:, :3000]), 3000,
+                                         f64(a["q"][:w]), f64(a["k_t"][:w]), f64(a["v_t"][:w]), pw, r.attn_scale)
+                check_close(got[li], ref, f"graph width {w} attention layer {li}")
+            for li, g in r.gdn.items():
+                ref = O.gdn_tree_verify(f64(snap[li][0]), f64(g["q"][:w]), f64(g["k"][:w]), f64(g["v"][:w]),
+                                        f64(g["alpha"][:w]), f64(g["beta"][:w]), pw, r.gdn_scale)
+                check_close(got[li], ref, f"graph width {w} GDN layer {li}")
         want_path = [x for x in path if x < w]
         a = int(r.acc_len[0])
         assert a == len(want_path), (w, a, want_path)

@@ -10,6 +10,7 @@ rows back returns exactly the pages no kept row touches.
 import pytest
 import torch
 
+from gpu_helpers import check_close, check_state, oracle_attn, oracle_commit_state, oracle_gdn, seq_slice
 from speculative_tree_verify_masked_gb300 import binding as B
 from speculative_tree_verify_masked_gb300 import synth
 from speculative_tree_verify_masked_gb300.round import VerifyRound
@@ -66,10 +67,24 @@ def test_pooled_rounds_equal_static_rounds():
             rp.commit_kv()
             lens = rp.len.tolist()
             assert pool.committed_bytes == expected_committed(rp, page, lambda q: min(rp.cap, lens[q] + margin))
+            S_before = {(li, q): S.clone() for li, g in rp.gdn.items() for q, S in enumerate(g["layer"].S)}
             rs.run(reset_len=False)
             rp.run(reset_len=False)
             torch.cuda.synchronize()
             assert rs.status() == 0 and rp.status() == 0
+            if rnd in (0, 5):  # pooled rounds against the oracle, before and after the page boundary
+                for q, L in enumerate(lens):
+                    lo, hi = seq_slice(rp, q)
+                    path = rp.path[q, :int(rp.acc_len[q])].tolist()
+                    for li in rp.attn:
+                        check_close(rp.attn[li]["out"][lo:hi], oracle_attn(rp, li, q, L=L),
+                                    f"pooled round {rnd} attention seq {q}")
+                    for li in rp.gdn:
+                        S0 = S_before[(li, q)]
+                        check_close(rp.gdn[li]["out"][lo:hi], oracle_gdn(rp, li, q, S0=S0),
+                                    f"pooled round {rnd} GDN seq {q}")
+                        check_state(rp.gdn[li]["layer"].S[q], oracle_commit_state(rp, li, q, S0, path),
+                                    f"pooled round {rnd} state seq {q}")
             assert torch.equal(rs.len, rp.len), rnd
             for name in ("path", "acc_len", "bonus"):
                 assert torch.equal(getattr(rs, name), getattr(rp, name)), (rnd, name)
