@@ -4,30 +4,28 @@
 // applied along every node's root path).  A lane group of LPR lanes owns two
 // state rows of one value head of one sequence, each with the lane layout
 // and the step arithmetic of decode and commit (gdn_step.cuh), so a verified
-// row is the decoded row bit for bit by construction.  A CTA of four warps
-// owns 4 * 2 * 32/LPR consecutive rows of one value head and stages the
-// tree's keys and queries (bf16, by cp.async), gates and values once.  The
+// row is the decoded row bit for bit by construction.  A CTA of W warps
+// owns W * 2 * 32/LPR consecutive rows of one value head and stages the
+// tree's keys and queries (by cp.async), gates and values once.  The
 // lane groups walk the tree in the order prepared by tv_tree_prepare, cut
 // into segments that restore a saved state only at their start and save one
-// only at their end, so the visits of a segment run without branches: a
-// leaf runs the same update with alpha = 1 and c = 0, which leaves the state
-// as it is (up to the sign of a zero element, which no later dot product can
-// see: every accumulator starts at +0), so its siblings still find their
-// parent's state in registers.  The few states that must outlive a subtree
+// only at their end.  Every lane group of a CTA visits the same node at the
+// same time, so the one branch inside a segment, a leaf skipping its update,
+// is uniform; a leaf leaves the state as it is, so its siblings still find
+// their parent's state in registers.  The few states that must outlive a subtree
 // sit in shared-memory slots.  No per-node state is written to memory: the
 // kernel reads the committed state once and writes one output value per
 // (node, row).
 //
-// Bound.  The chain of steps along the tree, not the 4 * Hv * dv * dk bytes
-// of state, sets the layer's time.  A warp issues its step in order, so the
-// dependent pieces of a visit (shared-memory loads, packed fp32 FMAs at one
-// per two cycles, the butterfly over the group, the update) add up unless
-// the compiler can overlap them, which branches inside the loop prevent, or
-// another warp fills the gaps: eight rows per warp (16 columns per lane, two
-// rows per lane group, one 16-byte bf16 load per chunk serving both rows)
-// give a 48-head x 128-row layer 768 warps, about two per SM sub-partition;
-// four warps per CTA share one staged copy of the tree's inputs (two warps:
-// the 64-layer round 39 us slower, 64-node trees of 4 sequences 5 % slower).
+// Bound.  The chain of dependent steps along the tree, not the
+// 4 * Hv * dv * dk bytes of state, sets the layer's time: every visit is a
+// chain of dependent pieces (shared-memory loads, packed fp32 FMAs, the
+// butterfly over the group, the update) that a warp issues in order, and
+// the tree's visits run one after another.  Two rows per lane group (16
+// columns per lane, one 16-byte bf16 load per chunk of the node's key or
+// query serving both rows) and CTAs of four or eight warps that share one
+// staged copy of the tree's inputs; leaves skip the update (nothing reads
+// their state).
 #include "common.cuh"
 #include "gdn_step.cuh"
 #include "host.hpp"
@@ -57,23 +55,32 @@ inline int slots_for(int n_max) {
   return k;
 }
 
-template <int LPR>
+// Layout of a verify CTA: WARPS warps, lane groups of LPR lanes, RPG state
+// rows per lane group (each row with the lane layout of gdn_step.cuh).
+template <int LPR, int RPG, int WARPS>
 struct GdnShape {
   static constexpr int DK = 2 * kPairs * LPR;  // key dim
-  static constexpr int W = 4;                  // warps per CTA
+  static constexpr int W = WARPS;              // warps per CTA
   static constexpr int NG = W * 32 / LPR;      // lane groups per CTA
-  static constexpr int RPG = 2;                // state rows per lane group
   static constexpr int R = NG * RPG;           // state rows per CTA
 };
+// The verify kernel runs two rows per lane group with CTAs of 4 or 8 warps:
+// 8 when CTAs of 4 warps would number at most two per SM (then one CTA of 8
+// warps per SM stages the tree once for twice the rows and keeps two warps
+// per scheduler; measured on one GDN layer of the 64-layer workload, 15.2
+// against 17.7 us), 4 otherwise (more sequences: 18.5 against 18.9 us on the
+// four-sequence workload).
+constexpr int kGdnRpg = 2;
 
-// Shared memory: slots [n_slots][R][DK] f32 | keys, queries [n_max][DK] T |
+// Shared memory: slots [n_slots][R][DK] f32 | keys, queries [n_max][DK] KQ |
 // (alpha, beta, k.q, -) [n_max] | v [n_max][R] f32 | visits [n_max] | segments [n_max].
-template <typename T, int LPR>
+// KQ is the input type: staging keys and queries widened to fp32 measured
+// no faster per visit and takes twice the shared memory.
+template <typename KQ, typename Sh>
 inline size_t gdn_verify_smem(int n_max, int n_slots) {
-  using Sh = GdnShape<LPR>;
   const size_t n = static_cast<size_t>(n_max);
   size_t b = static_cast<size_t>(n_slots) * Sh::R * Sh::DK * 4;
-  b += 2 * ((n * Sh::DK * sizeof(T) + 15) / 16 * 16);
+  b += 2 * ((n * Sh::DK * sizeof(KQ) + 15) / 16 * 16);
   b += n * 16 + n * Sh::R * 4 + 2 * n * 4;
   return b;
 }
@@ -82,36 +89,48 @@ __device__ __forceinline__ void cp_async16_g(void* dst, const void* src) {
   asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(static_cast<uint32_t>(__cvta_generic_to_shared(dst))), "l"(src) : "memory");
 }
 
-template <typename T, int LPR>
-__global__ void __launch_bounds__(32 * GdnShape<LPR>::W) gdn_verify_kernel(const GdnVerifyParams p) {
-  using Sh = GdnShape<LPR>;
-  constexpr int DK = Sh::DK, R = Sh::R, NG = Sh::NG, NT = 32 * Sh::W;
+// Values of a lane group's RPG rows (consecutive fp32 in shared memory).
+template <int N>
+__device__ __forceinline__ void load_vals(float (&v)[N], const float* src) {
+  if constexpr (N == 4) {
+    const float4 t = *reinterpret_cast<const float4*>(src);
+    v[0] = t.x; v[1] = t.y; v[2] = t.z; v[3] = t.w;
+  } else if constexpr (N == 2) {
+    const float2 t = *reinterpret_cast<const float2*>(src);
+    v[0] = t.x; v[1] = t.y;
+  } else {
+#pragma unroll
+    for (int i = 0; i < N; i++) v[i] = src[i];
+  }
+}
+
+template <typename T, int LPR, int RPG, int WARPS>
+__global__ void __launch_bounds__(32 * WARPS) gdn_verify_kernel(const GdnVerifyParams p) {
+  using KQ = T;
+  using Sh = GdnShape<LPR, RPG, WARPS>;
+  constexpr int DK = Sh::DK, R = Sh::R, NG = Sh::NG, NT = 32 * WARPS;
   const int s = blockIdx.y;
   const int rb_per_head = (p.dv + R - 1) / R;
   const int h = blockIdx.x / rb_per_head;
   const int rb = blockIdx.x % rb_per_head;
   const int tid = threadIdx.x, j = tid % LPR;
   const int gi = tid / LPR;                 // lane group within the CTA
-  const int row0 = rb * R + 2 * gi;         // the group's rows: row0, row0 + 1
-  const bool valid0 = row0 < p.dv, valid1 = row0 + 1 < p.dv;
+  const int row0 = rb * R + RPG * gi;       // the group's rows: row0 .. row0 + RPG - 1
 
   // this group's state rows first (they do not depend on the tree, and no
   // kernel of the round before commit writes them), so their loads overlap
   // the previous kernel's end and everything up to the first step
-  f2_t st0[kPairs], st1[kPairs];
+  f2_t st[RPG][kPairs];
   {
     const float* S = p.S[s] + static_cast<size_t>(h) * p.dv * DK;
-    if (valid0) {
-      load_row<LPR>(st0, S + static_cast<size_t>(row0) * DK, j);
-    } else {
 #pragma unroll
-      for (int e = 0; e < kPairs; e++) st0[e] = 0ull;
-    }
-    if (valid1) {
-      load_row<LPR>(st1, S + static_cast<size_t>(row0 + 1) * DK, j);
-    } else {
+    for (int i = 0; i < RPG; i++) {
+      if (row0 + i < p.dv) {
+        load_row<LPR>(st[i], S + static_cast<size_t>(row0 + i) * DK, j);
+      } else {
 #pragma unroll
-      for (int e = 0; e < kPairs; e++) st1[e] = 0ull;
+        for (int e = 0; e < kPairs; e++) st[i][e] = 0ull;
+      }
     }
   }
   pdl_wait();  // tree tables, status and node inputs come from earlier kernels
@@ -129,9 +148,9 @@ __global__ void __launch_bounds__(32 * GdnShape<LPR>::W) gdn_verify_kernel(const
 
   extern __shared__ float4 smem4[];
   float* slots = reinterpret_cast<float*>(smem4);  // [n_slots][R][DK]
-  T* kb = reinterpret_cast<T*>(slots + static_cast<size_t>(p.n_slots) * R * DK);
-  const size_t kq_bytes = (static_cast<size_t>(p.n_max) * DK * sizeof(T) + 15) / 16 * 16;
-  T* qb = reinterpret_cast<T*>(reinterpret_cast<uint8_t*>(kb) + kq_bytes);
+  KQ* kb = reinterpret_cast<KQ*>(slots + static_cast<size_t>(p.n_slots) * R * DK);
+  const size_t kq_bytes = (static_cast<size_t>(p.n_max) * DK * sizeof(KQ) + 15) / 16 * 16;
+  KQ* qb = reinterpret_cast<KQ*>(reinterpret_cast<uint8_t*>(kb) + kq_bytes);
   float4* nc = reinterpret_cast<float4*>(reinterpret_cast<uint8_t*>(qb) + kq_bytes);  // [n_max]
   float* vb = reinterpret_cast<float*>(nc + p.n_max);                                // [n_max][R]
   int* sch = reinterpret_cast<int*>(vb + static_cast<size_t>(p.n_max) * R);          // [n_max] visits
@@ -145,7 +164,7 @@ __global__ void __launch_bounds__(32 * GdnShape<LPR>::W) gdn_verify_kernel(const
     const T* kg = static_cast<const T*>(p.k);
     const T* qg = static_cast<const T*>(p.q);
     const T* vg = static_cast<const T*>(p.v);
-    constexpr int CPR = DK * static_cast<int>(sizeof(T)) / 16;  // 16-byte chunks of a row
+    constexpr int CPR = DK * static_cast<int>(sizeof(T)) / 16;  // 16-byte chunks of a source row
     constexpr int EPC = 16 / static_cast<int>(sizeof(T));       // elements per chunk
     for (int idx = tid; idx < n * CPR; idx += NT) {
       const int node = idx / CPR, c = idx % CPR;
@@ -209,21 +228,29 @@ __global__ void __launch_bounds__(32 * GdnShape<LPR>::W) gdn_verify_kernel(const
   __syncthreads();
 
   T* out = static_cast<T*>(p.out) + (static_cast<size_t>(off) * p.Hv + h) * p.dv + row0;
-  float* slot0 = slots + static_cast<size_t>(2 * gi) * DK;  // the group's rows in slot 0
+  float* slot0 = slots + static_cast<size_t>(RPG * gi) * DK;  // the group's rows in slot 0
   const size_t out_stride = static_cast<size_t>(p.Hv) * p.dv;
-  const bool pair_store = sizeof(T) == 2 && valid1 && (p.dv % 2) == 0;
+  const bool vec_store = sizeof(T) == 2 && (RPG == 2 || RPG == 4) && row0 + RPG <= p.dv && (p.dv % RPG) == 0;
   // Outputs go out as explicit global stores: the compiler then knows they
   // cannot alias the shared-memory tables and may issue the next visit's
   // loads ahead of them.
-  auto put = [&](int node, float o0, float o1) {
+  auto put = [&](int node, const float (&o)[RPG]) {
     T* dst = out + static_cast<size_t>(node) * out_stride;
-    if (pair_store) {
-      const uint32_t w = static_cast<uint32_t>(__bfloat16_as_ushort(__float2bfloat16_rn(o0))) |
-                         (static_cast<uint32_t>(__bfloat16_as_ushort(__float2bfloat16_rn(o1))) << 16);
-      asm volatile("st.global.b32 [%0], %1;" ::"l"(dst), "r"(w));
+    if (vec_store) {
+      uint32_t w[RPG / 2 > 0 ? RPG / 2 : 1];
+#pragma unroll
+      for (int i = 0; i + 1 < RPG; i += 2)
+        w[i / 2] = static_cast<uint32_t>(__bfloat16_as_ushort(__float2bfloat16_rn(o[i]))) |
+                   (static_cast<uint32_t>(__bfloat16_as_ushort(__float2bfloat16_rn(o[i + 1]))) << 16);
+      if constexpr (RPG == 4) {
+        asm volatile("st.global.v2.b32 [%0], {%1, %2};" ::"l"(dst), "r"(w[0]), "r"(w[1]));
+      } else {
+        asm volatile("st.global.b32 [%0], %1;" ::"l"(dst), "r"(w[0]));
+      }
     } else {
-      if (valid0) store_global(dst, from_f32<T>(o0));
-      if (valid1) store_global(dst + 1, from_f32<T>(o1));
+#pragma unroll
+      for (int i = 0; i < RPG; i++)
+        if (row0 + i < p.dv) store_global(dst + i, from_f32<T>(o[i]));
     }
   };
   const float scale = p.scale;
@@ -235,14 +262,15 @@ __global__ void __launch_bounds__(32 * GdnShape<LPR>::W) gdn_verify_kernel(const
   load_row_any<LPR>(k, kb + static_cast<size_t>(e & 0xFF) * DK, j);
   load_row_any<LPR>(q, qb + static_cast<size_t>(e & 0xFF) * DK, j);
   float4 c4 = nc[e & 0xFF];
-  float2 v2 = *reinterpret_cast<const float2*>(vb + (e & 0xFF) * R + 2 * gi);
+  float vv[RPG];
+  load_vals<RPG>(vv, vb + (e & 0xFF) * R + RPG * gi);
   for (int sg = 0; sg < n_seg; sg++) {
     const int sw = sgt[sg];
     const int first = sw & 0xFF, cnt = (sw >> 8) & 0xFF, src = (sw >> 16) & 0xFF, save = (sw >> 24) & 0xFF;
     if (src) {
       const float* sl = slot0 + static_cast<size_t>(src - 1) * R * DK;
-      load_row<LPR>(st0, sl, j);
-      load_row<LPR>(st1, sl + DK, j);
+#pragma unroll
+      for (int i = 0; i < RPG; i++) load_row<LPR>(st[i], sl + i * DK, j);
     }
     // the visits of the segment: no branch but the lane-0 store.  Each sum,
     // c and o is formed exactly as gdn_row_step forms it.  The next visit's
@@ -258,15 +286,28 @@ __global__ void __launch_bounds__(32 * GdnShape<LPR>::W) gdn_verify_kernel(const
       load_row_any<LPR>(kn, kb + static_cast<size_t>(en & 0xFF) * DK, j);
       load_row_any<LPR>(qn, qb + static_cast<size_t>(en & 0xFF) * DK, j);
       const float4 c4n = nc[en & 0xFF];
-      const float2 v2n = *reinterpret_cast<const float2*>(vb + (en & 0xFF) * R + 2 * gi);
-      float d[4] = {row_partial(st0, k), row_partial(st0, q), row_partial(st1, k), row_partial(st1, q)};
-      group_sum_n<LPR, 4>(d);
-      const float c0 = gdn_c(d[0], v2.x, c4.x, c4.y), c1 = gdn_c(d[2], v2.y, c4.x, c4.y);
-      const float o0 = gdn_o(c0, c4.z, c4.x, d[1], scale), o1 = gdn_o(c1, c4.z, c4.x, d[3], scale);
-      const float au = hc ? c4.x : 1.f;
-      gdn_update(st0, k, au, hc ? c0 : 0.f);
-      gdn_update(st1, k, au, hc ? c1 : 0.f);
-      if (j == 0) put(node, o0, o1);
+      float vn[RPG];
+      load_vals<RPG>(vn, vb + (en & 0xFF) * R + RPG * gi);
+      float d[2 * RPG];
+#pragma unroll
+      for (int i = 0; i < RPG; i++) {
+        d[2 * i] = row_partial(st[i], k);
+        d[2 * i + 1] = row_partial(st[i], q);
+      }
+      group_sum_n<LPR, 2 * RPG>(d);
+      float c[RPG], o[RPG];
+#pragma unroll
+      for (int i = 0; i < RPG; i++) {
+        c[i] = gdn_c(d[2 * i], vv[i], c4.x, c4.y);
+        o[i] = gdn_o(c[i], c4.z, c4.x, d[2 * i + 1], scale);
+      }
+      if (j == 0) put(node, o);
+      // a leaf's state is never read, so its update is skipped (the branch
+      // is uniform over the CTA: every lane group visits the same node)
+      if (hc) {
+#pragma unroll
+        for (int i = 0; i < RPG; i++) gdn_update(st[i], k, c4.x, c[i]);
+      }
       e = en;
 #pragma unroll
       for (int i = 0; i < kPairs; i++) {
@@ -274,12 +315,13 @@ __global__ void __launch_bounds__(32 * GdnShape<LPR>::W) gdn_verify_kernel(const
         q[i] = qn[i];
       }
       c4 = c4n;
-      v2 = v2n;
+#pragma unroll
+      for (int i = 0; i < RPG; i++) vv[i] = vn[i];
     }
     if (save) {
       float* sl = slot0 + static_cast<size_t>(save - 1) * R * DK;
-      store_row<LPR>(sl, st0, j);
-      store_row<LPR>(sl + DK, st1, j);
+#pragma unroll
+      for (int i = 0; i < RPG; i++) store_row<LPR>(sl + i * DK, st[i], j);
     }
   }
 }
@@ -346,18 +388,26 @@ static bool gdn_shape_ok(const tv_gdn_layer* l) {
          (l->dk == 64 || l->dk == 128) && l->dv >= 1 && l->dv <= 256 && l->S;
 }
 
-template <typename T, int LPR>
-static void launch_verify(const GdnVerifyParams& p, int n_seq, cudaStream_t st, bool ov) {
-  constexpr int R = GdnShape<LPR>::R;
+template <typename T, int LPR, int WARPS>
+static void launch_verify_w(const GdnVerifyParams& p, int n_seq, cudaStream_t st, bool ov) {
+  using Sh = GdnShape<LPR, kGdnRpg, WARPS>;
+  constexpr int R = Sh::R;
+  auto kern = gdn_verify_kernel<T, LPR, kGdnRpg, WARPS>;
   static bool attrs = false;  // one-time, sized for the largest tree
   if (!attrs) {
-    const int smem_max = static_cast<int>(gdn_verify_smem<T, LPR>(TV_MAX_NODES, slots_for(TV_MAX_NODES)));
-    cudaFuncSetAttribute(gdn_verify_kernel<T, LPR>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem_max);
+    const int smem_max = static_cast<int>(gdn_verify_smem<T, Sh>(TV_MAX_NODES, slots_for(TV_MAX_NODES)));
+    cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem_max);
     attrs = true;
   }
   const dim3 grid(p.Hv * ((p.dv + R - 1) / R), n_seq);
-  launch_k(ov, gdn_verify_kernel<T, LPR>, grid, dim3(32 * GdnShape<LPR>::W),
-           gdn_verify_smem<T, LPR>(p.n_max, p.n_slots), st, p);
+  launch_k(ov, kern, grid, dim3(32 * WARPS), gdn_verify_smem<T, Sh>(p.n_max, p.n_slots), st, p);
+}
+template <typename T, int LPR>
+static void launch_verify(const GdnVerifyParams& p, int n_seq, cudaStream_t st, bool ov) {
+  constexpr int R4 = GdnShape<LPR, kGdnRpg, 4>::R;
+  const long long ctas4 = static_cast<long long>(p.Hv) * ((p.dv + R4 - 1) / R4) * n_seq;
+  if (ctas4 <= 2LL * num_sms()) launch_verify_w<T, LPR, 8>(p, n_seq, st, ov);
+  else launch_verify_w<T, LPR, 4>(p, n_seq, st, ov);
 }
 
 template <typename T, int LPR>
