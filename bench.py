@@ -78,12 +78,11 @@ def round_bytes(cfg, n_nodes_per_seq, acc_lens):
 
 
 # DRAM bytes (read + write) of one attention verify call (split + tail
-# kernels) from a single-pass ncu capture at full size on a GB300, keyed by
-# workload name; the capture command and the figures are in
-# profiles/attn_traffic_64layer_128k.md.  Update together with the kernels.
-MEASURED_TRAFFIC = {
-    "64-layer mixer stack (48 GDN + 16 attention), L 131072, 32-node tree": 537351424 + 21152768 + 1061888,
-}
+# kernels) on a GB300, keyed by workload name: dram__bytes_read.sum +
+# dram__bytes_write.sum from an ncu capture of the current kernels.  A figure
+# is dropped whenever the kernels change and stays absent (reported as null)
+# until it is captured again.
+MEASURED_TRAFFIC: dict[str, int] = {}
 
 
 # ---------------------------------------------------------------------------
@@ -150,75 +149,179 @@ class ClockSampler:
 
 
 # ---------------------------------------------------------------------------
-# oracle sample (CPU baseline and reference arm)
+# workload description shared by both arms
 # ---------------------------------------------------------------------------
-def oracle_sample_inputs(cfg, device):
-    """Inputs of one 4-layer block (3 GDN + 1 attention) of sequence 0."""
-    from speculative_tree_verify_masked_gb300 import synth
-    parent, tok, greedy, _ = synth.tree_and_tokens(cfg, 0)
-    n = len(parent)
-    L = cfg.ctx_lens[0]
-    attn_li = cfg.attn_layers[0]
-    gdn_lis = [i for i in range(cfg.n_layers) if not cfg.is_attn(i)][:3]
-    a = synth.attn_layer_inputs(cfg, attn_li, 0, n, L + 64, device)
-    gs = [synth.gdn_layer_inputs(cfg, li, 0, n, device) for li in gdn_lis]
-    return parent, tok, greedy, a, gs
-
-
-def time_oracle(cfg, inputs, attn_kv_heads, attn_nodes, gdn_heads, gdn_nodes):
-    """Run the oracle on a sample of one 4-layer block of sequence 0:
-    attention for `attn_kv_heads` KV heads over the first `attn_nodes` tree
-    nodes (a prefix of a topologically ordered tree is a tree) with the full
-    context, and GDN for `gdn_heads` value heads over the first `gdn_nodes`
-    nodes of each of the block's GDN layers, plus the accept walk and the
-    commit.  The round estimate scales attention by query rows (each costs
-    one pass over the context) and GDN by (recurrence steps x value heads).
-    Returns (seconds, estimated seconds per round, attention seconds, GDN seconds)."""
-    import numpy as np
-
-    import oracle.tree_verify as O
-    s = cfg.shapes
-    parent, tok, greedy, a, gs = inputs
-    n = len(parent)
-    L = cfg.ctx_lens[0]
-    G = s.Hq // s.Hkv
-    d = lambda t: t.detach().double().cpu().numpy()
-    ka, na, gh, ng = attn_kv_heads, attn_nodes, gdn_heads, gdn_nodes
-    K = d(a["K"][:ka, :L]); V = d(a["V"][:ka, :L])
-    q = d(a["q"][:na, :ka * G]); kt = d(a["k_t"][:na, :ka]); vt = d(a["v_t"][:na, :ka])
-    kh = max(1, gh // (s.Hv // s.Hk))
-    gin = [(d(g["S0"][:gh]), d(g["q"][:ng, :kh]), d(g["k"][:ng, :kh]), d(g["v"][:ng, :gh]),
-            d(g["alpha"][:ng, :gh]), d(g["beta"][:ng, :gh])) for g in gs]
-    t0 = time.perf_counter()
-    O.attn_tree_verify(K, V, L, q, kt, vt, parent[:na], 1.0 / math.sqrt(s.D))
-    t1 = time.perf_counter()
-    path, alen, bonus = O.accept_path(parent, tok, greedy)
-    Kc, Vc = np.zeros((ka, L + 16, s.D)), np.zeros((ka, L + 16, s.D))
-    O.commit_attn(Kc, Vc, L, d(a["k_t"][:, :ka]), d(a["v_t"][:, :ka]), path)
-    sub_path = [x for x in path if x < ng]
-    for (S0, qg, kg, vg, al, be) in gin:
-        O.gdn_tree_verify(S0, qg, kg, vg, al, be, parent[:ng], 1.0 / math.sqrt(s.dk))
-        O.commit_gdn(S0, kg, vg, al, be, sub_path)
-    t2 = time.perf_counter()
-    dep = O.depths(parent)
-    steps_s = sum(x + 1 for x in dep[:ng]) + len(sub_path)
-    steps_f = sum(x + 1 for x in dep) + len(path)
-    n_attn = len(cfg.attn_layers)
-    n_gdn = cfg.n_layers - n_attn
-    est_attn = (t1 - t0) * (n * s.Hq) / (na * ka * G) * n_attn
-    est_gdn = (t2 - t1) * (steps_f * s.Hv) / (steps_s * gh) * (n_gdn / len(gs))
-    return t2 - t0, est_attn + est_gdn, t1 - t0, t2 - t1
-
-
-def blas_threads():
+def num_sms_or_default() -> int:
     try:
-        from threadpoolctl import threadpool_info
-        n = [i.get("num_threads") for i in threadpool_info() if i.get("user_api") == "blas"]
-        if n:
-            return int(max(n))
+        if torch.cuda.is_available():
+            return torch.cuda.get_device_properties(torch.cuda.current_device()).multi_processor_count
     except Exception:
         pass
-    return os.cpu_count() or 1
+    return 152  # GB300
+
+
+def workload_config(cfg, n_nodes, acc_lens, split, world, kv_desc, kv_window, layers_run=None):
+    c = {"workload": cfg.name, "layers": cfg.n_layers, "attention_layers": len(cfg.attn_layers),
+         "gdn_layers": cfg.n_layers - len(cfg.attn_layers), "ctx_lens": cfg.ctx_lens, "tree_nodes": n_nodes,
+         "accepted": acc_lens, "Hq_Hkv_D": [cfg.shapes.Hq, cfg.shapes.Hkv, cfg.shapes.D],
+         "Hk_Hv_dk_dv": [cfg.shapes.Hk, cfg.shapes.Hv, cfg.shapes.dk, cfg.shapes.dv], "split": split,
+         "timing": "CUDA-graph replay of whole rounds, CUDA events",
+         "l2": "no flush: every round streams inputs far larger than L2 (KV context per round)",
+         "parallelism": f"replicas x{world}", "kv": kv_desc, "kv_window": kv_window}
+    if layers_run is not None:
+        c["layers_run"] = layers_run
+    return c
+
+
+# ---------------------------------------------------------------------------
+# oracle sample (CPU baseline and reference arm)
+# ---------------------------------------------------------------------------
+# One step of the oracle is a fixed sample of one round, for every sequence of
+# the workload: the first attention layer restricted to KV head 0 (its query
+# heads, all tree nodes, the full context), the first GDN layer restricted to
+# key head 0 (its value heads, all tree nodes), the accept walk, and the commit
+# of that KV head's path rows and those value heads' states.  One round holds
+# n_attn x Hkv such attention pieces and n_gdn x Hk such GDN pieces; the round
+# estimate is the sum of each piece's time times its count.
+def sample_counts(cfg):
+    s = cfg.shapes
+    n_attn = len(cfg.attn_layers)
+    n_gdn = cfg.n_layers - n_attn
+    return {"attention": n_attn * s.Hkv, "gdn": n_gdn * s.Hk, "accept": 1, "commit_attention": n_attn * s.Hkv,
+            "commit_gdn": n_gdn * s.Hk}
+
+
+def sample_text(cfg):
+    s = cfg.shapes
+    c = sample_counts(cfg)
+    a0 = cfg.attn_layers[0] if cfg.attn_layers else None
+    g0 = next((i for i in range(cfg.n_layers) if not cfg.is_attn(i)), None)
+    return (f"fp64 numpy oracle; one step = for each of the {cfg.n_seq} sequence(s): attention layer {a0} "
+            f"restricted to KV head 0 ({s.Hq // s.Hkv} query heads, every tree node, the full context), GDN layer "
+            f"{g0} restricted to key head 0 ({s.Hv // s.Hk} value heads, every tree node), the accept walk, and "
+            f"the commit of that head's path rows and those heads' states; one round = {c['attention']} such "
+            f"attention pieces + {c['gdn']} GDN pieces (+ the commits alike), so the round estimate scales each "
+            f"piece's measured time by its count")
+
+
+def oracle_sample_inputs(cfg):
+    """The sample's inputs (fp64 numpy, generated on the host), per sequence."""
+    from speculative_tree_verify_masked_gb300 import synth
+    s = cfg.shapes
+    G, grp = s.Hq // s.Hkv, s.Hv // s.Hk
+    a0 = cfg.attn_layers[0] if cfg.attn_layers else None
+    g0 = next((i for i in range(cfg.n_layers) if not cfg.is_attn(i)), None)
+    d = lambda t: t.detach().double().cpu().numpy()
+    out = []
+    for q in range(cfg.n_seq):
+        parent, tok, greedy, _ = synth.tree_and_tokens(cfg, q)
+        n, L = len(parent), cfg.ctx_lens[q]
+        item = {"parent": parent, "tok": tok, "greedy": greedy, "L": L}
+        if a0 is not None:
+            a = synth.attn_layer_inputs(cfg, a0, q, n, L + 16, "cpu")
+            item["attn"] = (d(a["K"][:1]), d(a["V"][:1]), d(a["q"][:, :G]), d(a["k_t"][:, :1]), d(a["v_t"][:, :1]))
+        if g0 is not None:
+            g = synth.gdn_layer_inputs(cfg, g0, q, n, "cpu")
+            item["gdn"] = (d(g["S0"][:grp]), d(g["q"][:, :1]), d(g["k"][:, :1]), d(g["v"][:, :grp]),
+                           d(g["alpha"][:, :grp]), d(g["beta"][:, :grp]))
+        out.append(item)
+    return out
+
+
+def run_oracle_sample(cfg, inputs):
+    """One step of the sample; returns the wall seconds of each piece."""
+    import oracle.tree_verify as O
+    s = cfg.shapes
+    t = {"attention": 0.0, "gdn": 0.0, "accept": 0.0, "commit_attention": 0.0, "commit_gdn": 0.0}
+    for item in inputs:
+        parent, L = item["parent"], item["L"]
+        c0 = time.perf_counter()
+        if "attn" in item:
+            K, V, q, kt, vt = item["attn"]
+            O.attn_tree_verify(K, V, L, q, kt, vt, parent, 1.0 / math.sqrt(s.D))
+        c1 = time.perf_counter()
+        if "gdn" in item:
+            S0, q, k, v, al, be = item["gdn"]
+            O.gdn_tree_verify(S0, q, k, v, al, be, parent, 1.0 / math.sqrt(s.dk))
+        c2 = time.perf_counter()
+        path, _, _ = O.accept_path(parent, item["tok"], item["greedy"])
+        c3 = time.perf_counter()
+        if "attn" in item:
+            K, V, _, kt, vt = item["attn"]
+            O.commit_attn(K, V, L, kt, vt, path)
+        c4 = time.perf_counter()
+        if "gdn" in item:
+            S0, _, k, v, al, be = item["gdn"]
+            O.commit_gdn(S0, k, v, al, be, path)
+        c5 = time.perf_counter()
+        t["attention"] += c1 - c0
+        t["gdn"] += c2 - c1
+        t["accept"] += c3 - c2
+        t["commit_attention"] += c4 - c3
+        t["commit_gdn"] += c5 - c4
+    return t
+
+
+def round_estimate_s(cfg, pieces):
+    counts = sample_counts(cfg)
+    return sum(pieces[k] * counts[k] for k in counts)
+
+
+def host_cores() -> int:
+    try:
+        return len(os.sched_getaffinity(0))
+    except Exception:
+        return os.cpu_count() or 1
+
+
+def cpu_model() -> str:
+    try:
+        out = subprocess.run(["lscpu"], capture_output=True, text=True, timeout=10).stdout
+        for line in out.splitlines():
+            if line.lower().startswith("model name"):
+                return line.split(":", 1)[1].strip()
+    except Exception:
+        pass
+    try:
+        with open("/proc/cpuinfo") as f:
+            for line in f:
+                if line.lower().startswith("model name"):
+                    return line.split(":", 1)[1].strip()
+    except Exception:
+        pass
+    import platform
+    return platform.machine()
+
+
+ONE_THREAD_ENV = {"OMP_NUM_THREADS": "1", "OPENBLAS_NUM_THREADS": "1", "MKL_NUM_THREADS": "1",
+                  "BLIS_NUM_THREADS": "1", "VECLIB_MAXIMUM_THREADS": "1", "NUMEXPR_NUM_THREADS": "1"}
+
+
+def one_thread_sample(cfg_id: int, runs: int):
+    """The sample timed in a fresh process whose BLAS and OpenMP pools have
+    one thread (the pools are sized when numpy loads); returns the median
+    piece times or None."""
+    env = dict(os.environ, **ONE_THREAD_ENV)
+    try:
+        out = subprocess.run([sys.executable, os.path.abspath(__file__), "--oracle-sample-worker", "--config",
+                              str(cfg_id), "--steps", str(runs)], capture_output=True, text=True, env=env,
+                             timeout=900)
+        return json.loads(out.stdout.strip().splitlines()[-1])["pieces_s"]
+    except Exception:
+        return None
+
+
+def median_pieces(runs):
+    return {k: statistics.median(r[k] for r in runs) for k in runs[0]}
+
+
+def oracle_worker(args):
+    """--oracle-sample-worker: time the sample `--steps` times in this process, print JSON."""
+    from speculative_tree_verify_masked_gb300 import synth
+    cfg = synth.workload(args.config)
+    inp = oracle_sample_inputs(cfg)
+    runs = [run_oracle_sample(cfg, inp) for _ in range(max(1, args.steps))]
+    print(json.dumps({"pieces_s": median_pieces(runs)}), flush=True)
 
 
 # ---------------------------------------------------------------------------
@@ -253,7 +356,7 @@ def run_ours(args, rank, world, local_rank):
     cfg = synth.workload(args.config)
     pool = B.KVPool(local_rank) if args.kv_pool else None
     extra = {} if args.kv_window is None else {"cap_extra": args.kv_window - max(cfg.ctx_lens)}
-    r = VerifyRound(cfg, device=dev, split=args.split, kv_pool=pool, **extra)
+    r = VerifyRound(cfg, device=dev, split=args.split, kv_pool=pool, layers=args.layers_list, **extra)
     n_nodes = r.n_nodes
     acc_lens = [len(p) for p in r.expected_paths]
     nodes_per_round = sum(n_nodes)
@@ -288,17 +391,22 @@ def run_ours(args, rank, world, local_rank):
     # around each attention layer in a second graph of the same round (event
     # nodes would cut the programmatic launch edges of the timed graph),
     # replayed right after the timed region
-    attn_ms = None
-    if r.attn:
-        marked = r.capture(attn_marks=True)
-        ms_l = []
+    attn_ms = gdn_ms = None
+    if r.attn or r.gdn:
+        marked = r.capture(layer_marks=True)
+        ms_a, ms_g = [], []
         for _ in range(max(3, min(args.steps, 20))):
             marked.replay()
             torch.cuda.synchronize()
-            ms_l.append(statistics.mean(r.attn_marks_ms()))
-        attn_ms = statistics.median(ms_l)
+            if r.attn:
+                ms_a.append(statistics.mean(r.attn_marks_ms()))
+            if r.gdn:
+                ms_g.append(statistics.mean(r.gdn_marks_ms()))
+        attn_ms = statistics.median(ms_a) if ms_a else None
+        gdn_ms = statistics.median(ms_g) if ms_g else None
         assert r.status() == 0, f"device status {r.status()}"
-    attn_timing = ("CUDA events around each attention layer, captured in a graph of the same round and "
+        del marked
+    attn_timing = ("CUDA events around each layer's verify call, captured in a graph of the same round and "
                    "replayed after the timed region (median over replays of the mean over layers)")
 
     # --- eager rounds (launch overhead included), for context ---------------
@@ -316,25 +424,20 @@ def run_ours(args, rank, world, local_rank):
 
 
     # --- end to end through the C ABI with host buffers ---------------------
+    # Every input a host hands a round sits in one pinned host buffer and goes
+    # in with one copy; the accepted paths, lengths and bonus tokens come back
+    # with one copy.
     e2e = None
     if not args.no_e2e:
-        dev_in = [r.tree.parent, r.tree.node_off, r.tok, r.greedy]
-        for a in r.attn.values():
-            dev_in += [a["q"], a["k_t"], a["v_t"]]
-        for g in r.gdn.values():
-            dev_in += [g["q"], g["k"], g["v"], g["alpha"], g["beta"]]
-        host_in = [t.cpu().pin_memory() for t in dev_in]
-        dev_out = [r.path, r.acc_len, r.bonus]
-        host_out = [torch.empty(t.shape, dtype=t.dtype, pin_memory=True) for t in dev_out]
-        h2d = sum(t.numel() * t.element_size() for t in host_in)
-        d2h = sum(t.numel() * t.element_size() for t in host_out)
+        io_in, io_out = r.pack_io()
+        host_in = torch.empty(io_in.shape, dtype=torch.uint8, pin_memory=True)
+        host_in.copy_(io_in)
+        host_out = torch.empty(io_out.shape, dtype=torch.uint8, pin_memory=True)
 
         def e2e_step():
-            for d_, h_ in zip(dev_in, host_in):
-                d_.copy_(h_, non_blocking=True)
+            io_in.copy_(host_in, non_blocking=True)
             r.run()
-            for d_, h_ in zip(dev_out, host_out):
-                h_.copy_(d_, non_blocking=True)
+            host_out.copy_(io_out, non_blocking=True)
             stream.synchronize()
 
         for _ in range(3):
@@ -350,33 +453,28 @@ def run_ours(args, rank, world, local_rank):
         e2e_ms = max_over_ranks((time.perf_counter() - t0) * 1e3 / n_e2e, world, dev)
         assert r.status() == 0
         e2e = {"value": round(job_throughput(nodes_per_round, world, e2e_ms), 1), "unit": UNIT,
-               "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "ms_per_step": round(e2e_ms, 4),
-               "steps": n_e2e, "path": "eager C-ABI calls (ctypes), pinned host inputs in, accepted path out"}
+               "h2d_bytes_per_step": int(io_in.numel()), "d2h_bytes_per_step": int(io_out.numel()),
+               "h2d_copies_per_step": 1, "d2h_copies_per_step": 1, "ms_per_step": round(e2e_ms, 4),
+               "steps": n_e2e,
+               "path": "eager C-ABI calls (ctypes); the round's host inputs (trees, tokens, every layer's node "
+                       "inputs) in from one pinned buffer, the accepted paths, lengths and bonus tokens out"}
 
-    # --- CPU baseline: the oracle on a bounded sample (rank 0, N = 1) --------
+    # --- CPU baseline: the oracle on its stated sample (rank 0, N = 1) -------
     cpu = None
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
-        inp = oracle_sample_inputs(cfg, dev)
-        s = cfg.shapes
-        # calibrate on the smallest sample, then size it for about 12 s of CPU work
-        grp = max(1, s.Hv // s.Hk)  # value heads per key head: whole groups only
-        _, _, ta, tg = time_oracle(cfg, inp, 1, n_nodes[0], grp, n_nodes[0])
-        ka = int(min(s.Hkv, max(1, 6.0 // max(ta, 1e-3))))
-        gh = int(min(s.Hv, max(grp, (6.0 / max(tg, 1e-3)) * grp))) // grp * grp
-        secs, ests = 0.0, []
-        while secs < 10.0 and len(ests) < 5:  # at least 10 s of CPU work in all
-            t, e, _, _ = time_oracle(cfg, inp, ka, n_nodes[0], gh, n_nodes[0])
-            secs += t
-            ests.append(e)
-        est = statistics.median(ests)
-        cpu = {"value": round(nodes_per_round / est, 3) if cfg.n_seq == 1 else None, "unit": UNIT,
-               "cores": blas_threads(), "kind": "oracle",
-               "sample": (f"fp64 numpy oracle on sequence 0: one attention layer restricted to {ka} of {s.Hkv} KV "
-                          f"heads (all {n_nodes[0]} nodes, full context) and {min(3, cfg.n_layers - 1)} GDN layers "
-                          f"restricted to {gh} of {s.Hv} value heads, plus accept and commit, run {len(ests)} times; "
-                          f"{secs:.1f} s of CPU work in all, scaled by heads and layers to one "
-                          f"{cfg.n_layers}-layer round (median {est:.1f} s estimated per round)"),
-               "est_round_s": round(est, 2)}
+        inp = oracle_sample_inputs(cfg)
+        runs = [run_oracle_sample(cfg, inp) for _ in range(3)]
+        pieces = median_pieces(runs)
+        est = round_estimate_s(cfg, pieces)
+        one = one_thread_sample(args.config, 1)
+        est1 = round_estimate_s(cfg, one) if one else None
+        cpu = {"value": round(nodes_per_round / est, 4), "unit": UNIT, "cores": host_cores(), "kind": "oracle",
+               "sample": sample_text(cfg), "cpu_model": cpu_model(), "nproc": os.cpu_count(),
+               "runs": len(runs), "sample_s": round(sum(pieces.values()), 3),
+               "pieces_s": {k: round(v, 4) for k, v in pieces.items()}, "round_estimate_s": round(est, 2),
+               "one_thread": ({"value": round(nodes_per_round / est1, 4), "cores": 1,
+                               "pieces_s": {k: round(v, 4) for k, v in one.items()},
+                               "round_estimate_s": round(est1, 2)} if one else None)}
 
     hbm_peak, peak_kind = peaks()
     round_gbs = bytes_round / (ms / 1e3) / 1e9
@@ -391,29 +489,35 @@ def run_ours(args, rank, world, local_rank):
                 "timing": attn_timing,
                 "algorithmic_bytes_per_launch": ab, "ms_per_launch": round(attn_ms, 4),
                 "peak_kind": peak_kind}
+    roof_round = {"bound": "hbm", "achieved": round(round_gbs, 1), "peak": hbm_peak, "unit": "GB/s",
+                  "frac": round(round_gbs / hbm_peak, 4), "traffic": None,
+                  "kernel": "one whole verify round (prepare, every layer's verify, accept, commit)",
+                  "timing": "the timed region: CUDA-graph replays of whole rounds",
+                  "algorithmic_bytes_per_launch": bytes_round, "ms_per_launch": round(ms, 5),
+                  "peak_kind": peak_kind}
     n_attn = len(r.attn)
     n_gdn = len(r.gdn)
     launches_per_round = 1 + 2 * n_attn + n_gdn + 1 + (1 + math.ceil(n_attn / 16) + math.ceil(n_gdn / 32) + 1)
+    kv_desc = ("pool: address space reserved for the whole cache, 2 MiB pages committed for rows below "
+               f"L + {r.kv_margin}" if pool else "static buffers")
     line = {
         "metric": METRIC, "value": round(job_throughput(nodes_per_round, world, ms), 1), "unit": UNIT, "n_gpus": world,
         "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(ms, 5), "higher_is_better": True,
         "scaling": "weak", "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
-        "config": {"workload": cfg.name, "layers": cfg.n_layers, "attention_layers": n_attn, "gdn_layers": n_gdn,
-                   "ctx_lens": cfg.ctx_lens, "tree_nodes": n_nodes, "accepted": acc_lens,
-                   "Hq_Hkv_D": [cfg.shapes.Hq, cfg.shapes.Hkv, cfg.shapes.D],
-                   "Hk_Hv_dk_dv": [cfg.shapes.Hk, cfg.shapes.Hv, cfg.shapes.dk, cfg.shapes.dv],
-                   "split": r.split, "timing": "CUDA-graph replay of whole rounds, CUDA events",
-                   "l2": "no flush: every round streams inputs far larger than L2 (KV context per round)",
-                   "parallelism": f"replicas x{world}",
-                   "kv": ("pool: address space reserved for the whole cache, 2 MiB pages committed for rows below "
-                          f"L + {r.kv_margin}" if pool else "static buffers"), "kv_window": r.cap},
+        "config": workload_config(cfg, n_nodes, acc_lens, r.split, world, kv_desc, r.cap,
+                                  layers_run=args.layers_list),
         "us_per_round": round(ms * 1e3, 2),
         **({"kv_pool": {"committed_bytes": pool.committed_bytes, "reserved_bytes": pool.reserved_bytes,
                         "page_bytes": pool.page_bytes}} if pool else {}),
         "hbm": {"algorithmic_bytes_per_round": bytes_round, "achieved_gbs": round(round_gbs, 1),
                 "frac_of_measured": round(round_gbs / hbm_peak, 4), "frac_of_8tbs": round(round_gbs / SPEC_HBM_GBS, 4)},
         "eager_ms_per_step": round(eager_ms, 4),
-        "roofline": roof, "cpu_baseline": cpu, "e2e": e2e, "clocks": clk,
+        "layer_us": {"attention_verify": round(attn_ms * 1e3, 2) if attn_ms is not None else None,
+                     "gdn_verify": round(gdn_ms * 1e3, 2) if gdn_ms is not None else None,
+                     "how": "CUDA events around each layer's verify call in a marked copy of the round's graph "
+                            "(median over replays of the mean over layers of that kind; the marks cut the "
+                            "programmatic launch overlap between neighbouring layers)"},
+        "roofline": roof, "roofline_round": roof_round, "cpu_baseline": cpu, "e2e": e2e, "clocks": clk,
         "gpu_launches": launches_per_round * args.steps,
     }
     if rank == 0:
@@ -424,42 +528,41 @@ def run_ours(args, rank, world, local_rank):
 # reference arm: the CPU oracle
 # ---------------------------------------------------------------------------
 def run_reference(args, rank, world):
+    """The oracle, as it stands, on the host cores: W untimed and K timed
+    steps of the sample (rank 0 only).  ms_per_step is the measured time of
+    one step of the sample; value is the round throughput that sample
+    implies."""
     if rank != 0:
         return
     from speculative_tree_verify_masked_gb300 import synth
+    from speculative_tree_verify_masked_gb300.round import auto_split
     cfg = synth.workload(args.config)
-    s = cfg.shapes
-    inp = oracle_sample_inputs(cfg, "cpu")
-    n_nodes = len(inp[0])
-    # calibrate the smallest sample, then size each step so the run stays near two minutes
-    time_oracle(cfg, inp, 1, 1, 1, 1)
-    secs1 = time_oracle(cfg, inp, 1, 1, 1, 1)[0]
-    budget = 120.0 / max(1, args.steps + args.warmup)
-    grow = max(1.0, budget / max(secs1, 1e-4))
-    na = max(1, min(n_nodes, int(grow)))
-    ng = max(1, min(n_nodes, int(grow)))
-    gh = max(1, min(s.Hv // s.Hk, int(grow / ng)))
+    trees = [synth.tree_and_tokens(cfg, q) for q in range(cfg.n_seq)]
+    n_nodes = [len(t[0]) for t in trees]
+    acc_lens = [len(t[3]) for t in trees]
+    split = args.split or auto_split(cfg.ctx_lens, n_nodes, cfg.shapes.Hq, cfg.shapes.Hkv, num_sms_or_default())
+    inp = oracle_sample_inputs(cfg)
     for _ in range(args.warmup):
-        time_oracle(cfg, inp, 1, na, gh, ng)
-    ests = []
+        run_oracle_sample(cfg, inp)
+    runs, walls = [], []
     t0 = time.perf_counter()
     for _ in range(args.steps):
-        est = time_oracle(cfg, inp, 1, na, gh, ng)[1]
-        ests.append(est)
+        a = time.perf_counter()
+        runs.append(run_oracle_sample(cfg, inp))
+        walls.append(time.perf_counter() - a)
     wall = time.perf_counter() - t0
-    est = statistics.median(ests)
-    value = round(n_nodes * cfg.n_seq / est, 4)
-    sample = (f"fp64 numpy oracle, per step: one attention layer restricted to 1 of {s.Hkv} KV heads and the first "
-              f"{na} of {n_nodes} tree nodes (full context), 3 GDN layers restricted to {gh} of {s.Hv} value heads "
-              f"and the first {ng} nodes, plus accept and commit; scaled by query rows and recurrence steps to one "
-              f"{cfg.n_layers}-layer round")
+    pieces = median_pieces(runs)
+    est = round_estimate_s(cfg, pieces)
+    value = round(sum(n_nodes) / est, 4)
+    kv_window = max(cfg.ctx_lens) + 64
     line = {"impl": "reference", "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world,
-            "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(est * 1e3, 2),
+            "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(statistics.median(walls) * 1e3, 2),
             "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
-            "config": {"workload": cfg.name, "layers": cfg.n_layers, "ctx_lens": cfg.ctx_lens,
-                       "tree_nodes": [n_nodes] * cfg.n_seq, "parallelism": "rank 0 only (CPU)"},
-            "cpu_baseline": {"value": value, "unit": UNIT, "cores": blas_threads(), "kind": "oracle",
-                             "sample": sample, "wall_s": round(wall, 1)},
+            "config": workload_config(cfg, n_nodes, acc_lens, split, world, "static buffers", kv_window),
+            "cpu_baseline": {"value": value, "unit": UNIT, "cores": host_cores(), "kind": "oracle",
+                             "sample": sample_text(cfg), "cpu_model": cpu_model(), "nproc": os.cpu_count(),
+                             "pieces_s": {k: round(v, 4) for k, v in pieces.items()},
+                             "round_estimate_s": round(est, 2), "wall_s": round(wall, 1)},
             "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
     print(json.dumps(line), flush=True)
 
@@ -480,7 +583,14 @@ def main():
     ap.add_argument("--kv-pool", action="store_true", help="attention caches from the KV pool (tv_kvpool_*)")
     ap.add_argument("--kv-window", type=int, default=None,
                     help="cache rows per sequence (default: the context plus 64)")
+    ap.add_argument("--layers", default=None,
+                    help="comma-separated layer indices: run only these layers of the stack (for profiling)")
+    ap.add_argument("--oracle-sample-worker", action="store_true", help=argparse.SUPPRESS)
     args = ap.parse_args()
+    args.layers_list = [int(x) for x in args.layers.split(",")] if args.layers else None
+    if args.oracle_sample_worker:
+        oracle_worker(args)
+        return
     args.warmup = max(3, args.warmup)
     world = int(os.environ.get("WORLD_SIZE", "1"))
     rank = int(os.environ.get("RANK", "0"))

@@ -39,7 +39,12 @@
  *    malformed tree, a cache that would overflow, a bounded wait that
  *    expired) write their tv_status code into the caller's device status word
  *    (first error wins) and make every later call that is given the same
- *    word a no-op.  Nothing traps.
+ *    word a no-op.  The word belongs to a launch, not to one sequence: an
+ *    error in any sequence of a joint launch stops the round for all of its
+ *    sequences (a caller that wants the others to go on gives them their own
+ *    tree descriptors and words, at the cost of one launch each).  Calls
+ *    already running when the word is set may still finish their work.
+ *    Nothing traps.
  *  - Node-indexed arrays concatenate the sequences' trees: sequence s owns
  *    global nodes node_off[s] .. node_off[s+1]-1, whose local index 0 is the
  *    root.  The root is the last committed token: it is not yet in the cache

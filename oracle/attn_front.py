@@ -9,7 +9,7 @@ __graft_entry__.smoke() and bench.py's CPU baseline may use it.
 Source (page title, section): "Adding a model", "What is still specific to
 Qwen3.8": the model's attention has "a gated output and partial rotary".  The
 pages give no formula for either, so this module writes out the plainest
-reading (each is listed in DESIGN.md):
+reading:
   * rotary: the first `rot_dims` dimensions of every query and key head turn
     as rot_dims/2 planes; plane j pairs dimension j with j + rot_dims/2 and
     turns by the angle pos * theta^(-2j/rot_dims); the other dimensions pass

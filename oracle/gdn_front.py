@@ -12,7 +12,7 @@ Source (page title, section): "Adding a model", "What is still specific to
 Qwen3.8": "the Gated DeltaNet layer with its gated norm"; "The model layer":
 per-sequence state is the recurrent state plus the `gdn.conv` tails.  The
 pages give no formula for any of these steps, so this module writes out the
-plainest reading (each is listed in the design doc):
+plainest reading:
   * channels: the layer's raw query, key and value projections side by side,
     C = 2 * Hk * dk + Hv * dv channels per token;
   * short convolution: depthwise, causal, width W: the output of a token at

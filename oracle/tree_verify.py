@@ -23,7 +23,7 @@ Sources (page title, section):
     + b_t v_t k_t^T, and the ancestor-bitmask tree mask are taken as the
     method's definition (they are not printed on the pages).
 
-Readings where the pages are silent (each is listed in the design doc):
+Readings where the pages are silent:
   * node 0 is the root = the last committed token, not yet in the cache or in
     the state; a node at depth d sees the L context rows plus its d+1
     ancestors-or-self, placed at logical positions L..L+d;

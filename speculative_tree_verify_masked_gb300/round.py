@@ -74,7 +74,7 @@ class VerifyRound:
             split = auto_split(cfg.ctx_lens, self.n_nodes, s.Hq, s.Hkv, sms)
         self.split = split
         self.plan = B.plan(split)
-        self._attn_marks = None  # events around attention layers while capturing
+        self._marks = None  # (layer, start, end) events around layers while capturing
         self._graph_marks = None
         # With a KV pool the caches are reserved whole and only the rows below
         # the context length plus kv_margin are committed; the committed rows
@@ -110,6 +110,9 @@ class VerifyRound:
         self.path = torch.full((cfg.n_seq, B.TV_MAX_PATH), -1, dtype=torch.int32, device=device)
         self.acc_len = torch.zeros(cfg.n_seq, dtype=torch.int32, device=device)
         self.bonus = torch.zeros(cfg.n_seq, dtype=torch.int32, device=device)
+        self._build_commit_args()
+
+    def _build_commit_args(self):
         al = [li for li in self.layers if li in self.attn]
         gl = [li for li in self.layers if li in self.gdn]
         self.commit_args = B.CommitArgs(
@@ -117,6 +120,58 @@ class VerifyRound:
             [self.attn[li]["v_t"] for li in al], [self.gdn[li]["layer"] for li in gl],
             [self.gdn[li]["k"] for li in gl], [self.gdn[li]["v"] for li in gl],
             [self.gdn[li]["alpha"] for li in gl], [self.gdn[li]["beta"] for li in gl])
+
+    def pack_io(self):
+        """Place every input a host hands a round (the trees' node offsets
+        and parent arrays, the drafted and greedy tokens, every layer's node
+        inputs) in one device byte buffer, and the results it reads back
+        (accepted paths, lengths, bonus tokens) in another, each tensor at a
+        256-byte aligned offset with its values kept; the round's tensors
+        become views of the two buffers.  A host then feeds a round with one
+        copy in and reads it with one copy out.  Returns (inputs, outputs)."""
+        ins = [("tree", "node_off"), ("tree", "parent"), ("r", "tok"), ("r", "greedy")]
+        for li in self.layers:
+            names = ("q", "k_t", "v_t") if li in self.attn else ("q", "k", "v", "alpha", "beta")
+            ins += [(li, n) for n in names]
+
+        def get(key):
+            owner, name = key
+            if owner == "tree":
+                return getattr(self.tree, name)
+            if owner == "r":
+                return getattr(self, name)
+            return (self.attn.get(owner) or self.gdn[owner])[name]
+
+        def put(key, t):
+            owner, name = key
+            if owner == "tree":
+                setattr(self.tree, name, t)
+            elif owner == "r":
+                setattr(self, name, t)
+            else:
+                (self.attn.get(owner) or self.gdn[owner])[name] = t
+
+        def pack(keys):
+            offs, total = [], 0
+            for key in keys:
+                t = get(key)
+                offs.append(total)
+                total += (t.numel() * t.element_size() + 255) // 256 * 256
+            buf = torch.empty(max(total, 256), dtype=torch.uint8, device=self.device)
+            for key, o in zip(keys, offs):
+                t = get(key)
+                nb = t.numel() * t.element_size()
+                v = buf[o:o + nb].view(t.dtype).view(t.shape)
+                v.copy_(t)
+                put(key, v)
+            return buf
+
+        self.io_in = pack(ins)
+        self.io_out = pack([("r", "path"), ("r", "acc_len"), ("r", "bonus")])
+        self.tree.c.node_off = self.tree.node_off.data_ptr()
+        self.tree.c.parent = self.tree.parent.data_ptr()
+        self._build_commit_args()
+        return self.io_in, self.io_out
 
     def _alloc_ws(self):
         ws_bytes = 0
@@ -164,7 +219,7 @@ class VerifyRound:
     def verify(self, stream=None):
         self.prepare(stream)
         for li in self.layers:
-            marks = self._attn_marks is not None and li in self.attn
+            marks = self._marks is not None
             if marks:
                 # external events become timing-capable record nodes of the graph
                 a = torch.cuda.Event(enable_timing=True, external=True)
@@ -173,7 +228,7 @@ class VerifyRound:
             self.verify_layer(li, stream)
             if marks:
                 b.record()
-                self._attn_marks.append((a, b))
+                self._marks.append((li, a, b))
 
     def accept(self, stream=None):
         B.tv_accept_path(self.tree, self.tok, self.greedy, self.path, self.acc_len, self.bonus, stream)
@@ -194,11 +249,13 @@ class VerifyRound:
     def status(self) -> int:
         return self.tree.status_code()
 
-    def capture(self, attn_marks: bool = False):
+    def capture(self, layer_marks: bool = False):
         """Capture run() in a CUDA graph on a side stream; returns the graph.
-        With attn_marks, CUDA events recorded around every attention layer
-        become part of the graph; after a replay, attn_marks_ms() gives each
-        layer's time in that replay."""
+        With layer_marks, CUDA events recorded around every layer's verify
+        call become part of the graph; after a replay, attn_marks_ms() and
+        gdn_marks_ms() give each layer's time in that replay.  (Event nodes
+        cut the programmatic launch edges around them, so a marked graph is
+        for breaking a round down, not for timing it.)"""
         g = torch.cuda.CUDAGraph()
         s = torch.cuda.Stream()
         s.wait_stream(torch.cuda.current_stream())
@@ -206,13 +263,17 @@ class VerifyRound:
             self.run()  # warm (attribute setup outside capture)
         torch.cuda.current_stream().wait_stream(s)
         torch.cuda.synchronize()
-        self._attn_marks = [] if attn_marks else None
+        self._marks = [] if layer_marks else None
         with torch.cuda.graph(g):
             self.run()
-        self._graph_marks, self._attn_marks = self._attn_marks, None
+        self._graph_marks, self._marks = self._marks, None
         return g
 
     def attn_marks_ms(self):
         """Per attention layer, the ms between the events around it in the
-        latest replay of the graph captured with attn_marks."""
-        return [a.elapsed_time(b) for a, b in (self._graph_marks or [])]
+        latest replay of the graph captured with layer_marks."""
+        return [a.elapsed_time(b) for li, a, b in (self._graph_marks or []) if li in self.attn]
+
+    def gdn_marks_ms(self):
+        """Per GDN layer, as attn_marks_ms."""
+        return [a.elapsed_time(b) for li, a, b in (self._graph_marks or []) if li in self.gdn]

@@ -86,3 +86,31 @@ def test_graph_replay_matches_eager():
     g.replay()
     torch.cuda.synchronize()
     assert r.status() == 0
+
+
+def test_packed_host_io_gives_the_same_round():
+    """A round whose host inputs live in one packed buffer (and whose results
+    come back in another) gives the bits of the ordinary round, also when the
+    packed inputs are refilled from a pinned host copy."""
+    cfg = synth.workload(2)
+    plain = VerifyRound(cfg)
+    plain.run()
+    torch.cuda.synchronize()
+    packed = VerifyRound(cfg)
+    io_in, io_out = packed.pack_io()
+    host_in = io_in.cpu().pin_memory()
+    io_in.zero_()
+    io_in.copy_(host_in, non_blocking=True)
+    packed.run()
+    host_out = io_out.cpu()
+    torch.cuda.synchronize()
+    assert packed.status() == 0 and plain.status() == 0
+    for li in plain.layers:
+        a = plain.attn[li]["out"] if li in plain.attn else plain.gdn[li]["out"]
+        b = packed.attn[li]["out"] if li in packed.attn else packed.gdn[li]["out"]
+        assert torch.equal(a, b), li
+    for name in ("path", "acc_len", "bonus", "len"):
+        assert torch.equal(getattr(plain, name), getattr(packed, name)), name
+    # the read-back buffer holds the accepted path first
+    n = cfg.n_seq * 16
+    assert torch.equal(host_out[:4 * n].view(torch.int32).view(cfg.n_seq, 16), plain.path.cpu())
