@@ -82,7 +82,11 @@ def round_bytes(cfg, n_nodes_per_seq, acc_lens):
 # dram__bytes_write.sum from an ncu capture of the current kernels.  A figure
 # is dropped whenever the kernels change and stays absent (reported as null)
 # until it is captured again.
-MEASURED_TRAFFIC: dict[str, int] = {}
+MEASURED_TRAFFIC: dict[str, int] = {
+    # one attention layer of the stack (bench.py --layers 3): split 538,482,176 read + 2,969,344 written,
+    # tail 15,775,488 read; the same kernels and launch as every attention layer of the full round
+    "64-layer mixer stack (48 GDN + 16 attention), L 131072, 32-node tree": 538482176 + 2969344 + 15775488,
+}
 
 
 # ---------------------------------------------------------------------------
@@ -497,7 +501,7 @@ def run_ours(args, rank, world, local_rank):
                   "peak_kind": peak_kind}
     n_attn = len(r.attn)
     n_gdn = len(r.gdn)
-    launches_per_round = 1 + 2 * n_attn + n_gdn + 1 + (1 + math.ceil(n_attn / 16) + math.ceil(n_gdn / 32) + 1)
+    launches_per_round = 1 + 2 * n_attn + n_gdn + 1 + (1 + math.ceil(n_attn / 16) + math.ceil(n_gdn / 64) + 1)
     kv_desc = ("pool: address space reserved for the whole cache, 2 MiB pages committed for rows below "
                f"L + {r.kv_margin}" if pool else "static buffers")
     line = {

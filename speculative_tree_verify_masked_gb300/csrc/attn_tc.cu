@@ -578,6 +578,9 @@ __global__ void __launch_bounds__(384, 1) attn_split_kernel(const __grid_constan
     if (!ok && lane == 0) set_status(p.status, TV_ERR_TIMEOUT);
   } else if (!skip && warp >= 2 && warp <= 9) {
     // ---------------- softmax / epilogue: warps 2-9, two warpgroups, one half tile each ----------------
+    // Their waits are warp-wide (every lane gets the same outcome), so a wait
+    // that gives up takes the whole warp out of the loop and no tcgen05.ld or
+    // .st below ever runs with part of a warp.
     const uint32_t tl = tbase + (static_cast<uint32_t>(quad * 32) << 16);
     uint32_t t = 0;  // CTA-wide tile counter
     bool ok = true;
@@ -594,7 +597,7 @@ __global__ void __launch_bounds__(384, 1) attn_split_kernel(const __grid_constan
       float m = -INFINITY, lh = 0.f;
       for (int k = 0; k < n; k++) {
         const int b = t & 1;
-        if (!wait_role(SFULL0 + 8u * b, (t >> 1) & 1, abort_flag, kWaitCycles)) {
+        if (!wait_warp(SFULL0 + 8u * b, (t >> 1) & 1, abort_flag, kWaitCycles)) {
           ok = false;
           break;
         }
@@ -606,7 +609,7 @@ __global__ void __launch_bounds__(384, 1) attn_split_kernel(const __grid_constan
         const float mh = half_max(sv, kHalf);
         xmax[b][hf][lrow] = mh;
         mbar_arrive(XBAR0 + 8u * b);
-        if (!wait_role(XBAR0 + 8u * b, (t >> 1) & 1, abort_flag, kWaitCycles)) {
+        if (!wait_warp(XBAR0 + 8u * b, (t >> 1) & 1, abort_flag, kWaitCycles)) {
           ok = false;
           break;
         }
@@ -619,14 +622,14 @@ __global__ void __launch_bounds__(384, 1) attn_split_kernel(const __grid_constan
         m = m_new;
         const int ps = t % C::NP;
         if (t >= static_cast<uint32_t>(C::NP) &&
-            !wait_role(ODONE0 + 8u * ps, ((t - C::NP) / C::NP) & 1, abort_flag, kWaitCycles)) {  // slot's previous PV done
+            !wait_warp(ODONE0 + 8u * ps, ((t - C::NP) / C::NP) & 1, abort_flag, kWaitCycles)) {  // slot's previous PV done
           ok = false;
           break;
         }
         store_p_half(pring + ps * C::PTILE, lrow, hf, P);
         if (k > 0 && __any_sync(0xffffffffu, alpha != 1.f)) {
           const uint32_t tp = t - 1;  // PV of the previous tile must be complete
-          if (!wait_role(ODONE0 + 8u * (tp % C::NP), (tp / C::NP) & 1, abort_flag, kWaitCycles)) {
+          if (!wait_warp(ODONE0 + 8u * (tp % C::NP), (tp / C::NP) & 1, abort_flag, kWaitCycles)) {
             ok = false;
             break;
           }
@@ -642,7 +645,7 @@ __global__ void __launch_bounds__(384, 1) attn_split_kernel(const __grid_constan
       if (!ok) break;
       {
         const uint32_t tp = t - 1;  // the item's last PV
-        if (!wait_role(ODONE0 + 8u * (tp % C::NP), (tp / C::NP) & 1, abort_flag, kWaitCycles)) {
+        if (!wait_warp(ODONE0 + 8u * (tp % C::NP), (tp / C::NP) & 1, abort_flag, kWaitCycles)) {
           ok = false;
           break;
         }

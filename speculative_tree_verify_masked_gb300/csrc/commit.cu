@@ -13,8 +13,12 @@
 
 namespace tv {
 
-constexpr int kAttnCommitLayers = 16;  // layers per launch (kernel parameter space)
-constexpr int kGdnCommitLayers = 32;
+// Layers per launch.  The per-layer pointer blocks travel as kernel
+// parameters (up to 32 KB of them on this toolkit and architecture): 64 GDN
+// layers take 6.2 KB, so a 48-layer stack commits in one launch instead of
+// two that each leave the GPU half busy at their end.
+constexpr int kAttnCommitLayers = 16;
+constexpr int kGdnCommitLayers = 64;
 
 // Capacity and path-length checks for every sequence, before anything is written.
 __global__ void commit_check_kernel(const int32_t* acc_len, const int32_t* len, int32_t* status, int n_seq,
