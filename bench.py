@@ -83,9 +83,6 @@ def round_bytes(cfg, n_nodes_per_seq, acc_lens):
 # is dropped whenever the kernels change and stays absent (reported as null)
 # until it is captured again.
 MEASURED_TRAFFIC: dict[str, int] = {
-    # one attention layer of the stack (bench.py --layers 3): split 538,482,176 read + 2,969,344 written,
-    # tail 15,775,488 read; the same kernels and launch as every attention layer of the full round
-    "64-layer mixer stack (48 GDN + 16 attention), L 131072, 32-node tree": 538482176 + 2969344 + 15775488,
 }
 
 

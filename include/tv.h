@@ -113,21 +113,21 @@ typedef struct {
 
 /* TV_TREE_OVERLAP: the calls that take this tree launch their kernels with
  * programmatic dependent launch, so that a kernel can start (shared- and
- * tensor-memory setup, loads of the recurrent state) while the kernel before
- * it on the stream finishes; the next
- * kernel is let in only after a kernel's own wait for its predecessor has
- * returned (right after that wait in the attention split kernel and GDN
- * verify, at exit elsewhere),
- * so everything older than the predecessor has completed.  Before waiting, a
- * kernel reads only the recurrent states (GDN verify; GDN commit, whose
- * predecessor is always a kernel of the same commit call), the lengths and
- * node_off (attention; the split kernel also prefetches K/V tiles into L2,
- * which is only a cache hint), and the tree tables, the query rows, the
- * tree's K/V rows and the cache rows of its own tile (the attention tail,
- * whose predecessor is always its own split kernel); no kernel of a verify round
- * (prepare, per-layer verify, accept, commit, in that order on one stream)
- * writes these directly before such a read.  The caller must not enqueue its
- * own kernel that writes them directly before a call with this flag. */
+ * tensor-memory setup, loads of the recurrent state, work that needs nothing
+ * from its predecessor) while the kernel before it on the stream finishes.
+ * A kernel lets the next one in right after its own wait for its
+ * predecessor has returned (the attention split kernel and GDN verify), or
+ * at exit, so everything older than the predecessor has completed.  Before
+ * waiting, a kernel reads only the recurrent states (GDN verify; GDN commit,
+ * whose predecessor is always a kernel of the same commit call), the lengths
+ * and node_off (attention; the split kernel also prefetches K/V tiles into
+ * L2, which is only a cache hint), and the tree tables, the query rows, the
+ * tree's K/V rows and the cache rows of its own segment (the attention tail,
+ * whose predecessor is always its own split kernel, and which computes the
+ * node's own segment before waiting); no kernel of a verify round (prepare,
+ * per-layer verify, accept, commit, in that order on one stream) writes
+ * these directly before such a read.  The caller must not enqueue its own
+ * kernel that writes them directly before a call with this flag. */
 #define TV_TREE_OVERLAP 1
 /* Every call that takes a tv_tree returns TV_ERR_ARG, enqueueing nothing, when
  * the descriptor is ill formed on the host: NULL, counts out of range, or a
@@ -457,8 +457,8 @@ tv_status tv_kvpool_destroy(tv_kv_pool* pool);
 /* ------------------------------------------------------------------------
  * Diagnostics
  * ------------------------------------------------------------------------
- * Every wait inside the pipelined kernels (the attention split and tail
- * kernels) is bounded: after a limit it raises a give-up flag the other
+ * Every wait inside the pipelined kernel (the attention split kernel) is
+ * bounded: after a limit it raises a give-up flag the other
  * roles see, lets its own copies land, and the kernel writes TV_ERR_TIMEOUT
  * into the status word instead of hanging.  This call runs those same wait
  * routines against barriers that nothing arrives at, with a caller-chosen

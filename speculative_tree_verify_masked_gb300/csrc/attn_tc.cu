@@ -2,26 +2,30 @@
 // cores ("One request, end to end" 2.6: one forward pass verifies the whole
 // tree; "Adding a model" step 4: every verified row equals the decode row).
 //
-// Row function.  Row (node, query head) sees logical positions 0 .. L+d: the
-// L cache rows, then its ancestors-or-self at L .. L+d.  Positions are cut
-// into tiles of 64 and splits of plan.split positions, both aligned at
-// absolute position 0.  Within a split the tiles run in order through one
-// online softmax: S = Q K^T on the tensor core (fp32); the tile's 64 slots are
-// handled as two halves of 32 that share the scaled tile max; p = 2^(s*c - m)
-// rounded to bf16; each half keeps its own running sum of the rounded p;
-// O = O * alpha + P V on the tensor core.  Splits are merged in split order.
-// The running state (m, l_A, l_B, O) is carried between kernels as exact
-// fp32 and every tile update runs the same code, so the result depends only
-// on the row's query and key sequence: a node verified in a tree and the same
-// token decoded after its ancestors were committed produce the same bits.
+// Row function.  Row (node, query head) sees logical positions 0 .. P =
+// L+d: the L cache rows, then its ancestors-or-self at L .. L+d.  Its
+// positions split at 64R, R = max(floor(P/64) - 1, 0), a function of P alone.
+// Below 64R: tiles of 64 positions in splits of plan.split positions, both
+// aligned at absolute position 0.  Within a split the tiles run in order
+// through one online softmax: S = Q K^T on the tensor core (fp32); the tile's
+// 64 slots are handled as two halves of 32 that share the scaled tile max;
+// p = 2^(s*c - m) rounded to bf16; each half keeps its own running sum of the
+// rounded p; O = O * alpha + P V on the tensor core.  From 64R to P (65 to
+// 128 positions once P >= 64: at most two cache tiles and the ancestors):
+// the own segment, one softmax in fp32 on the CUDA cores.  The split states
+// and the own state are merged in that order.  Every state is carried as
+// exact fp32 and each piece runs the same code for the same positions, so
+// the result depends only on the row's query and key sequence: a node
+// verified in a tree and the same token decoded after its ancestors were
+// committed produce the same bits.
 //
 // Kernels.
 //  split kernel (persistent, one CTA per SM): the tiles that every node of a
-//    sequence shares (positions below 64*floor(L/64), all cache rows) for up to
-//    128 query rows (node x head of one KV head) at once.  Warps 0 and 10
-//    stream K and V tiles with TMA (128B-swizzled boxes) through two rings,
-//    prefetching into L2 the tile two ahead (and, before the wait for the
-//    previous kernel, the first tiles);
+//    sequence shares (below 64 * (floor((L + d_max)/64) - 1), all cache rows)
+//    for up to 128 query rows (node x head of one KV head) at once.  Warps 0
+//    and 10 stream K and V tiles with TMA (128B-swizzled boxes) through two
+//    rings, prefetching into L2 the tile two ahead (and, before the wait for
+//    the previous kernel, the first tiles);
 //    warp 1 issues QK^T (Q in TMEM, K in
 //    shared memory, S double-buffered in TMEM) and warp 11 issues PV (P in a
 //    ring of shared-memory slots, V in shared memory, O in TMEM); warps 2-5
@@ -32,13 +36,15 @@
 //    128-row blocks, the two row blocks of a (sequence, KV head, split) run
 //    on neighbouring CTAs that stream the same tiles side by side, so the
 //    second read of a tile is served by L2; each of the two prefetches half
-//    of every tile's boxes into L2.  Each split's state goes to the workspace.
-//  tail kernel (one CTA per node and KV head): the node's own tiles (cache
-//    rows past the last shared tile plus its ancestors at their logical
-//    slots, gathered into shared memory with cp.async, the first one before
-//    the wait for the split kernel), continuing the split state the split
-//    kernel left, then the in-order merge of all splits and the bf16 output
-//    (times the front end's sigmoid gate when one is given).
+//    of every tile's boxes into L2.  Each split's state goes to the
+//    workspace; the last split of a sequence whose rows start their own
+//    segments at two different tiles also leaves its state one tile before
+//    its end.
+//  tail kernel (one CTA per node and KV head, no tensor memory): the node's
+//    own segment for its G query rows, from K/V rows gathered into shared
+//    memory with cp.async, computed while the split kernel's last CTAs run;
+//    then, after the wait for the split kernel, the in-order merge and the
+//    bf16 output (times the front end's sigmoid gate when one is given).
 //  Decode runs the same two kernels with a one-node tree per sequence and
 //  appends its own K/V row.
 #include <cmath>
@@ -84,10 +90,6 @@ struct Tc {
   static constexpr int RING = (NK + NV) * TILE + NP * PTILE;
   static constexpr int NBAR = 2 * (NK + NV) + 2 * NP + 9;
   static constexpr int SMEM_SPLIT = 1024 + RING + NBAR * 8 + 16;
-  // tail kernel: tiles, P, barriers, then (sized at launch) the staged
-  // partial states of the splits the split kernel finished
-  static constexpr int TAIL_FIXED = 1024 + 2 * TILE + PTILE + 1024;
-  static constexpr int REC = D + 4;  // workspace record: O[D], m, l_A, l_B, pad
 };
 
 struct TcParams {
@@ -106,7 +108,11 @@ struct TcParams {
   int32_t* status;
   float* ws;
   int n_seq, n_total, Hq, Hkv, G, cap, max_len, split_tiles, max_splits, rows_max, decode;
-  int n_mstage;  // tail kernel: finished splits whose states are staged in shared memory
+  int ws_splits;    // records per (sequence, KV head, row): the splits, then the snapshot
+  int tail_two;     // tail kernel: keys and values staged at once (else keys, then values)
+  int tail_staged;  // tail kernel: the split records' weights and sums fit its shared memory
+  int tail_a;       // tail kernel: offset of the own-segment buffers (and staged records) in shared memory
+  int n_mstage;     // tail kernel: split records staged in shared memory
   int pair;      // split kernel: CTAs 2c, 2c+1 run row blocks 0, 1 of the same (sequence, KV head, split)
   float c;  // scale * log2(e)
 };
@@ -223,8 +229,11 @@ __device__ __forceinline__ void rescale_o(uint32_t tO, int c0, int c1, float alp
 }
 
 // Workspace record of (sequence, KV head, split, row).
+// Record slot past the splits: the state of a sequence's last split one
+// tile before its end.
+__device__ __forceinline__ int snap_slot(const TcParams& p) { return p.max_splits; }
 __device__ __forceinline__ float* ws_rec(const TcParams& p, int s, int g, int split, int row, int D) {
-  return p.ws + ((((static_cast<size_t>(s) * p.Hkv + g) * p.max_splits + split) * p.rows_max + row) *
+  return p.ws + ((((static_cast<size_t>(s) * p.Hkv + g) * p.ws_splits + split) * p.rows_max + row) *
                  static_cast<size_t>(D + 4));
 }
 
@@ -330,11 +339,80 @@ __device__ __forceinline__ void store_state_warp(uint32_t tO, uint32_t xbuf, int
 }
 
 // ---------------------------------------------------------------------------
+// rows and their segments
+// ---------------------------------------------------------------------------
+// First tile of the own segment of a row whose last position is P.  It
+// depends on P alone, so a verified row and the decode row of the same token
+// cut their positions in the same place; one tile back from P's tile, so
+// that for every node of a tree (depth below 64) the tiles before it are
+// cache tiles below floor(L/64), which the whole tree shares.
+__device__ __forceinline__ int own_tile(int P) { return max((P >> 6) - 1, 0); }
+// Tiles of a sequence that the split kernel runs: those below the own
+// segment of its deepest possible row (depth below the tree's size and
+// TV_MAX_PATH).  Every row of the sequence starts its own segment at this
+// tile or one before it.
+__device__ __forceinline__ int split_end(int L, int nodes, int decode) {
+  const int dub = decode ? 0 : min(max(nodes - 1, 0), TV_MAX_PATH - 1);
+  return own_tile(L + dub);
+}
+
+// The sequence, first node, context length, tree size and depth of a node
+// (verify) or of a sequence's one row (decode).
+struct RowInfo {
+  int s, off, L, nodes, depth;
+};
+__device__ inline RowInfo row_info(const TcParams& p, int node_g) {
+  RowInfo ri;
+  if (p.decode) {
+    ri.s = node_g;
+    ri.off = node_g;
+    ri.L = p.len[node_g];
+    ri.nodes = 1;
+    ri.depth = 0;
+    return ri;
+  }
+  // every global load issued before any result is used
+  int ends[TV_MAX_SEQ], lens[TV_MAX_SEQ];
+#pragma unroll
+  for (int i = 0; i < TV_MAX_SEQ; i++) {
+    ends[i] = i < p.n_seq ? p.node_off[i + 1] : 0;
+    lens[i] = i < p.n_seq ? p.len[i] : 0;
+  }
+  const int off0 = p.node_off[0];
+  const MetaView mv = meta_view(const_cast<void*>(p.meta), p.n_total);
+  const int depth = mv.depth[node_g];
+  ri.depth = depth < 0 ? 0 : (depth >= TV_MAX_PATH ? TV_MAX_PATH - 1 : depth);
+  ri.s = 0;
+  ri.off = off0;
+  ri.L = lens[0];
+  int end = ends[0];
+#pragma unroll
+  for (int i = 0; i + 1 < TV_MAX_SEQ; i++) {
+    if (i + 1 < p.n_seq && node_g >= ends[i]) {
+      ri.s = i + 1;
+      ri.off = ends[i];
+      ri.L = lens[i + 1];
+      end = ends[i + 1];
+    }
+  }
+  ri.nodes = end - ri.off;
+  return ri;
+}
+// A row unit the own-segment and merge kernels can run: a length within the
+// host bound (and, for decode, a free cache row) and a node whose rows lie
+// inside the workspace (a malformed tree is reported by tv_tree_prepare).
+__device__ __forceinline__ bool row_ok(const TcParams& p, const RowInfo& ri, int local) {
+  return ri.L >= 0 && ri.L <= p.max_len && !(p.decode && ri.L >= p.cap) && local >= 0 &&
+         (local + 1) * p.G <= p.rows_max;
+}
+
+// ---------------------------------------------------------------------------
 // split kernel
 // ---------------------------------------------------------------------------
 struct ItemSpace {
   int cum[TV_MAX_SEQ + 1];
-  int tsh[TV_MAX_SEQ];   // shared tiles of each sequence
+  int tend[TV_MAX_SEQ];  // tiles of each sequence run here
+  int snap[TV_MAX_SEQ];  // some row starts its own segment at tend - 1: the last split keeps a snapshot
   int nrb[TV_MAX_SEQ];   // 128-row blocks
   int rows[TV_MAX_SEQ];  // query rows = nodes * G
   int off[TV_MAX_SEQ];   // first node
@@ -359,8 +437,9 @@ __device__ inline void item_space(const TcParams& p, ItemSpace& is) {
     is.off[s] = off;
     is.rows[s] = nodes * p.G;
     is.nrb[s] = p.pair ? 1 : (is.rows[s] + 127) / 128;  // a pair covers row blocks 0 and 1
-    is.tsh[s] = L / kTile;
-    const int nsplit = (is.tsh[s] + p.split_tiles - 1) / p.split_tiles;
+    is.tend[s] = split_end(L, nodes, p.decode);
+    is.snap[s] = is.tend[s] > own_tile(L) ? 1 : 0;  // the root's row starts one tile earlier
+    const int nsplit = (is.tend[s] + p.split_tiles - 1) / p.split_tiles;
     is.cum[s + 1] = is.cum[s] + nsplit * p.Hkv * is.nrb[s];
   }
 }
@@ -376,7 +455,7 @@ __device__ inline Item item_at(const ItemSpace& is, const TcParams& p, int w, in
   it.g = r % p.Hkv;
   it.split = r / p.Hkv;
   it.t0 = it.split * p.split_tiles;
-  it.t1 = min(it.t0 + p.split_tiles, is.tsh[s]);
+  it.t1 = min(it.t0 + p.split_tiles, is.tend[s]);
   return it;
 }
 
@@ -587,6 +666,8 @@ __global__ void __launch_bounds__(384, 1) attn_split_kernel(const __grid_constan
     for (int w = cid; w < total && ok; w += ncl) {
       const Item I = item_at(is, p, w, rank);
       const int n = I.t1 - I.t0;
+      const int rbase = I.rb * 128 + quad * 32, nrows = is.rows[I.s];
+      const bool snap_item = is.snap[I.s] && I.t1 == is.tend[I.s] && n >= 2;
       // this thread's Q share (bf16 pairs) into TMEM; every QK^T of the
       // previous item has completed (its S was read)
       if (w != cid) q_fetch<D>(q_row(I), hf, qv);
@@ -606,6 +687,23 @@ __global__ void __launch_bounds__(384, 1) attn_split_kernel(const __grid_constan
         tmem_ld32f(tl + C::T_S + b * kTile + hf * kHalf, sv);
         tc_fence_before();
         mbar_arrive(SFREE0 + 8u * b);  // S(t) is in registers: QK^T(t+2) may overwrite the buffer
+        if (snap_item && k == n - 1) {
+          // The state one tile before the split's end, for the rows whose own
+          // segment starts at this tile: O once PV of the previous tile is
+          // complete, with m and the sums before this tile.  Every PV so far
+          // is then complete, so the P ring is free until this tile's P,
+          // which no warp writes before the half-max exchange below.
+          const uint32_t tp = t - 1;
+          if (!wait_warp(ODONE0 + 8u * (tp % C::NP), (tp / C::NP) & 1, abort_flag, kWaitCycles)) {
+            ok = false;
+            break;
+          }
+          tc_fence_after();
+          store_state_warp<D>(tl + C::T_O, pring + static_cast<uint32_t>(warp - 2) * 4096u, hf, lane, m, lh,
+                              [&](int r) -> float* {
+                                return rbase + r < nrows ? ws_rec(p, I.s, I.g, snap_slot(p), rbase + r, D) : nullptr;
+                              });
+        }
         const float mh = half_max(sv, kHalf);
         xmax[b][hf][lrow] = mh;
         mbar_arrive(XBAR0 + 8u * b);
@@ -655,7 +753,6 @@ __global__ void __launch_bounds__(384, 1) attn_split_kernel(const __grid_constan
       // warpgroup writes only after this read of O.  Every PV of the item is
       // complete, so the P ring is free: warp k of the softmax turns its rows
       // around in the ring's k-th 4 KB.
-      const int rbase = I.rb * 128 + quad * 32, nrows = is.rows[I.s];
       store_state_warp<D>(tl + C::T_O, pring + static_cast<uint32_t>(warp - 2) * 4096u, hf, lane, m, lh,
                           [&](int r) -> float* {
                             return rbase + r < nrows ? ws_rec(p, I.s, I.g, I.split, rbase + r, D) : nullptr;
@@ -669,462 +766,416 @@ __global__ void __launch_bounds__(384, 1) attn_split_kernel(const __grid_constan
   if (warp == 1) tmem_dealloc(tbase, C::COLS);
 }
 
-// ---------------------------------------------------------------------------
-// tail kernel: the node's own tiles, then the split merge
-// ---------------------------------------------------------------------------
 __device__ __forceinline__ void cp_async16(uint32_t dst, const void* src, bool valid) {
   asm volatile("cp.async.cg.shared.global [%0], [%1], 16, %2;" ::"r"(dst), "l"(src), "r"(valid ? 16 : 0)
                : "memory");
 }
-__device__ __forceinline__ void cp_async_wait_all() { asm volatile("cp.async.wait_all;" ::: "memory"); }
+__device__ __forceinline__ void cp_async_commit() { asm volatile("cp.async.commit_group;" ::: "memory"); }
+template <int N>
+__device__ __forceinline__ void cp_async_wait_group() {
+  asm volatile("cp.async.wait_group %0;" ::"n"(N) : "memory");
+}
+
+// ---------------------------------------------------------------------------
+// tail kernel: the row's own segment, then the merge
+// ---------------------------------------------------------------------------
+// Warp-level bf16 tensor-core tiles (m16n8k16, fp32 accumulate) for the own
+// segment's two small products: its rows are one node's G query heads, far
+// below the 64- or 128-row tiles of tcgen05, and these need no tensor memory,
+// so several tail CTAs share an SM.
+__device__ __forceinline__ void ldsm_x4(uint32_t addr, uint32_t (&r)[4]) {
+  asm volatile("ldmatrix.sync.aligned.m8n8.x4.shared.b16 {%0, %1, %2, %3}, [%4];"
+               : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3])
+               : "r"(addr));
+}
+__device__ __forceinline__ void ldsm_x4_t(uint32_t addr, uint32_t (&r)[4]) {
+  asm volatile("ldmatrix.sync.aligned.m8n8.x4.trans.shared.b16 {%0, %1, %2, %3}, [%4];"
+               : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3])
+               : "r"(addr));
+}
+// d += a b for one 16 x 8 x 16 tile (a: 16 x 16 row-major, b: 16 x 8 column-major)
+__device__ __forceinline__ void mma16816(float (&d)[4], const uint32_t (&a)[4], uint32_t b0, uint32_t b1) {
+  asm volatile("mma.sync.aligned.m16n8k16.row.col.f32.bf16.bf16.f32 {%0, %1, %2, %3}, {%4, %5, %6, %7}, {%8, %9}, "
+               "{%0, %1, %2, %3};"
+               : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
+               : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b0), "r"(b1));
+}
+// Byte offset of 16-byte chunk c of row r in a buffer of rows rb bytes long:
+// chunk c sits at c ^ (r mod 8), so the 8 rows of an 8 x 8 matrix load fall
+// on distinct banks.
+__device__ __forceinline__ uint32_t swz(int r, int c, int rb) {
+  return static_cast<uint32_t>(r * rb + ((c ^ (r & 7)) << 4));
+}
 
 template <int D>
-__global__ void __launch_bounds__(256, 1) attn_tail_kernel(const __grid_constant__ TcParams p) {
-  using C = Tc<D>;
-  extern __shared__ uint8_t smem_raw[];
-  __shared__ int skip;
-  __shared__ float xmax[2][128];
+struct Tail {
+  static constexpr int NT = 512;          // threads
+  static constexpr int NW = NT / 32;      // warps
+  static constexpr int CH = D / 8;        // 16-byte chunks of a K/V/Q row
+  static constexpr int NPOS = 2 * kTile;  // positions of an own segment, at most
+  static constexpr int KV = NPOS * D * 2; // bytes of its keys (or values)
+  static constexpr int PRB = NPOS * 2;    // bytes of a probability row
+  static constexpr int MB = 8;            // unstaged split records in flight per merge thread
+  static constexpr int REC = (D + 4) * 4; // bytes of one record row: O[D], m, l_A, l_B, pad
+  // Shared memory: the own segment's O [G][D] fp32 and (when staged) the
+  // merge's weights and sums come first; from offset tail_a the own
+  // segment's buffers: keys [NPOS][D] bf16, values (their own buffer, or the
+  // keys' after the scores), queries [16 MT][D] bf16, probabilities
+  // [16 MT][NPOS] bf16 (MT = ceil(G/16) row tiles; K/V/Q/P rows
+  // chunk-swizzled) and scores [G][NPOS] fp32.  Once the own segment is
+  // done, the split records are staged from tail_a on, as many as fit.
+  __host__ __device__ static constexpr int q_off(bool two) { return (two ? 2 : 1) * KV; }
+  __host__ __device__ static constexpr int p_off(int G, bool two) { return q_off(two) + ((G + 15) / 16) * 16 * D * 2; }
+  __host__ __device__ static constexpr int sc_off(int G, bool two) { return p_off(G, two) + ((G + 15) / 16) * 16 * PRB; }
+  __host__ __device__ static constexpr int own_bytes(int G, bool two) { return sc_off(G, two) + G * NPOS * 4; }
+  __host__ __device__ static constexpr int wbytes(int G, int max_splits) { return (2 * max_splits + 2) * G * 4; }
+  __host__ __device__ static constexpr int a_off(int G, int wb) { return (G * D * 4 + wb + 1023) & ~1023; }
+};
+
+// One CTA per (node, KV head), or (sequence, KV head) for decode; the split
+// kernel of the same call runs before it.
+//  Own segment, before the wait for the split kernel (which writes none of
+//  what it reads): the segment's K/V rows (cache rows below L, then the
+//  node's ancestors-or-self at L .. L+d; zeros up to a multiple of 16) and
+//  the node's G query rows come into shared memory with cp.async; with two
+//  buffers the values load while the scores are computed, with one they
+//  follow the keys into the same buffer.  S = Q K^T by 16 x 8 x 16 tensor-core
+//  tiles, each output accumulated over the head dimension in order; m = the
+//  segment's scaled maximum; p = 2^(s*c - m) rounded to bf16; l = the sum of
+//  the rounded p over a warp's fixed lanes; O = P V by the same tiles,
+//  accumulated over the positions in order.  Verify and decode place a
+//  row's positions and heads in the same tile slots, so both run the same
+//  arithmetic.
+//  Merge, after the wait: the split records of the node's G rows (each
+//  record's rows are contiguous) come into shared memory by bulk copies, as
+//  many as fit, while the weights are formed from their m and l read
+//  directly.  A row takes its split states, then its own state.  The last
+//  split is the one the split kernel finished unless that split ran one
+//  tile past the row's own segment start, in which case it is the snapshot
+//  taken one tile before its end.  Weights 2^(m_i - max m), O = sum w_i O_i
+//  and l = sum w_i (l_A + l_B) in record order; the output is O / l (times
+//  the front end's sigmoid gate when one is given).  Decode then appends the
+//  token's K/V at row L.
+template <int D>
+__global__ void __launch_bounds__(512, 2) attn_tail_kernel(const __grid_constant__ TcParams p) {
+  using T = Tail<D>;
+  extern __shared__ __align__(16) uint8_t tsm[];
   __shared__ int anc_s[TV_MAX_PATH];  // global node of the ancestor at each depth
-  const uint32_t raw = smem_u32(smem_raw);
-  const uint32_t sb = (raw + 1023u) & ~1023u;
-  uint8_t* gb = smem_raw + (sb - raw);
-  const uint32_t pbase = sb + 2 * C::TILE;  // P tile (the PV A operand)
-  const uint32_t BAR = pbase + C::PTILE, DRAIN = BAR + 8, MBAR = BAR + 16;
-  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(gb + 2 * C::TILE + C::PTILE + 16);
-  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const int hf = warp >> 2;  // softmax half of this thread
-  const int lrow = (warp & 3) * 32 + lane;
-  const int item = blockIdx.x;
-  const int g = item % p.Hkv;
-  const int node_g = item / p.Hkv;  // global node (verify) or sequence (decode)
-  // the node's sequence, offset, depth, ancestors and context length, with
-  // every global load issued before any result is used
-  int s = 0, off = 0, depth = 0, L = 0;
-  if (p.decode) {
-    s = node_g;
-    off = node_g;
-    L = p.len[s];
-    if (threadIdx.x < TV_MAX_PATH) anc_s[threadIdx.x] = node_g;
-  } else {
-    int ends[TV_MAX_SEQ], lens[TV_MAX_SEQ];
-#pragma unroll
-    for (int i = 0; i < TV_MAX_SEQ; i++) {
-      ends[i] = i < p.n_seq ? p.node_off[i + 1] : 0;
-      lens[i] = i < p.n_seq ? p.len[i] : 0;
-    }
-    const int off0 = p.node_off[0];
-    MetaView mv = meta_view(const_cast<void*>(p.meta), p.n_total);
-    depth = mv.depth[node_g];
-    depth = depth < 0 ? 0 : (depth >= TV_MAX_PATH ? TV_MAX_PATH - 1 : depth);
-    const int a = threadIdx.x < TV_MAX_PATH ? mv.anc_at[static_cast<size_t>(node_g) * TV_MAX_PATH + threadIdx.x] : 0;
-    off = off0;
-    L = lens[0];
-#pragma unroll
-    for (int i = 0; i + 1 < TV_MAX_SEQ; i++) {
-      if (i + 1 < p.n_seq && node_g >= ends[i]) {
-        s = i + 1;
-        off = ends[i];
-        L = lens[i + 1];
-      }
-    }
-    // clamped to the node buffers: with a malformed tree (reported by
-    // tv_tree_prepare) the tables may be stale, and the first tile is
-    // gathered before the status word is read
-    const int an = threadIdx.x > depth ? node_g : off + a;
-    if (threadIdx.x < TV_MAX_PATH) anc_s[threadIdx.x] = an < 0 ? 0 : (an >= p.n_total ? p.n_total - 1 : an);
-  }
-  const int local = node_g - off;
-  const int G = p.G;
-  // Set-up that needs nothing the split kernel writes: barriers, TMEM and,
-  // when they fit in the P tile area, the node's query rows and its first
-  // own tile (cache rows and tree rows), so that their loads overlap the
-  // split kernel's last CTAs.  The carried split state waits for it.
-  if (threadIdx.x == 0) {
-    mbar_init(BAR, 1);
-    mbar_init(DRAIN, 1);
+  __shared__ int skip;
+  __shared__ float mown[kMaxGroup], lown[kMaxGroup];
+  __shared__ __align__(8) uint64_t mbar;  // staged split records
+  const int G = p.G, tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  const int g = static_cast<int>(blockIdx.x) % p.Hkv, node_g = static_cast<int>(blockIdx.x) / p.Hkv;
+  const bool two = p.tail_two != 0;
+  const int MT = (G + 15) / 16;
+  const uint32_t MBAR = smem_u32(&mbar);
+  if (tid == 0) {
     mbar_init(MBAR, 1);
     fence_mbar_init();
   }
-  if (warp == 0) {
-    tmem_alloc(smem_u32(tmem_slot), C::COLS);
-    tmem_relinquish();
-  }
-  const bool lok = L >= 0 && L <= p.max_len && !(p.decode && L >= p.cap);
-  const uint32_t qbytes = static_cast<uint32_t>(G * D * 2 + 15) & ~15u;
-  const bool early = lok && qbytes + static_cast<uint32_t>(G * C::REC * 4) <= static_cast<uint32_t>(C::PTILE);
-  const uint32_t qstage = early ? pbase : sb + C::TILE, ostage = early ? pbase + qbytes : sb;
-  const int P = L + depth + 1;
-  const int tsh = lok ? L / kTile : 0;
-  // the node's K/V tile t: cache rows below L, ancestors at L..L+d, zeros after
-  auto gather = [&](int t) {
-    for (int idx = threadIdx.x; idx < kTile * (D / 8); idx += blockDim.x) {
-      const int j = idx / (D / 8), cc = idx % (D / 8), pos = t * kTile + j;
-      const __nv_bfloat16* ksrc = p.kt;
-      const __nv_bfloat16* vsrc = p.vt;
-      bool have = false;
-      if (pos < L) {
-        const size_t r = (static_cast<size_t>(g) * p.cap + pos) * D + cc * 8;
-        ksrc = p.K[s] + r;
-        vsrc = p.V[s] + r;
-        have = true;
-      } else if (pos < P) {
-        const size_t r = (static_cast<size_t>(anc_s[pos - L]) * p.Hkv + g) * D + cc * 8;
-        ksrc = p.kt + r;
-        vsrc = p.vt + r;
-        have = true;
-      }
-      const int kb = cc >> 3, c = cc & 7;
-      const uint32_t o = kb * kBox + (j >> 3) * 1024 + (j & 7) * 128 + ((c ^ (j & 7)) << 4);
-      cp_async16(sb + o, ksrc, have);
-      cp_async16(sb + C::TILE + o, vsrc, have);
+  // Lengths, tree tables, queries, caches and the tree's K/V rows: none is
+  // written by the split kernel before this one, and the split kernel lets
+  // this kernel in only after its own wait, so all are complete.
+  const RowInfo ri = row_info(p, node_g);
+  const int local = node_g - ri.off;
+  const bool rok = row_ok(p, ri, local);
+  if (tid < TV_MAX_PATH) {
+    int an = node_g;
+    if (!p.decode) {
+      const MetaView mv = meta_view(const_cast<void*>(p.meta), p.n_total);
+      const int a = mv.anc_at[static_cast<size_t>(node_g) * TV_MAX_PATH + tid];
+      an = tid > ri.depth ? node_g : ri.off + a;
     }
-  };
-  if (early) {
-    __syncthreads();  // anc_s
-    const __nv_bfloat16* qsrc = p.q + (static_cast<size_t>(node_g) * p.Hq + g * G) * D;
-    for (int idx = threadIdx.x; idx < G * D / 8; idx += blockDim.x) cp_async16(qstage + idx * 16, qsrc + idx * 8, true);
-    gather(tsh);
+    // clamped to the node buffers: with a malformed tree (reported by
+    // tv_tree_prepare) the tables may be stale
+    anc_s[tid] = an < 0 ? 0 : (an >= p.n_total ? p.n_total - 1 : an);
+  }
+  __syncthreads();
+  const int P = ri.L + ri.depth;
+  const int tend = split_end(ri.L, ri.nodes, p.decode);
+  const int R = min(own_tile(P), tend);
+  const int p0 = R * kTile, n = min(P - p0 + 1, T::NPOS);
+  const int n16 = (n + 15) & ~15;  // positions the tiles cover
+  float* const oown = reinterpret_cast<float*>(tsm);  // [G][D]
+  uint8_t* const ob = tsm + p.tail_a;                 // own-segment buffers, then staged records
+  float* const sc = reinterpret_cast<float*>(ob + T::sc_off(G, two));  // [G][NPOS]
+  if (rok) {
+    const uint32_t kb = smem_u32(ob), vb = two ? kb + T::KV : kb;
+    const uint32_t qb = kb + T::q_off(two), pb = kb + T::p_off(G, two);
+    auto stage = [&](uint32_t dst, bool values) {
+      const __nv_bfloat16* cache = values ? p.V[ri.s] : p.K[ri.s];
+      const __nv_bfloat16* tree = values ? p.vt : p.kt;
+      for (int idx = tid; idx < n16 * T::CH; idx += T::NT) {
+        const int j = idx / T::CH, cc = idx % T::CH, pos = p0 + j;
+        const __nv_bfloat16* src =
+            j >= n ? tree
+                   : (pos < ri.L ? cache + (static_cast<size_t>(g) * p.cap + pos) * D + cc * 8
+                                 : tree + (static_cast<size_t>(anc_s[pos - ri.L]) * p.Hkv + g) * D + cc * 8);
+        cp_async16(dst + swz(j, cc, D * 2), src, j < n);  // zeros past the segment
+      }
+    };
+    stage(kb, false);
+    {
+      const __nv_bfloat16* qsrc = p.q + (static_cast<size_t>(node_g) * p.Hq + g * G) * D;
+      for (int idx = tid; idx < MT * 16 * T::CH; idx += T::NT) {
+        const int r = idx / T::CH, cc = idx % T::CH;
+        cp_async16(qb + swz(r, cc, D * 2), r < G ? qsrc + r * D + cc * 8 : qsrc, r < G);
+      }
+    }
+    cp_async_commit();
+    if (two) stage(vb, true);
+    cp_async_commit();
+    // probability rows past the group stay zero
+    for (int idx = tid; idx < (MT * 16 - G) * (T::PRB / 16); idx += T::NT) {
+      const int r = G + idx / (T::PRB / 16), cc = idx % (T::PRB / 16);
+      *reinterpret_cast<uint4*>(ob + T::p_off(G, two) + swz(r, cc, T::PRB)) = make_uint4(0u, 0u, 0u, 0u);
+    }
+    cp_async_wait_group<1>();  // keys and queries
+    __syncthreads();
+    // S = Q K^T: warp items (row tile, 8-position tile); two k-steps per pass
+    {
+      const int nt8 = (n + 7) >> 3, mi = lane >> 3, rr = lane & 7;
+      for (int it = warp; it < MT * nt8; it += T::NW) {
+        const int mt = it / nt8, nt = it % nt8;
+        float acc[4] = {0.f, 0.f, 0.f, 0.f};
+        const int qrow = mt * 16 + (mi & 1) * 8 + rr, krow = nt * 8 + rr;
+#pragma unroll 4
+        for (int ks = 0; ks < D / 16; ks += 2) {
+          uint32_t a0[4], a1[4], b[4];
+          ldsm_x4(qb + swz(qrow, 2 * ks + (mi >> 1), D * 2), a0);
+          ldsm_x4(qb + swz(qrow, 2 * ks + 2 + (mi >> 1), D * 2), a1);
+          ldsm_x4(kb + swz(krow, 2 * ks + mi, D * 2), b);  // chunks 2ks .. 2ks + 3 of the 8 key rows
+          mma16816(acc, a0, b[0], b[1]);
+          mma16816(acc, a1, b[2], b[3]);
+        }
+        const int r0 = mt * 16 + (lane >> 2), j0 = nt * 8 + 2 * (lane & 3);
+#pragma unroll
+        for (int h = 0; h < 2; h++) {
+          const int r = r0 + 8 * h;
+          if (r < G) {
+            if (j0 < n) sc[r * T::NPOS + j0] = acc[2 * h];
+            if (j0 + 1 < n) sc[r * T::NPOS + j0 + 1] = acc[2 * h + 1];
+          }
+        }
+      }
+    }
+    __syncthreads();
+    if (!two) {
+      stage(kb, true);  // every read of the keys is done
+      cp_async_commit();
+    }
+    // softmax: warp w takes rows w, w + 16, ...; lane takes positions lane + 32i
+    {
+#pragma unroll 1
+      for (int r = warp; r < G; r += T::NW) {
+        const float* row = sc + r * T::NPOS;
+        float v[4], mx = -INFINITY;
+#pragma unroll
+        for (int i = 0; i < 4; i++) {
+          const int j = lane + 32 * i;
+          v[i] = j < n ? row[j] : -INFINITY;
+          mx = fmaxf(mx, v[i]);
+        }
+#pragma unroll
+        for (int o = 16; o >= 1; o >>= 1) mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, o));
+        const float m = __fmul_rn(mx, p.c);
+        float e[4];
+#pragma unroll
+        for (int i = 0; i < 4; i++) {
+          const int j = lane + 32 * i;
+          const float pj = j < n ? ex2_approx(__fmaf_rn(v[i], p.c, -m)) : 0.f;
+          const __nv_bfloat16 pb16 = __float2bfloat16_rn(pj);
+          e[i] = __bfloat162float(pb16);
+          *reinterpret_cast<__nv_bfloat16*>(ob + T::p_off(G, two) + swz(r, j >> 3, T::PRB) + (j & 7) * 2) = pb16;
+        }
+        float l = __fadd_rn(__fadd_rn(e[0], e[1]), __fadd_rn(e[2], e[3]));
+#pragma unroll
+        for (int o = 16; o >= 1; o >>= 1) l = __fadd_rn(l, __shfl_xor_sync(0xffffffffu, l, o));
+        if (lane == 0) {
+          mown[r] = m;
+          lown[r] = l;
+        }
+      }
+    }
+    cp_async_wait_group<0>();  // values
+    __syncthreads();
+    // O = P V: warp items (row tile, pair of 8-column tiles of the head dimension)
+    {
+      const int nk = n16 >> 4, mi = lane >> 3, rr = lane & 7;
+      constexpr int NDT = D / 16;  // column-tile pairs
+      for (int it = warp; it < MT * NDT; it += T::NW) {
+        const int mt = it / NDT, dt = it % NDT;
+        float acc0[4] = {0.f, 0.f, 0.f, 0.f}, acc1[4] = {0.f, 0.f, 0.f, 0.f};
+        const int prow = mt * 16 + (mi & 1) * 8 + rr;
+        // V^T fragments: matrices (rows 0-7, cols 2dt), (rows 8-15, 2dt), (0-7, 2dt+1), (8-15, 2dt+1)
+        const int vrow_in = (mi & 1) * 8 + rr, vchunk = 2 * dt + (mi >> 1);
+        for (int kt = 0; kt < nk; kt++) {
+          uint32_t a[4], b[4];
+          ldsm_x4(pb + swz(prow, 2 * kt + (mi >> 1), T::PRB), a);
+          ldsm_x4_t(vb + swz(16 * kt + vrow_in, vchunk, D * 2), b);
+          mma16816(acc0, a, b[0], b[1]);
+          mma16816(acc1, a, b[2], b[3]);
+        }
+        const int r0 = mt * 16 + (lane >> 2), d0 = dt * 16 + 2 * (lane & 3);
+#pragma unroll
+        for (int h = 0; h < 2; h++) {
+          const int r = r0 + 8 * h;
+          if (r < G) {
+            *reinterpret_cast<float2*>(oown + r * D + d0) = make_float2(acc0[2 * h], acc0[2 * h + 1]);
+            *reinterpret_cast<float2*>(oown + r * D + d0 + 8) = make_float2(acc1[2 * h], acc1[2 * h + 1]);
+          }
+        }
+      }
+    }
   }
   // the split kernel before this one writes the workspace and may set the status
   pdl_wait();
-  if (threadIdx.x == 0) {
+  if (tid == 0) {
     int bad = status_bad(p.status) ? 1 : 0;
-    if (!bad && (L < 0 || L > p.max_len)) {
+    if (!bad && (ri.L < 0 || ri.L > p.max_len)) {
       set_status(p.status, TV_ERR_LEN);
       bad = 1;
     }
-    if (!bad && p.decode && L >= p.cap) {
+    if (!bad && p.decode && ri.L >= p.cap) {
       set_status(p.status, TV_ERR_CAPACITY);
       bad = 1;
     }
+    if (!bad && !rok) bad = 1;  // a malformed tree: reported by tv_tree_prepare
     skip = bad;
   }
-  tc_fence_before();
-  __syncthreads();
-  tc_fence_after();
-  const uint32_t tbase = *tmem_slot;
-  const uint32_t tl = tbase + (static_cast<uint32_t>((warp & 3) * 32) << 16);
-
-  if (skip) cp_async_wait_all();  // copies issued before the wait land before the CTA leaves
-  if (!skip) {
-    const int tlast = (L + depth) / kTile;
-    const int ST = p.split_tiles;
-    const bool vrow = lrow < G;
-    const int row_seq = local * G + lrow;
-    int cur = tsh / ST;
-    const bool cont = (tsh % ST) != 0;  // the split kernel started this split
-
-    // The finished splits' states (the node's G rows of a split are one
-    // contiguous block) come in by bulk copies issued first thing after the
-    // wait, so their latency hides behind the carried state, the queries and
-    // the node's own tiles; the node's final split state is kept in shared
-    // memory too.  Shared layout: [nst][G][REC], then [G][REC].
-    const uint32_t mst_s = sb + (C::TAIL_FIXED - 1024);
-    const int nst = min(cur, p.n_mstage);
-    const uint32_t mown_s = mst_s + static_cast<uint32_t>(nst * G * C::REC * 4);
-    float* const mown = reinterpret_cast<float*>(gb + (C::TAIL_FIXED - 1024) + nst * G * C::REC * 4);
-    if (warp == 0 && nst > 0) {
-      // one lane sets the byte count first; the copies are spread over the warp
-      const uint32_t bytes = static_cast<uint32_t>(G * C::REC * 4);
-      if (lane == 0) mbar_arrive_expect_tx(MBAR, bytes * nst);
-      __syncwarp();
-      for (int sp = lane; sp < nst; sp += 32)
-        bulk_g2s(mst_s + sp * bytes, ws_rec(p, s, g, sp, local * G, D), bytes, MBAR);
+  fence_proxy_async_smem();  // this thread's accesses to the own-segment buffers come before the bulk copies
+  __syncthreads();  // also: the own segment's O, m and l are in shared memory
+  if (skip) return;
+  const int ST = p.split_tiles;
+  const int n_reg = (R + ST - 1) / ST;
+  const bool snap = n_reg > 0 && R != min(n_reg * ST, tend);
+  // record i of the node's rows: split i, or the snapshot in place of the last split
+  auto rec = [&](int i, int r) -> const float* {
+    const int slot = (i == n_reg - 1 && snap) ? snap_slot(p) : i;
+    return ws_rec(p, ri.s, g, slot, local * G + r, D);
+  };
+  const int nst = min(n_reg, p.n_mstage);  // records staged in shared memory
+  const uint32_t rbytes = static_cast<uint32_t>(G * T::REC);
+  if (warp == 0 && nst > 0) {
+    // one lane sets the byte count first; the copies are spread over the warp
+    if (lane == 0) mbar_arrive_expect_tx(MBAR, rbytes * nst);
+    __syncwarp();
+    for (int i = lane; i < nst; i += 32) bulk_g2s(smem_u32(ob) + i * rbytes, rec(i, 0), rbytes, MBAR);
+  }
+  auto weight = [](float m, float mm) { return m == mm ? 1.f : ex2_approx(__fsub_rn(m, mm)); };
+  const bool staged = p.tail_staged != 0;
+  float* const wgt = oown + G * D;                           // [n_reg][G]
+  float* const lsm = wgt + static_cast<size_t>(n_reg) * G;   // [n_reg][G]
+  float* const ltot = lsm + static_cast<size_t>(n_reg) * G;  // [G] max, then [G] sum
+  float* const wown = ltot + G;                              // [G] own weight
+  if (staged) {
+    for (int idx = tid; idx < n_reg * G; idx += T::NT) {
+      const float4 t4 = *reinterpret_cast<const float4*>(rec(idx / G, idx % G) + D);  // m, l_A, l_B, pad
+      wgt[idx] = t4.x;
+      lsm[idx] = __fadd_rn(t4.y, t4.z);
     }
-    // stage this node's G query rows (unless staged early) and, when
-    // continuing, the carried state records with cp.async
-    const bool ostaged = early || G * C::REC * 4 <= C::TILE;
-    {
-      if (!early) {
-        const __nv_bfloat16* qsrc = p.q + (static_cast<size_t>(node_g) * p.Hq + g * G) * D;
-        for (int idx = threadIdx.x; idx < G * D / 8; idx += blockDim.x)
-          cp_async16(qstage + idx * 16, qsrc + idx * 8, true);
-      }
-      if (cont && ostaged) {
-        for (int idx = threadIdx.x; idx < G * C::REC / 4; idx += blockDim.x) {
-          const int r = idx / (C::REC / 4), cc = idx % (C::REC / 4);
-          cp_async16(ostage + idx * 16, ws_rec(p, s, g, cur, local * G + r, D) + cc * 4, true);
-        }
-      }
-      cp_async_wait_all();
-      __syncthreads();
-    }
-    // Q and the carried O into TMEM (each half its own columns)
-    {
-      const uint4* qs = reinterpret_cast<const uint4*>(gb + (qstage - sb)) + lrow * (D / 8);
-#pragma unroll 1
-      for (int c0 = hf * (D / 4); c0 < (hf + 1) * (D / 4); c0 += 32) {
-        uint32_t r[32];
-#pragma unroll
-        for (int i = 0; i < 8; i++) {
-          const uint4 v = vrow ? qs[c0 / 4 + i] : make_uint4(0u, 0u, 0u, 0u);
-          r[4 * i] = v.x;
-          r[4 * i + 1] = v.y;
-          r[4 * i + 2] = v.z;
-          r[4 * i + 3] = v.w;
-        }
-        tmem_st32(tl + C::T_Q + c0, r);
-      }
-    }
-    float m = -INFINITY, lh = 0.f;
-    bool fresh = true;
-    if (cont) {
-      const float* rec = vrow ? (ostaged ? reinterpret_cast<const float*>(gb + (ostage - sb)) + lrow * C::REC
-                                         : ws_rec(p, s, g, cur, row_seq, D))
-                              : nullptr;
-#pragma unroll 1
-      for (int c0 = hf * (D / 2); c0 < (hf + 1) * (D / 2); c0 += 32) {
-        uint32_t r[32];
-#pragma unroll
-        for (int i = 0; i < 8; i++) {
-          const uint4 v = rec ? reinterpret_cast<const uint4*>(rec + c0)[i] : make_uint4(0u, 0u, 0u, 0u);
-          r[4 * i] = v.x;
-          r[4 * i + 1] = v.y;
-          r[4 * i + 2] = v.z;
-          r[4 * i + 3] = v.w;
-        }
-        tmem_st32(tl + C::T_O + c0, r);
-      }
-      if (rec) {
-        m = rec[D];
-        lh = rec[D + 1 + hf];
-      }
-      fresh = false;
-    }
-    tmem_st_wait();
-    tc_fence_before();
     __syncthreads();
-    tc_fence_after();
-
-    uint32_t ph = 0;
-    bool ok = true;
-    for (int t = tsh; t <= tlast && ok; t++) {
-      if (t / ST != cur) {
-        store_state<D>(tl + C::T_O, vrow ? ws_rec(p, s, g, cur, row_seq, D) : nullptr, hf, m, lh);
-        cur = t / ST;
-        fresh = true;
-        m = -INFINITY;
-        lh = 0.f;
-      }
-      // the node's K/V tile (the first one may have been gathered before the wait)
-      if (!(early && t == tsh)) gather(t);
-      cp_async_wait_all();
-      fence_proxy_async_smem();
-      tc_fence_before();
-      __syncthreads();
-      tc_fence_after();
-      if (threadIdx.x == 0) {
-        issue_qk<D>(tbase + C::T_S, tbase + C::T_Q, sb);
-        tc_commit(BAR);
-      }
-      if (__syncthreads_or(!mbar_wait(BAR, ph, kWaitCycles))) {
-        ok = false;
-        break;
-      }
-      ph ^= 1;
-      tc_fence_after();
-      float sv[kHalf];
-      tmem_ld32f(tl + C::T_S + hf * kHalf, sv);
-      const int nvalid = min(kTile, P - t * kTile) - hf * kHalf;
-      const float mh = half_max(sv, nvalid);
-      xmax[hf][lrow] = mh;
-      tc_fence_before();
-      __syncthreads();
-      tc_fence_after();
-      const float mo = xmax[hf ^ 1][lrow];
-      float alpha;
-      const float m_new = next_max(m, fmaxf(mh, mo), p.c, alpha);
-      uint32_t Pw[kHalf / 2];
-      const float rs = half_probs(sv, nvalid, p.c, m_new, Pw);
-      lh = __fmaf_rn(lh, alpha, rs);
-      m = m_new;
-      store_p_half(pbase, lrow, hf, Pw);
-      if (!fresh && __any_sync(0xffffffffu, alpha != 1.f))
-        rescale_o(tl + C::T_O, hf * (D / 2), (hf + 1) * (D / 2), alpha);
-      tmem_st_wait();
-      fence_proxy_async_smem();  // P visible to the tensor core
-      tc_fence_before();
-      __syncthreads();
-      tc_fence_after();
-      if (threadIdx.x == 0) {
-        issue_pv_ss<D>(tbase + C::T_O, pbase, desc_v(sb + C::TILE, 0), !fresh);
-        tc_commit(BAR);
-      }
-      if (__syncthreads_or(!mbar_wait(BAR, ph, kWaitCycles))) {
-        ok = false;
-        break;
-      }
-      ph ^= 1;
-      tc_fence_after();
-      fresh = false;
+    for (int r = tid; r < G; r += T::NT) {
+      float mm = mown[r];
+      for (int i = 0; i < n_reg; i++) mm = fmaxf(mm, wgt[i * G + r]);
+      ltot[r] = mm;
     }
-    // the staged splits have landed (every thread observes the barrier, and
-    // no copy is in flight when the CTA leaves, whatever happened before)
-    if (__syncthreads_or(nst > 0 && !mbar_wait(MBAR, 0, kWaitCycles))) ok = false;
-    if (!ok) {
-      set_status(p.status, TV_ERR_TIMEOUT);
-    } else {
-      store_state<D>(tl + C::T_O, vrow ? mown + lrow * C::REC : nullptr, hf, m, lh);
-      __syncthreads();
-      // merge splits 0..cur in split order: weights 2^(m_s - max m), sums l_A + l_B
-      const int ns = cur + 1;
-      // O columns 4*c4 .. 4*c4+3 and (m, l_A, l_B) of split sp, row r
-      auto rec4 = [&](int sp, int r, int c4) -> float4 {
-        float4 v;
-        if (sp < nst || sp == cur) {
-          const uint32_t a = (sp < nst ? mst_s + static_cast<uint32_t>((sp * G + r) * C::REC * 4)
-                                       : mown_s + static_cast<uint32_t>(r * C::REC * 4)) + 16u * c4;
-          asm volatile("ld.shared.v4.f32 {%0, %1, %2, %3}, [%4];"
-                       : "=f"(v.x), "=f"(v.y), "=f"(v.z), "=f"(v.w)
-                       : "r"(a));
-        } else {
-          v = reinterpret_cast<const float4*>(ws_rec(p, s, g, sp, local * G + r, D))[c4];
-        }
-        return v;
-      };
-      float* wsm = reinterpret_cast<float*>(gb);                 // [ns][G] weights (tile area is free now)
-      float* ltot = wsm + static_cast<size_t>(ns) * G;           // [G]
-      const bool wstaged = (2 * static_cast<size_t>(ns) * G + 2 * G) * 4 <= 2 * C::TILE;
-      if (wstaged) {
-        // (m, l_A + l_B) of every (split, row), loaded in parallel
-        float* lsm = ltot + G;  // [ns][G]
-        for (int base = threadIdx.x; base < ns * G; base += 4 * blockDim.x) {
-          float mv4[4], la[4], lb[4];
-#pragma unroll
-          for (int u = 0; u < 4; u++) {
-            const int idx = base + u * blockDim.x;
-            if (idx < ns * G) {
-              const float4 t4 = rec4(idx / G, idx % G, D / 4);  // m, l_A, l_B, pad
-              mv4[u] = t4.x;
-              la[u] = t4.y;
-              lb[u] = t4.z;
-            }
-          }
-#pragma unroll
-          for (int u = 0; u < 4; u++) {
-            const int idx = base + u * blockDim.x;
-            if (idx < ns * G) {
-              wsm[idx] = mv4[u];
-              lsm[idx] = __fadd_rn(la[u], lb[u]);
-            }
-          }
-        }
-        __syncthreads();
-        // max reference per row, then every weight in parallel, then the sums in split order
-        float* mref = lsm + static_cast<size_t>(ns) * G;  // [G]
-        for (int r = threadIdx.x; r < G; r += blockDim.x) {
-          float mm = -INFINITY;
-#pragma unroll 8
-          for (int sp = 0; sp < ns; sp++) mm = fmaxf(mm, wsm[sp * G + r]);
-          mref[r] = mm;
-        }
-        __syncthreads();
-        for (int idx = threadIdx.x; idx < ns * G; idx += blockDim.x) {
-          const float ms = wsm[idx], mm = mref[idx % G];
-          wsm[idx] = (ms == mm) ? 1.f : ex2_approx(__fsub_rn(ms, mm));
-        }
-        __syncthreads();
-        for (int r = threadIdx.x; r < G; r += blockDim.x) {
-          float ls = 0.f;
-#pragma unroll 8
-          for (int sp = 0; sp < ns; sp++) ls = __fmaf_rn(wsm[sp * G + r], lsm[sp * G + r], ls);
-          ltot[r] = ls;
-        }
-        __syncthreads();
-      }
-      for (int idx = threadIdx.x; idx < G * (D / 4); idx += blockDim.x) {
-        const int r = idx / (D / 4), c4 = idx % (D / 4);
-        float mm = 0.f, ls = 0.f;
-        if (!wstaged) {
-          mm = -INFINITY;
-          for (int sp = 0; sp < ns; sp++) mm = fmaxf(mm, rec4(sp, r, D / 4).x);
-        }
-        float4 o = make_float4(0.f, 0.f, 0.f, 0.f);
-        if (wstaged && nst == cur) {
-          // every split's record is in shared memory (the common case): plain
-          // shared loads the compiler can batch, accumulated in split order
-          const float4* st4 = reinterpret_cast<const float4*>(gb + (C::TAIL_FIXED - 1024)) + r * (C::REC / 4) + c4;
-#pragma unroll 4
-          for (int sp = 0; sp < cur; sp++) {
-            const float4 v = st4[static_cast<size_t>(sp) * G * (C::REC / 4)];
-            const float wgt = wsm[sp * G + r];
-            o.x = __fmaf_rn(wgt, v.x, o.x);
-            o.y = __fmaf_rn(wgt, v.y, o.y);
-            o.z = __fmaf_rn(wgt, v.z, o.z);
-            o.w = __fmaf_rn(wgt, v.w, o.w);
-          }
-          {
-            const float4 v = reinterpret_cast<const float4*>(mown + r * C::REC)[c4];
-            const float wgt = wsm[cur * G + r];
-            o.x = __fmaf_rn(wgt, v.x, o.x);
-            o.y = __fmaf_rn(wgt, v.y, o.y);
-            o.z = __fmaf_rn(wgt, v.z, o.z);
-            o.w = __fmaf_rn(wgt, v.w, o.w);
-          }
-          ls = ltot[r];
-        } else if (wstaged) {
-          // up to 16 splits' partial rows in flight at a time, accumulated in split order
-          for (int sp0 = 0; sp0 < ns; sp0 += 16) {
-            float4 v[16];
-#pragma unroll
-            for (int u = 0; u < 16; u++)
-              if (sp0 + u < ns) v[u] = rec4(sp0 + u, r, c4);
-#pragma unroll
-            for (int u = 0; u < 16; u++) {
-              if (sp0 + u < ns) {
-                const float wgt = wsm[(sp0 + u) * G + r];
-                o.x = __fmaf_rn(wgt, v[u].x, o.x);
-                o.y = __fmaf_rn(wgt, v[u].y, o.y);
-                o.z = __fmaf_rn(wgt, v[u].z, o.z);
-                o.w = __fmaf_rn(wgt, v[u].w, o.w);
-              }
-            }
-          }
-          ls = ltot[r];
-        } else {
-          for (int sp = 0; sp < ns; sp++) {
-            const float4 t4 = rec4(sp, r, D / 4);
-            const float ms = t4.x;
-            const float wgt = (ms == mm) ? 1.f : ex2_approx(__fsub_rn(ms, mm));
-            ls = __fmaf_rn(wgt, __fadd_rn(t4.y, t4.z), ls);
-            const float4 v = rec4(sp, r, c4);
-            o.x = __fmaf_rn(wgt, v.x, o.x);
-            o.y = __fmaf_rn(wgt, v.y, o.y);
-            o.z = __fmaf_rn(wgt, v.z, o.z);
-            o.w = __fmaf_rn(wgt, v.w, o.w);
-          }
-        }
-        const size_t oi = (static_cast<size_t>(node_g) * p.Hq + g * G + r) * D + 4 * c4;
-        float4 y = make_float4(__fdiv_rn(o.x, ls), __fdiv_rn(o.y, ls), __fdiv_rn(o.z, ls), __fdiv_rn(o.w, ls));
-        if (p.gate) {
-          const uint2 gw = *reinterpret_cast<const uint2*>(p.gate + oi);
-          y = make_float4(gate_mul(y.x, bf16_lo(gw.x)), gate_mul(y.y, bf16_hi(gw.x)), gate_mul(y.z, bf16_lo(gw.y)),
-                          gate_mul(y.w, bf16_hi(gw.y)));
-        }
-        uint2 packed;
-        packed.x = pack_bf16x2(y.x, y.y);
-        packed.y = pack_bf16x2(y.z, y.w);
-        *reinterpret_cast<uint2*>(p.out + oi) = packed;
-      }
-      if (p.decode) {
-        // append the token's own key/value at row L
-        const size_t dst = (static_cast<size_t>(g) * p.cap + L) * D;
-        const size_t src = (static_cast<size_t>(node_g) * p.Hkv + g) * D;
-        for (int cc = threadIdx.x; cc < D / 8; cc += blockDim.x) {
-          reinterpret_cast<uint4*>(p.K[s] + dst)[cc] = reinterpret_cast<const uint4*>(p.kt + src)[cc];
-          reinterpret_cast<uint4*>(p.V[s] + dst)[cc] = reinterpret_cast<const uint4*>(p.vt + src)[cc];
-        }
-      }
-    }
-    if (threadIdx.x == 0) {
-      tc_commit(DRAIN);
-      mbar_wait(DRAIN, 0, kWaitCycles);
+    __syncthreads();
+    for (int idx = tid; idx < n_reg * G; idx += T::NT) wgt[idx] = weight(wgt[idx], ltot[idx % G]);
+    for (int r = tid; r < G; r += T::NT) wown[r] = weight(mown[r], ltot[r]);
+    __syncthreads();
+    for (int r = tid; r < G; r += T::NT) {
+      float ls = 0.f;
+      for (int i = 0; i < n_reg; i++) ls = __fmaf_rn(wgt[i * G + r], lsm[i * G + r], ls);
+      ltot[r] = __fmaf_rn(wown[r], lown[r], ls);
     }
   }
-  tc_fence_before();
-  __syncthreads();
-  tc_fence_after();
-  if (warp == 0) tmem_dealloc(tbase, C::COLS);
+  // the staged records have landed (every thread observes the barrier, and
+  // no copy is in flight when the CTA leaves, whatever happened before)
+  if (__syncthreads_or(nst > 0 && !mbar_wait(MBAR, 0, kWaitCycles))) {
+    if (tid == 0) set_status(p.status, TV_ERR_TIMEOUT);
+    return;
+  }
+  const float4* const st4 = reinterpret_cast<const float4*>(ob);
+  for (int idx = tid; idx < G * (D / 4); idx += T::NT) {
+    const int r = idx / (D / 4), c4 = idx % (D / 4);
+    float mm = 0.f, ls = 0.f, wo = 0.f;
+    if (!staged) {
+      mm = mown[r];
+      for (int i = 0; i < n_reg; i++) mm = fmaxf(mm, rec(i, r)[D]);
+      for (int i = 0; i < n_reg; i++) {
+        const float4 t4 = *reinterpret_cast<const float4*>(rec(i, r) + D);
+        ls = __fmaf_rn(weight(t4.x, mm), __fadd_rn(t4.y, t4.z), ls);
+      }
+      wo = weight(mown[r], mm);
+      ls = __fmaf_rn(wo, lown[r], ls);
+    } else {
+      ls = ltot[r];
+      wo = wown[r];
+    }
+    auto wt = [&](int i) { return staged ? wgt[i * G + r] : weight(rec(i, r)[D], mm); };
+    // records in order: the staged ones from shared memory (the first
+    // unstaged ones already in flight), then the rest MB at a time, then
+    // the own state
+    float4 o = make_float4(0.f, 0.f, 0.f, 0.f);
+    float4 v[T::MB];
+#pragma unroll
+    for (int u = 0; u < T::MB; u++)
+      if (nst + u < n_reg) v[u] = reinterpret_cast<const float4*>(rec(nst + u, r))[c4];
+#pragma unroll 4
+    for (int i = 0; i < nst; i++) {
+      const float4 x = st4[(i * G + r) * (T::REC / 16) + c4];
+      const float w = wt(i);
+      o.x = __fmaf_rn(w, x.x, o.x);
+      o.y = __fmaf_rn(w, x.y, o.y);
+      o.z = __fmaf_rn(w, x.z, o.z);
+      o.w = __fmaf_rn(w, x.w, o.w);
+    }
+    for (int i0 = nst; i0 < n_reg; i0 += T::MB) {
+      if (i0 > nst) {
+#pragma unroll
+        for (int u = 0; u < T::MB; u++)
+          if (i0 + u < n_reg) v[u] = reinterpret_cast<const float4*>(rec(i0 + u, r))[c4];
+      }
+#pragma unroll
+      for (int u = 0; u < T::MB; u++) {
+        if (i0 + u < n_reg) {
+          const float w = wt(i0 + u);
+          o.x = __fmaf_rn(w, v[u].x, o.x);
+          o.y = __fmaf_rn(w, v[u].y, o.y);
+          o.z = __fmaf_rn(w, v[u].z, o.z);
+          o.w = __fmaf_rn(w, v[u].w, o.w);
+        }
+      }
+    }
+    {
+      const float4 x = reinterpret_cast<const float4*>(oown + r * D)[c4];
+      o.x = __fmaf_rn(wo, x.x, o.x);
+      o.y = __fmaf_rn(wo, x.y, o.y);
+      o.z = __fmaf_rn(wo, x.z, o.z);
+      o.w = __fmaf_rn(wo, x.w, o.w);
+    }
+    const size_t oi = (static_cast<size_t>(node_g) * p.Hq + g * G + r) * D + 4 * c4;
+    float4 y = make_float4(__fdiv_rn(o.x, ls), __fdiv_rn(o.y, ls), __fdiv_rn(o.z, ls), __fdiv_rn(o.w, ls));
+    if (p.gate) {
+      const uint2 gw = *reinterpret_cast<const uint2*>(p.gate + oi);
+      y = make_float4(gate_mul(y.x, bf16_lo(gw.x)), gate_mul(y.y, bf16_hi(gw.x)), gate_mul(y.z, bf16_lo(gw.y)),
+                      gate_mul(y.w, bf16_hi(gw.y)));
+    }
+    uint2 packed;
+    packed.x = pack_bf16x2(y.x, y.y);
+    packed.y = pack_bf16x2(y.z, y.w);
+    *reinterpret_cast<uint2*>(p.out + oi) = packed;
+  }
+  if (p.decode) {
+    // append the token's own key/value at row L
+    const size_t dst = (static_cast<size_t>(g) * p.cap + ri.L) * D;
+    const size_t src = (static_cast<size_t>(node_g) * p.Hkv + g) * D;
+    for (int cc = tid; cc < D / 8; cc += T::NT) {
+      reinterpret_cast<uint4*>(p.K[ri.s] + dst)[cc] = reinterpret_cast<const uint4*>(p.kt + src)[cc];
+      reinterpret_cast<uint4*>(p.V[ri.s] + dst)[cc] = reinterpret_cast<const uint4*>(p.vt + src)[cc];
+    }
+  }
 }
 
 // ---------------------------------------------------------------------------
@@ -1160,26 +1211,41 @@ static int max_splits_for(int split_tiles, int max_len) {
   return (max_len + TV_MAX_PATH + split_tiles * kTile - 1) / (split_tiles * kTile) + 1;
 }
 
+// Workspace: per (sequence, KV head), max_splits split records and the
+// snapshot record, each [rows][O[D], m, l_A, l_B, pad].
 size_t attn_tc_ws_bytes(const tv_plan* plan, const tv_attn_layer* layer, int n_seq, int n_max, int max_len) {
   if (!plan || !layer || plan->split < kTile || plan->split % kTile) return 0;
   const int G = layer->Hq / (layer->Hkv > 0 ? layer->Hkv : 1);
-  const size_t splits = static_cast<size_t>(max_splits_for(plan->split / kTile, max_len));
-  return static_cast<size_t>(n_seq) * layer->Hkv * splits * static_cast<size_t>(n_max) * G * (layer->D + 4) * 4;
+  const size_t slots = static_cast<size_t>(max_splits_for(plan->split / kTile, max_len)) + 1;
+  return static_cast<size_t>(n_seq) * layer->Hkv * slots * static_cast<size_t>(n_max) * G * (layer->D + 4) * 4;
 }
 
 // Dynamic shared memory the tail kernel may use (the per-block limit less
-// its static arrays, with a margin).
+// its static arrays, with a margin), and the most that leaves room for two
+// tail CTAs on an SM.
 constexpr int kTailSmemMax = 232448 - 2048;
+constexpr int kTailSmemTwoPerSm = 112 * 1024;
 
 template <int D>
-static tv_status launch_tc(TcParams& p, int n_items_bound, int n_tail, cudaStream_t st, bool ov) {
+static tv_status launch_tc(TcParams& p, int n_items_bound, int n_units, cudaStream_t st, bool ov) {
   using C = Tc<D>;
-  // stage as many finished splits' states as fit next to the tail's tiles
-  const int per_split = p.G * C::REC * 4;
-  const int fit = (kTailSmemMax - C::TAIL_FIXED) / per_split - 1;  // less the node's own final split
-  if (fit < 0) return TV_ERR_SHAPE;
-  p.n_mstage = fit < p.max_splits ? fit : p.max_splits;
-  const int smem_tail = C::TAIL_FIXED + (p.n_mstage + 1) * per_split;
+  using T = Tail<D>;
+  p.ws_splits = p.max_splits + 1;
+  // weights and sums of every split record staged when they fit
+  const int wb = T::wbytes(p.G, p.max_splits);
+  p.tail_staged = T::a_off(p.G, wb) + T::own_bytes(p.G, false) <= kTailSmemMax ? 1 : 0;
+  p.tail_a = T::a_off(p.G, p.tail_staged ? wb : 0);
+  // keys and values staged at once while the tail CTAs fit one wave at one
+  // CTA per SM; otherwise one buffer, so that two CTAs share an SM
+  p.tail_two = (n_units <= num_sms() && p.tail_a + T::own_bytes(p.G, true) <= kTailSmemMax) ? 1 : 0;
+  const int base = p.tail_a + T::own_bytes(p.G, p.tail_two != 0);
+  if (base > kTailSmemMax) return TV_ERR_SHAPE;
+  const int cap = p.tail_two || base > kTailSmemTwoPerSm ? kTailSmemMax : kTailSmemTwoPerSm;
+  // split records staged for the merge: as many as the budget holds
+  const int rbytes = p.G * T::REC;
+  const int want = p.tail_a + p.max_splits * rbytes;
+  const int smem_tail = want > base ? (want < cap ? want : cap) : base;
+  p.n_mstage = (smem_tail - p.tail_a) / rbytes;
   // one-time attribute setup (never inside a stream capture after the first call)
   static bool attrs = false;
   if (!attrs) {
@@ -1196,7 +1262,7 @@ static tv_status launch_tc(TcParams& p, int n_items_bound, int n_tail, cudaStrea
     const int units = n_items_bound < num_sms() / per ? n_items_bound : num_sms() / per;
     launch_k(ov, attn_split_kernel<D>, dim3(per * units), dim3(384), C::SMEM_SPLIT, st, p);
   }
-  launch_k(ov, attn_tail_kernel<D>, dim3(n_tail), dim3(256), smem_tail, st, p);
+  launch_k(ov, attn_tail_kernel<D>, dim3(n_units), dim3(T::NT), smem_tail, st, p);
   return launch_status();
 }
 
@@ -1243,6 +1309,7 @@ tv_status attn_tc_launch(const tv_plan* plan, const AttnCall& a, void* ws, size_
   p.rows_max = n_max * G;
   p.decode = a.decode;
   p.c = a.scale * 1.4426950408889634f;
+  // the split kernel runs at most floor(max_len / 64) tiles of a sequence
   const int tiles_bound = a.max_len / kTile;
   const int splits_bound = (tiles_bound + p.split_tiles - 1) / p.split_tiles;
   // pair mode when the largest tree spans exactly two 128-row blocks (and a
@@ -1250,11 +1317,11 @@ tv_status attn_tc_launch(const tv_plan* plan, const AttnCall& a, void* ws, size_
   const int nrb_max = (n_max * G + 127) / 128;
   p.pair = (!a.decode && l->D >= 128 && nrb_max == 2) ? 1 : 0;
   const int items_bound = a.n_seq * l->Hkv * splits_bound * (p.pair ? 1 : nrb_max);
-  const int n_tail = (a.decode ? a.n_seq : a.n_total) * l->Hkv;
+  const int n_units = (a.decode ? a.n_seq : a.n_total) * l->Hkv;
   switch (l->D) {
-    case 64: return launch_tc<64>(p, items_bound, n_tail, st, a.overlap);
-    case 128: return launch_tc<128>(p, items_bound, n_tail, st, a.overlap);
-    case 256: return launch_tc<256>(p, items_bound, n_tail, st, a.overlap);
+    case 64: return launch_tc<64>(p, items_bound, n_units, st, a.overlap);
+    case 128: return launch_tc<128>(p, items_bound, n_units, st, a.overlap);
+    case 256: return launch_tc<256>(p, items_bound, n_units, st, a.overlap);
     default: return TV_ERR_SHAPE;
   }
 }

@@ -26,36 +26,8 @@
 
 namespace tv {
 
-typedef unsigned long long f2_t;  // two fp32 values in one 64-bit register
-
 constexpr int kPairs = 8;            // packed pairs of a row per lane (16 elements)
 constexpr int kChunks = kPairs / 4;  // chunks of 8 columns of a row per lane
-
-__device__ __forceinline__ f2_t f2_fma(f2_t a, f2_t b, f2_t c) {
-  f2_t d;
-  asm("fma.rn.f32x2 %0, %1, %2, %3;" : "=l"(d) : "l"(a), "l"(b), "l"(c));
-  return d;
-}
-__device__ __forceinline__ f2_t f2_mul(f2_t a, f2_t b) {
-  f2_t d;
-  asm("mul.rn.f32x2 %0, %1, %2;" : "=l"(d) : "l"(a), "l"(b));
-  return d;
-}
-__device__ __forceinline__ f2_t f2_add(f2_t a, f2_t b) {
-  f2_t d;
-  asm("add.rn.f32x2 %0, %1, %2;" : "=l"(d) : "l"(a), "l"(b));
-  return d;
-}
-__device__ __forceinline__ f2_t f2_dup(float x) {
-  f2_t d;
-  asm("mov.b64 %0, {%1, %1};" : "=l"(d) : "f"(x));
-  return d;
-}
-__device__ __forceinline__ float f2_hsum(f2_t a) {
-  float lo, hi;
-  asm("mov.b64 {%0, %1}, %2;" : "=f"(lo), "=f"(hi) : "l"(a));
-  return __fadd_rn(lo, hi);
-}
 
 template <int LPR>
 __device__ __forceinline__ float group_sum(float x) {

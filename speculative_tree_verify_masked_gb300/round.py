@@ -32,10 +32,12 @@ def auto_split(ctx_lens, n_nodes, Hq, Hkv, num_sms, lo=512, hi=16384):
         st = split // TILE
         costs = []
         for L, n in zip(ctx_lens, n_nodes):
-            tsh = L // TILE
+            # the split kernel's tiles: below the own segment of the deepest
+            # possible row, one tile back from its last position's tile
+            tend = max((L + min(n - 1, B.TV_MAX_PATH - 1)) // TILE - 1, 0)
             nrb = -(-n * G // 128)
-            for sp in range(-(-tsh // st)):
-                c = min(st, tsh - sp * st) + 4
+            for sp in range(-(-tend // st)):
+                c = min(st, tend - sp * st) + 4
                 costs += [c] * (Hkv * nrb)
         loads = [0] * num_sms
         for w, c in enumerate(costs):

@@ -86,12 +86,13 @@ def _bf16_layer(Hq=24, Hkv=4, D=256, cap=4096, n_seq=1):
 
 
 def test_workspace_size_formula(L):
-    """Per KV head, split and query row one record of D + 4 fp32 values."""
+    """Per KV head and query row one record of D + 4 fp32 values for each
+    split and one for the last split's snapshot."""
     layer, keep = _bf16_layer()
     pl = B.tv_plan(512)
     n_seq, n_max, max_len = 2, 16, 4000
     splits = (max_len + 16 + 512 - 1) // 512 + 1
-    want = n_seq * 4 * splits * n_max * 6 * (256 + 4) * 4
+    want = n_seq * 4 * (splits + 1) * n_max * 6 * (256 + 4) * 4
     assert L.tv_attn_workspace_bytes(ctypes.byref(pl), ctypes.byref(layer), n_seq, n_max, max_len) == want
     bad = B.tv_plan(100)  # not a multiple of 64
     assert L.tv_attn_workspace_bytes(ctypes.byref(bad), ctypes.byref(layer), n_seq, n_max, max_len) == 0
