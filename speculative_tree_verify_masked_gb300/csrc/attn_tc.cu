@@ -88,7 +88,7 @@ struct Tc {
   static constexpr uint32_t IDESC_QK = idesc_bf16_f32(128, kTile, false, false);
   static constexpr uint32_t IDESC_PV = idesc_bf16_f32(128, D, false, true);
   static constexpr int RING = (NK + NV) * TILE + NP * PTILE;
-  static constexpr int NBAR = 2 * (NK + NV) + 2 * NP + 9;
+  static constexpr int NBAR = 2 * (NK + NV) + 2 * NP + 15;
   static constexpr int SMEM_SPLIT = 1024 + RING + NBAR * 8 + 16;
 };
 
@@ -484,7 +484,7 @@ __global__ void __launch_bounds__(384, 1) attn_split_kernel(const __grid_constan
   const uint32_t PFULL0 = SFREE0 + 16u, ODONE0 = PFULL0 + 8u * C::NP;
   const uint32_t QREADY = ODONE0 + 8u * C::NP;
   const uint32_t DRAIN = QREADY + 8u;  // [2] one per MMA warp
-  const uint32_t XBAR0 = DRAIN + 16u;  // [2] half-max exchange, by tile parity
+  const uint32_t XBAR0 = DRAIN + 16u;  // [2][4] half-max exchange, by tile parity and row quarter
   const uint32_t kring = sb, vring = sb + C::NK * C::TILE, pring = vring + C::NV * C::TILE;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   // Pair mode: CTAs 2c and 2c+1 run row blocks 0 and 1 of the same items,
@@ -508,7 +508,7 @@ __global__ void __launch_bounds__(384, 1) attn_split_kernel(const __grid_constan
     for (int b = 0; b < 2; b++) {
       mbar_init(SFULL0 + 8u * b, 1);
       mbar_init(SFREE0 + 8u * b, 256);
-      mbar_init(XBAR0 + 8u * b, 256);
+      for (int q = 0; q < 4; q++) mbar_init(XBAR0 + 8u * (b * 4 + q), 64);  // the two warps of a row quarter
     }
     for (int i = 0; i < C::NP; i++) {
       mbar_init(PFULL0 + 8u * i, 256);
@@ -691,23 +691,25 @@ __global__ void __launch_bounds__(384, 1) attn_split_kernel(const __grid_constan
           // The state one tile before the split's end, for the rows whose own
           // segment starts at this tile: O once PV of the previous tile is
           // complete, with m and the sums before this tile.  Every PV so far
-          // is then complete, so the P ring is free until this tile's P,
-          // which no warp writes before the half-max exchange below.
+          // is then complete, so the two P slots other than this tile's are
+          // free (the next item's P waits for every softmax warp's queries):
+          // warp (half, quarter) turns its rows around in 4 KB of them.
           const uint32_t tp = t - 1;
           if (!wait_warp(ODONE0 + 8u * (tp % C::NP), (tp / C::NP) & 1, abort_flag, kWaitCycles)) {
             ok = false;
             break;
           }
           tc_fence_after();
-          store_state_warp<D>(tl + C::T_O, pring + static_cast<uint32_t>(warp - 2) * 4096u, hf, lane, m, lh,
+          const uint32_t xbuf = pring + ((t + 1 + hf) % C::NP) * C::PTILE + static_cast<uint32_t>(quad) * 4096u;
+          store_state_warp<D>(tl + C::T_O, xbuf, hf, lane, m, lh,
                               [&](int r) -> float* {
                                 return rbase + r < nrows ? ws_rec(p, I.s, I.g, snap_slot(p), rbase + r, D) : nullptr;
                               });
         }
         const float mh = half_max(sv, kHalf);
         xmax[b][hf][lrow] = mh;
-        mbar_arrive(XBAR0 + 8u * b);
-        if (!wait_warp(XBAR0 + 8u * b, (t >> 1) & 1, abort_flag, kWaitCycles)) {
+        mbar_arrive(XBAR0 + 8u * (b * 4 + quad));
+        if (!wait_warp(XBAR0 + 8u * (b * 4 + quad), (t >> 1) & 1, abort_flag, kWaitCycles)) {
           ok = false;
           break;
         }
