@@ -141,6 +141,7 @@ def small_workload(cfg_id, shapes, ctx_lens, tree_kinds, accept=None):
 SH128 = synth.Shapes(Hq=8, Hkv=2, D=128, Hk=2, Hv=4, dk=64, dv=64, kv_dtype=torch.bfloat16)
 SH64 = synth.Shapes(Hq=4, Hkv=1, D=64, Hk=1, Hv=2, dk=128, dv=100, kv_dtype=torch.bfloat16)
 SHF = synth.Shapes(Hq=6, Hkv=2, D=128, Hk=2, Hv=6, dk=128, dv=128, kv_dtype=torch.float32)
+SHG64 = synth.Shapes(Hq=64, Hkv=1, D=64, Hk=1, Hv=2, dk=64, dv=64, kv_dtype=torch.bfloat16)  # largest group
 
 EDGES = [
     # (name, shapes, context lengths, trees, split)
@@ -159,6 +160,14 @@ EDGES = [
     ("D128", SH128, [1500, 70], [("merged", 30, 10), ("merged", 9, 5)], 512),
     ("D64", SH64, [900], [("merged", 40, 16)], 256),
     ("f32-D128", SHF, [300, 5], [("merged", 20, 8), ("chain", 4)], 4096),
+    # the root's row starts its own segment one tile before the deeper rows,
+    # which read the last split's snapshot in place of its final state
+    ("snapshot-D128", SH128, [191], [("chain", 16)], 512),
+    ("snapshot-D64", SH64, [447], [("merged", 20, 8)], 256),
+    # more split records than the tail stages in shared memory (the rest read
+    # from global memory), and so many that not even their weights are staged
+    ("many-splits", synth.SHAPES_27B, [3000], [("merged", 8, 4)], 64),
+    ("unstaged-weights", SHG64, [18_000], [("chain", 2)], 64),
 ]
 
 
