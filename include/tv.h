@@ -120,8 +120,8 @@ typedef struct {
  * at exit, so everything older than the predecessor has completed.  Before
  * waiting, a kernel reads only the recurrent states (GDN verify; GDN commit,
  * whose predecessor is always a kernel of the same commit call), the lengths
- * and node_off (attention; the split kernel also prefetches K/V tiles into
- * L2, which is only a cache hint), and the tree tables, the query rows, the
+ * and node_off (attention; the split kernel also prefetches K/V tiles and
+ * its first query rows into L2, which is only a cache hint), and the tree tables, the query rows, the
  * tree's K/V rows and the cache rows of its own segment (the attention tail,
  * whose predecessor is always its own split kernel, and which computes the
  * node's own segment before waiting); no kernel of a verify round (prepare,

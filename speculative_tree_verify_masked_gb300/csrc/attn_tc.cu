@@ -530,16 +530,25 @@ __global__ void __launch_bounds__(384, 1) attn_split_kernel(const __grid_constan
   tc_fence_after();
   const uint32_t tbase = *tmem_slot;
   const int total = is.cum[p.n_seq];
-  // L2 prefetch of the first item's first tiles while the previous kernel
-  // finishes: a prefetch only warms L2 (the point of coherence), so it is
-  // safe whatever the previous kernel writes, and the ring's first loads
-  // then hit L2.
+  // L2 prefetch of the first item's first tiles and query rows while the
+  // previous kernel finishes: a prefetch only warms L2 (the point of
+  // coherence), so it is safe whatever the previous kernel writes, and the
+  // ring's first loads and the first queries then hit L2.
   if ((warp == 0 || warp == 10) && lane == 0 && cid < total) {
     const Item I = item_at(is, p, cid, rank);
     const CUtensorMap* maps = warp == 0 ? p.tmK : p.tmV;
     const int nfirst = min(I.t1 - I.t0, (warp == 0 ? C::NK : C::NV) + kL2Ahead);
     for (int t = I.t0; t < I.t0 + nfirst; t++)
       for (int kb = kb0; kb < kb1; kb++) tma_prefetch_l2_2d(&maps[I.s], kb * 64, I.g * p.cap + t * kTile);
+  }
+  if (warp >= 2 && warp <= 9 && cid < total) {
+    const Item I = item_at(is, p, cid, rank);
+    const int row = I.rb * 128 + (warp & 3) * 32 + lane, hq = (warp - 2) >> 2;
+    if (row < is.rows[I.s]) {
+      const char* qr = reinterpret_cast<const char*>(
+          p.q + (static_cast<size_t>(is.off[I.s] + row / p.G) * p.Hq + I.g * p.G + row % p.G) * D);
+      for (int b = hq * (D * 2 / 2); b < (hq + 1) * (D * 2 / 2); b += 128) prefetch_l2(qr + b);
+    }
   }
   pdl_wait();  // queries, status and the workspace (read by the previous tail) from here on
   pdl_trigger();

@@ -281,6 +281,10 @@ __device__ __forceinline__ void tmem_st_wait() {
   asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory");
 }
 
+// Fetch the 128-byte line holding p into L2 (a cache hint; no data returned).
+__device__ __forceinline__ void prefetch_l2(const void* p) {
+  asm volatile("prefetch.global.L2 [%0];" ::"l"(p) : "memory");
+}
 // Fetch one box of a tensor into L2 ahead of its TMA load (no completion
 // signal, no shared memory): more DRAM requests in flight than the ring holds.
 __device__ __forceinline__ void tma_prefetch_l2_2d(const CUtensorMap* map, int x, int y) {
