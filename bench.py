@@ -83,9 +83,9 @@ def round_bytes(cfg, n_nodes_per_seq, acc_lens):
 # is dropped whenever the kernels change and stays absent (reported as null)
 # until it is captured again.
 MEASURED_TRAFFIC: dict[str, int] = {
-    # one attention layer of the stack (bench.py --layers 3): split 537,512,960 read + 2,993,664 written,
+    # one attention layer of the stack (bench.py --layers 3): split 537,728,256 read + 2,998,016 written,
     # tail 16,038,912 read; the same kernels and launch as every attention layer of the full round
-    "64-layer mixer stack (48 GDN + 16 attention), L 131072, 32-node tree": 537512960 + 2993664 + 16038912,
+    "64-layer mixer stack (48 GDN + 16 attention), L 131072, 32-node tree": 537728256 + 2998016 + 16038912,
 }
 
 
