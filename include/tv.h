@@ -116,8 +116,9 @@ typedef struct {
  * tensor-memory setup, loads of the recurrent state, work that needs nothing
  * from its predecessor) while the kernel before it on the stream finishes.
  * A kernel lets the next one in right after its own wait for its
- * predecessor has returned (the attention split kernel and GDN verify), or
- * at exit, so everything older than the predecessor has completed.  Before
+ * predecessor has returned (the attention split and tail kernels, GDN
+ * verify), or at exit, so everything older than the predecessor has
+ * completed.  Before
  * waiting, a kernel reads only the recurrent states (GDN verify; GDN commit,
  * whose predecessor is always a kernel of the same commit call), the lengths
  * and node_off (attention; the split kernel also prefetches K/V tiles and

@@ -1041,6 +1041,7 @@ __global__ void __launch_bounds__(512, 2) attn_tail_kernel(const __grid_constant
   }
   // the split kernel before this one writes the workspace and may set the status
   pdl_wait();
+  pdl_trigger();  // the next kernel may start on SMs this grid leaves free
   if (tid == 0) {
     int bad = status_bad(p.status) ? 1 : 0;
     if (!bad && (ri.L < 0 || ri.L > p.max_len)) {
