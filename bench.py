@@ -83,9 +83,9 @@ def round_bytes(cfg, n_nodes_per_seq, acc_lens):
 # is dropped whenever the kernels change and stays absent (reported as null)
 # until it is captured again.
 MEASURED_TRAFFIC: dict[str, int] = {
-    # one attention layer of the stack (bench.py --layers 3): split 537,728,256 read + 2,998,016 written,
-    # tail 16,038,912 read; the same kernels and launch as every attention layer of the full round
-    "64-layer mixer stack (48 GDN + 16 attention), L 131072, 32-node tree": 537728256 + 2998016 + 16038912,
+    # one attention layer of the stack (bench.py --layers 3): split 538,193,664 read + 2,713,344 written,
+    # tail 16,039,424 read; the same kernels and launch as every attention layer of the full round
+    "64-layer mixer stack (48 GDN + 16 attention), L 131072, 32-node tree": 538193664 + 2713344 + 16039424,
 }
 
 
