@@ -333,6 +333,22 @@ tv_status tv_gdn_front(const tv_gdn_front_layer* layer, const tv_tree* tree, int
 tv_status tv_gdn_out_norm(const tv_gdn_front_layer* layer, int32_t rows, const void* o, const void* z,
                           const float* w_norm, void* out, tv_stream stream);
 
+/* tv_gdn_front, tv_gdn_tree_verify and tv_gdn_out_norm in two launches: the
+ * verify kernel forms each node's query, key, value and gates from the raw
+ * projections inside its staging (no q, k, v, alpha or beta in memory), runs
+ * the recurrence, writes o to out; a second kernel applies the gated norm to
+ * out in place (the norm of a (node, value head) needs all dv rows, which
+ * two verify CTAs share).  The result equals the three calls bit for bit.
+ *  layer  tv_gdn_tree_verify's layer (states updated the same way: none)
+ *  front  the front-end layer: same dtype, Hk, Hv, dk, dv
+ *  x [n_total][C], a_raw, b_raw [n_total][Hv], z [n_total][Hv][dv], w_norm [dv]
+ *  out    [n_total][Hv][dv], 16-byte aligned
+ * Errors as tv_gdn_tree_verify's and tv_gdn_front's; TV_ERR_SHAPE when the two
+ * layers disagree.  The tails are read only. */
+tv_status tv_gdn_tree_verify_fused(const tv_gdn_layer* layer, const tv_gdn_front_layer* front, const tv_tree* tree,
+                                   const void* x, const float* a_raw, const float* b_raw, const void* z,
+                                   const float* w_norm, void* out, float scale, tv_stream stream);
+
 /* Commit of the convolution tails: each sequence's tail becomes the last W-1
  * of (tail, x[path[0..a-1]]) for the accepted path of tv_accept_path (tree),
  * or of (tail, x[s]) for a decoded token (tree NULL, n_seq tokens).  Run it

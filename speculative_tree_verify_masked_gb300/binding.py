@@ -112,6 +112,8 @@ def lib():
         L.tv_gdn_front.argtypes = [F, T, c_int32, vp, vp, vp, vp, vp, vp, vp, vp, vp, vp]
         L.tv_gdn_out_norm.restype = c_int32
         L.tv_gdn_out_norm.argtypes = [F, c_int32, vp, vp, vp, vp, vp]
+        L.tv_gdn_tree_verify_fused.restype = c_int32
+        L.tv_gdn_tree_verify_fused.argtypes = [G, F, T, vp, vp, vp, vp, vp, vp, c_float, vp]
         L.tv_gdn_conv_commit.restype = c_int32
         L.tv_gdn_conv_commit.argtypes = [F, T, c_int32, vp, vp, vp, vp, vp]
         L.tv_kvpool_page_bytes.restype = c_size_t
@@ -142,7 +144,7 @@ EXPORTED = ["tv_status_string", "tv_version", "tv_tree_meta_bytes", "tv_tree_pre
             "tv_kvpool_create", "tv_kvpool_reserve", "tv_kvpool_commit_rows", "tv_kvpool_release_rows",
             "tv_kvpool_committed_bytes", "tv_kvpool_reserved_bytes", "tv_kvpool_destroy", "tv_attn_rope",
             "tv_attn_tree_verify_gated", "tv_attn_decode_gated", "tv_gdn_front", "tv_gdn_out_norm",
-            "tv_gdn_conv_commit", "tv_wait_selftest"]
+            "tv_gdn_conv_commit", "tv_gdn_tree_verify_fused", "tv_wait_selftest"]
 
 
 def _check(code: int, where: str):
@@ -330,6 +332,13 @@ def tv_gdn_tree_verify(layer: GdnLayer, tree: Tree, q, k, v, alpha, beta, out, s
     _check(lib().tv_gdn_tree_verify(ctypes.byref(layer.c), ctypes.byref(tree.c), _ptr(q), _ptr(k), _ptr(v),
                                     _ptr(alpha), _ptr(beta), _ptr(out), scale, _stream(stream)),
            "tv_gdn_tree_verify")
+
+
+def tv_gdn_tree_verify_fused(layer: GdnLayer, front: GdnFrontLayer, tree: Tree, x, a_raw, b_raw, z, w_norm, out,
+                             scale, stream=None):
+    _check(lib().tv_gdn_tree_verify_fused(ctypes.byref(layer.c), ctypes.byref(front.c), ctypes.byref(tree.c), _ptr(x),
+                                          _ptr(a_raw), _ptr(b_raw), _ptr(z), _ptr(w_norm), _ptr(out), scale,
+                                          _stream(stream)), "tv_gdn_tree_verify_fused")
 
 
 def tv_accept_path(tree: Tree, tok, greedy, path, acc_len, bonus, stream=None):

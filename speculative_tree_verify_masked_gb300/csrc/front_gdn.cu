@@ -20,14 +20,11 @@
 #include <cmath>
 
 #include "common.cuh"
+#include "front_gdn.cuh"
 #include "host.hpp"
+#include "launchers.hpp"
 
 namespace tv {
-
-constexpr float kNormEps = 1e-6f;
-constexpr int kMaxConvWidth = 8;
-
-__device__ __forceinline__ float silu_f(float x) { return __fdiv_rn(x, __fadd_rn(1.f, expf(-x))); }
 
 struct GdnFrontParams {
   const void* x;
@@ -58,12 +55,7 @@ __global__ void __launch_bounds__(128) gdn_front_kernel(const GdnFrontParams p) 
   if (warp >= p.n_rows * units) {
     // gates: one thread per (row, value head)
     const int gi = (warp - p.n_rows * units) * 32 + lane;
-    if (gi < p.n_rows * p.Hv) {
-      const float a = p.a_raw[gi], b = p.b_raw[gi];
-      const float sp = a > 20.f ? a : log1pf(expf(a));
-      p.alpha[gi] = expf(-sp);
-      p.beta[gi] = __fdiv_rn(1.f, __fadd_rn(1.f, expf(-b)));
-    }
+    if (gi < p.n_rows * p.Hv) front_gates(p.a_raw[gi], p.b_raw[gi], p.alpha[gi], p.beta[gi]);
     return;
   }
   const int row = warp / units, u = warp % units;
@@ -82,33 +74,14 @@ __global__ void __launch_bounds__(128) gdn_front_kernel(const GdnFrontParams p) 
   const T* tail = static_cast<const T*>(p.tail[s]);
   // the rows of the window: node rows (global) or tail rows (negative: -1 - r)
   int src[kMaxConvWidth];
-#pragma unroll
-  for (int j = 0; j < kMaxConvWidth; j++) {
-    if (j < p.W) {
-      const int m = depth + j - (p.W - 1);
-      src[j] = m >= 0 ? (p.decode ? row : off + anc[m]) : -1 - (depth + j);
-    }
-  }
+  conv_window(src, p.W, depth, off, anc, row);
   float val[CPL];
-  float ss = 0.f;
 #pragma unroll
-  for (int e = 0; e < CPL; e++) {
-    const int c = c0 + lane + 32 * e;
-    float acc = 0.f;
-    for (int j = 0; j < p.W; j++) {
-      const float xin = src[j] >= 0 ? to_f32(x[static_cast<size_t>(src[j]) * C + c])
-                                    : to_f32(tail[static_cast<size_t>(-1 - src[j]) * C + c]);
-      acc = __fmaf_rn(p.wconv[static_cast<size_t>(c) * p.W + j], xin, acc);
-    }
-    val[e] = silu_f(acc);
-    ss = __fmaf_rn(val[e], val[e], ss);
-  }
+  for (int e = 0; e < CPL; e++) val[e] = conv_silu(x, tail, p.wconv, C, p.W, src, c0 + lane + 32 * e);
   T* dst;
   float scale = 1.f;
   if (u < 2 * p.Hk) {
-#pragma unroll
-    for (int o = 16; o >= 1; o >>= 1) ss = __fadd_rn(ss, __shfl_xor_sync(0xffffffffu, ss, o));
-    scale = __fdiv_rn(1.f, __fsqrt_rn(__fadd_rn(ss, kNormEps)));
+    scale = warp_l2_scale<CPL>(val);
     const int hk = u < p.Hk ? u : u - p.Hk;
     dst = static_cast<T*>(u < p.Hk ? p.q : p.k) + (static_cast<size_t>(row) * p.Hk + hk) * p.dk;
   } else {

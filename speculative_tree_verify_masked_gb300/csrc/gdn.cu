@@ -27,6 +27,7 @@
 // staged copy of the tree's inputs; leaves skip the update (nothing reads
 // their state).
 #include "common.cuh"
+#include "front_gdn.cuh"
 #include "gdn_step.cuh"
 #include "host.hpp"
 #include "launchers.hpp"
@@ -45,6 +46,14 @@ struct GdnVerifyParams {
   int32_t* status;
   int n_total, n_max, n_slots, Hk, Hv, dv;
   float scale;
+  // front end of the fused verify: raw projections [n_total][C], raw gates
+  // [n_total][Hv], convolution weights [C][W] and each sequence's tail [W-1][C]
+  const void* x;
+  const float* a_raw;
+  const float* b_raw;
+  const float* wconv;
+  const void* tail[TV_MAX_SEQ];
+  int C, W;
 };
 
 // Slots for states that must outlive a subtree: at most floor(log2(n / 5)) + 1
@@ -104,7 +113,7 @@ __device__ __forceinline__ void load_vals(float (&v)[N], const float* src) {
   }
 }
 
-template <typename T, int LPR, int RPG, int WARPS>
+template <typename T, int LPR, int RPG, int WARPS, bool FRONT>
 __global__ void __launch_bounds__(32 * WARPS) gdn_verify_kernel(const GdnVerifyParams p) {
   using KQ = T;
   using Sh = GdnShape<LPR, RPG, WARPS>;
@@ -156,6 +165,53 @@ __global__ void __launch_bounds__(32 * WARPS) gdn_verify_kernel(const GdnVerifyP
   int* sch = reinterpret_cast<int*>(vb + static_cast<size_t>(p.n_max) * R);          // [n_max] visits
   int* sgt = sch + p.n_max;                                                           // [n_max] segments
 
+  if constexpr (FRONT) {
+    // The front end, as tv_gdn_front forms it (front_gdn.cuh): this key
+    // head's query and key of every node (one warp per node and vector:
+    // convolution along the node's ancestor path into the committed tail,
+    // SiLU, division by the head's L2 norm, rounding to the layer type), the
+    // values of this CTA's rows (convolution, SiLU, rounding) and the gates.
+    const T* x = static_cast<const T*>(p.x);
+    const T* tail = static_cast<const T*>(p.tail[s]);
+    const int warp = tid >> 5, lane = tid & 31;
+    constexpr int CPL = DK / 32;
+    auto window = [&](int node, int (&src)[kMaxConvWidth]) {
+      const int row = off + node;
+      conv_window(src, p.W, mv.depth[row], off, mv.anc_at + static_cast<size_t>(row) * TV_MAX_PATH, row);
+    };
+    for (int w = warp; w < 2 * n; w += WARPS) {
+      const int node = w >> 1, is_k = w & 1;
+      int src[kMaxConvWidth];
+      window(node, src);
+      const int c0 = (is_k ? p.Hk + g : g) * DK;
+      float val[CPL];
+#pragma unroll
+      for (int e = 0; e < CPL; e++) val[e] = conv_silu(x, tail, p.wconv, p.C, p.W, src, c0 + lane + 32 * e);
+      const float sc = warp_l2_scale<CPL>(val);
+      KQ* dst = (is_k ? kb : qb) + static_cast<size_t>(node) * DK;
+#pragma unroll
+      for (int e = 0; e < CPL; e++) dst[lane + 32 * e] = from_f32<KQ>(__fmul_rn(val[e], sc));
+    }
+    for (int idx = tid; idx < n * R; idx += NT) {
+      const int node = idx / R, rr = rb * R + idx % R;
+      float vv = 0.f;
+      if (rr < p.dv) {
+        int src[kMaxConvWidth];
+        window(node, src);
+        vv = to_f32(from_f32<T>(conv_silu(x, tail, p.wconv, p.C, p.W, src, 2 * p.Hk * DK + h * p.dv + rr)));
+      }
+      vb[idx] = vv;
+    }
+    for (int idx = tid; idx < n; idx += NT) {
+      const size_t ah = static_cast<size_t>(off + idx) * p.Hv + h;
+      float a, b;
+      front_gates(p.a_raw[ah], p.b_raw[ah], a, b);
+      nc[idx] = make_float4(a, b, 0.f, 0.f);
+      sch[idx] = mv.sched[off + idx];
+      sgt[idx] = mv.seg[off + idx];
+    }
+    __syncthreads();
+  } else {
   // Stage the tree's keys and queries of this key head (cp.async), the
   // values of this CTA's rows, alpha, beta and the steps.  Every global load
   // goes into registers (or a cp.async) before any shared-memory store, so
@@ -212,6 +268,7 @@ __global__ void __launch_bounds__(32 * WARPS) gdn_verify_kernel(const GdnVerifyP
     }
     asm volatile("cp.async.wait_all;" ::: "memory");
     __syncthreads();
+  }
   }
   // k . q of every node, one node per lane group at a time (warp-uniform
   // trip count, so every lane of a warp takes part in each butterfly)
@@ -388,11 +445,11 @@ static bool gdn_shape_ok(const tv_gdn_layer* l) {
          (l->dk == 64 || l->dk == 128) && l->dv >= 1 && l->dv <= 256 && l->S;
 }
 
-template <typename T, int LPR, int WARPS>
+template <typename T, int LPR, int WARPS, bool FRONT>
 static void launch_verify_w(const GdnVerifyParams& p, int n_seq, cudaStream_t st, bool ov) {
   using Sh = GdnShape<LPR, kGdnRpg, WARPS>;
   constexpr int R = Sh::R;
-  auto kern = gdn_verify_kernel<T, LPR, kGdnRpg, WARPS>;
+  auto kern = gdn_verify_kernel<T, LPR, kGdnRpg, WARPS, FRONT>;
   static bool attrs = false;  // one-time, sized for the largest tree
   if (!attrs) {
     const int smem_max = static_cast<int>(gdn_verify_smem<T, Sh>(TV_MAX_NODES, slots_for(TV_MAX_NODES)));
@@ -402,12 +459,12 @@ static void launch_verify_w(const GdnVerifyParams& p, int n_seq, cudaStream_t st
   const dim3 grid(p.Hv * ((p.dv + R - 1) / R), n_seq);
   launch_k(ov, kern, grid, dim3(32 * WARPS), gdn_verify_smem<T, Sh>(p.n_max, p.n_slots), st, p);
 }
-template <typename T, int LPR>
+template <typename T, int LPR, bool FRONT>
 static void launch_verify(const GdnVerifyParams& p, int n_seq, cudaStream_t st, bool ov) {
   constexpr int R4 = GdnShape<LPR, kGdnRpg, 4>::R;
   const long long ctas4 = static_cast<long long>(p.Hv) * ((p.dv + R4 - 1) / R4) * n_seq;
-  if (ctas4 <= 2LL * num_sms()) launch_verify_w<T, LPR, 8>(p, n_seq, st, ov);
-  else launch_verify_w<T, LPR, 4>(p, n_seq, st, ov);
+  if (ctas4 <= 2LL * num_sms()) launch_verify_w<T, LPR, 8, FRONT>(p, n_seq, st, ov);
+  else launch_verify_w<T, LPR, 4, FRONT>(p, n_seq, st, ov);
 }
 
 template <typename T, int LPR>
@@ -472,10 +529,56 @@ extern "C" tv_status tv_gdn_tree_verify(const tv_gdn_layer* l, const tv_tree* t,
   const bool ov = tree_overlap(t);
   if (l->dk == 128) {
     constexpr int LPR = lanes_per_row<128>();
-    if (bf) launch_verify<__nv_bfloat16, LPR>(p, t->n_seq, st, ov); else launch_verify<float, LPR>(p, t->n_seq, st, ov);
+    if (bf) launch_verify<__nv_bfloat16, LPR, false>(p, t->n_seq, st, ov); else launch_verify<float, LPR, false>(p, t->n_seq, st, ov);
   } else {
     constexpr int LPR = lanes_per_row<64>();
-    if (bf) launch_verify<__nv_bfloat16, LPR>(p, t->n_seq, st, ov); else launch_verify<float, LPR>(p, t->n_seq, st, ov);
+    if (bf) launch_verify<__nv_bfloat16, LPR, false>(p, t->n_seq, st, ov); else launch_verify<float, LPR, false>(p, t->n_seq, st, ov);
   }
   return launch_status();
+}
+
+// The fused form: the front end computed inside the verify kernel from the
+// raw projections (no q, k, v, alpha or beta in memory), then the gated RMS
+// norm of the outputs in place.  The norm needs all dv rows of a (node,
+// value head), which two CTAs of the verify kernel share, so it is a second
+// kernel over `out`.
+extern "C" tv_status tv_gdn_tree_verify_fused(const tv_gdn_layer* l, const tv_gdn_front_layer* f, const tv_tree* t,
+                                              const void* x, const float* a_raw, const float* b_raw, const void* z,
+                                              const float* w_norm, void* out, float scale, tv_stream stream) {
+  if (!tree_ok(t)) return TV_ERR_ARG;
+  if (!l || !l->S || !f) return TV_ERR_ARG;
+  if (l->dtype != TV_F32 && l->dtype != TV_BF16) return TV_ERR_DTYPE;
+  if (!gdn_shape_ok(l) || !front_layer_ok(f)) return TV_ERR_SHAPE;
+  if (f->dtype != l->dtype || f->Hk != l->Hk || f->Hv != l->Hv || f->dk != l->dk || f->dv != l->dv)
+    return TV_ERR_SHAPE;
+  if (!x || !a_raw || !b_raw || !z || !w_norm || !out) return TV_ERR_ARG;
+  if (!aligned16(out)) return TV_ERR_ALIGN;
+  GdnVerifyParams p{};
+  for (int s = 0; s < t->n_seq; s++) {
+    if (!l->S[s]) return TV_ERR_ARG;
+    if (!aligned16(l->S[s])) return TV_ERR_ALIGN;
+    if (f->width > 1 && !f->tail[s]) return TV_ERR_ARG;
+    p.S[s] = l->S[s];
+    p.tail[s] = f->tail[s];
+  }
+  p.out = out;
+  p.meta = t->meta; p.status = t->status;
+  p.n_total = t->n_total; p.n_max = t->n_max; p.n_slots = slots_for(t->n_max);
+  p.Hk = l->Hk; p.Hv = l->Hv; p.dv = l->dv; p.scale = scale;
+  p.x = x; p.a_raw = a_raw; p.b_raw = b_raw; p.wconv = f->wconv;
+  p.C = 2 * l->Hk * l->dk + l->Hv * l->dv;
+  p.W = f->width;
+  cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
+  const bool bf = l->dtype == TV_BF16;
+  const bool ov = tree_overlap(t);
+  if (l->dk == 128) {
+    constexpr int LPR = lanes_per_row<128>();
+    if (bf) launch_verify<__nv_bfloat16, LPR, true>(p, t->n_seq, st, ov); else launch_verify<float, LPR, true>(p, t->n_seq, st, ov);
+  } else {
+    constexpr int LPR = lanes_per_row<64>();
+    if (bf) launch_verify<__nv_bfloat16, LPR, true>(p, t->n_seq, st, ov); else launch_verify<float, LPR, true>(p, t->n_seq, st, ov);
+  }
+  const tv_status ls = launch_status();
+  if (ls != TV_OK) return ls;
+  return tv_gdn_out_norm(f, t->n_total, out, z, w_norm, out, stream);
 }

@@ -33,6 +33,9 @@ tv_status attn_f32_launch(const AttnCall& c, cudaStream_t st);
 tv_status attn_tc_launch(const tv_plan* plan, const AttnCall& c, void* ws, size_t ws_bytes, cudaStream_t st);
 size_t attn_tc_ws_bytes(const tv_plan* plan, const tv_attn_layer* layer, int n_seq, int n_max, int max_len);
 
+// A front-end layer descriptor the front-end kernels accept.
+bool front_layer_ok(const tv_gdn_front_layer* f);
+
 tv_status gdn_decode_launch(const tv_gdn_layer* l, int32_t n_seq, const void* q, const void* k, const void* v,
                             const float* alpha, const float* beta, void* out, float scale, int32_t* status,
                             cudaStream_t st);

@@ -173,6 +173,33 @@ def test_gdn_front_host_argument_errors(L):
     assert L.tv_gdn_conv_commit(ctypes.byref(f), ctypes.byref(t), 1, vp(16), None, vp(16), None, None) == 1
 
 
+def test_gdn_fused_host_argument_errors(L):
+    """tv_gdn_tree_verify_fused rejects a missing or mismatched front-end
+    layer, a missing input and a misaligned output before any launch."""
+    vp = ctypes.c_void_p
+    tails = (vp * 1)(vp(0x1000))
+    states = (vp * 1)(vp(0x3000))
+    g = B.tv_gdn_layer(B.TV_BF16, 16, 48, 128, 128, states)
+    f = B.tv_gdn_front_layer(B.TV_BF16, 16, 48, 128, 128, 4, vp(0x2000), tails)
+    t = B.tv_tree(1, 4, 4, 0x1000, 0x2000, 0x3000, 0x4000)
+    io = [vp(16)] * 4  # a_raw, b_raw, z, w_norm
+
+    def fused(front, out=vp(16), x=vp(16)):
+        return L.tv_gdn_tree_verify_fused(ctypes.byref(g), front, ctypes.byref(t), x, *io, out, 0.1, None)
+
+    assert fused(None) == 1                                                        # no front-end layer
+    other = B.tv_gdn_front_layer(B.TV_BF16, 16, 32, 128, 128, 4, vp(0x2000), tails)  # Hv differs
+    assert fused(ctypes.byref(other)) == 2
+    f32 = B.tv_gdn_front_layer(B.TV_F32, 16, 48, 128, 128, 4, vp(0x2000), tails)      # dtype differs
+    assert fused(ctypes.byref(f32)) == 2
+    wide = B.tv_gdn_front_layer(B.TV_BF16, 16, 48, 128, 128, 9, vp(0x2000), tails)    # width above 8
+    assert fused(ctypes.byref(wide)) == 2
+    no_tail = B.tv_gdn_front_layer(B.TV_BF16, 16, 48, 128, 128, 4, vp(0x2000), (vp * 1)(None))
+    assert fused(ctypes.byref(no_tail)) == 1                                       # W > 1 needs each tail
+    assert fused(ctypes.byref(f), x=None) == 1
+    assert fused(ctypes.byref(f), out=vp(24)) == 4                                 # misaligned output
+
+
 def test_static_scratch_rejects_oversized_request_on_host(L):
     """The size check comes before any device call, so it runs here."""
     layer, keep = _bf16_layer(cap=40000)

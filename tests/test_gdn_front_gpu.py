@@ -4,7 +4,8 @@ gated norm; "The model layer": convolution tails): tv_gdn_front ->
 tv_gdn_tree_verify -> tv_gdn_out_norm against the fp64 oracle
 (oracle/gdn_front.py), verified rows equal to the same tokens decoded one by
 one with real tail commits, bit for bit, and the tail commit of the accepted
-path equal to the decoded tail."""
+path equal to the decoded tail; the fused call (front end inside the verify
+kernel) equal to the three calls bit for bit."""
 import numpy as np
 import pytest
 import torch
@@ -157,3 +158,48 @@ def test_gdn_front_verify_rows_equal_decode_rows(cfg_id):
         torch.cuda.synchronize()
         assert torch.equal(bits(tail2), bits(tail)), f"path {path}: committed tail != decoded tail"
         assert np.array_equal(f64(tail2), G.commit_tail(f64(c.tail0), f64(c.x), path))
+
+
+@pytest.mark.parametrize("cfg_id,width", [(0, 1), (0, 4), (1, 8), (2, 4), (3, 4), (4, 4)])
+def test_gdn_fused_equals_front_verify_norm(cfg_id, width):
+    """tv_gdn_tree_verify_fused gives the bits of tv_gdn_front ->
+    tv_gdn_tree_verify -> tv_gdn_out_norm on every sequence of the workload's
+    trees (one 8/16/64/32-node tree, four 16-node trees), for convolution
+    widths 1 (no tail), 4 and 8 (windows reaching past the root into each
+    sequence's own tail); states and tails stay as they were."""
+    cfg = synth.workload(cfg_id)
+    sh = cfg.shapes
+    dt = sh.kv_dtype
+    parents = [synth.tree_and_tokens(cfg, s)[0] for s in range(cfg.n_seq)]
+    n = sum(len(p) for p in parents)
+    C = 2 * sh.Hk * sh.dk + sh.Hv * sh.dv
+    g = torch.Generator(device="cuda").manual_seed(1200 + 10 * cfg_id + width)
+    rn = lambda *shape, std=1.0, d=torch.float32: (torch.randn(*shape, generator=g, device="cuda") * std).to(d)
+    x = rn(n, C, d=dt)
+    a_raw, b_raw = rn(n, sh.Hv), rn(n, sh.Hv)
+    z = rn(n, sh.Hv, sh.dv, d=dt)
+    wconv, w_norm = rn(C, width, std=0.5), 1.0 + rn(sh.dv, std=0.1)
+    tails = [rn(max(width - 1, 1), C, d=dt) for _ in parents]
+    S0 = [rn(sh.Hv, sh.dv, sh.dk, std=0.1) for _ in parents]
+    scale = sh.dk ** -0.5
+    tree = B.Tree(parents)
+    B.tv_tree_prepare(tree)
+    fl = B.GdnFrontLayer(sh.Hk, sh.Hv, sh.dk, sh.dv, wconv, tails, dt)
+    e = lambda *shape, d=dt: torch.empty(*shape, dtype=d, device="cuda")
+    q, k, v = e(n, sh.Hk, sh.dk), e(n, sh.Hk, sh.dk), e(n, sh.Hv, sh.dv)
+    alpha, beta = e(n, sh.Hv, d=torch.float32), e(n, sh.Hv, d=torch.float32)
+    o, ref = e(n, sh.Hv, sh.dv), e(n, sh.Hv, sh.dv)
+    S1 = [s.clone() for s in S0]
+    B.tv_gdn_front(fl, tree, cfg.n_seq, x, a_raw, b_raw, q, k, v, alpha, beta)
+    B.tv_gdn_tree_verify(B.GdnLayer(S1, sh.Hk, dt), tree, q, k, v, alpha, beta, o, scale)
+    B.tv_gdn_out_norm(fl, n, o, z, w_norm, ref)
+    S2 = [s.clone() for s in S0]
+    tails0 = [t.clone() for t in tails]
+    out = torch.full((n, sh.Hv, sh.dv), float("nan"), dtype=dt, device="cuda")
+    B.tv_gdn_tree_verify_fused(B.GdnLayer(S2, sh.Hk, dt), fl, tree, x, a_raw, b_raw, z, w_norm, out, scale)
+    torch.cuda.synchronize()
+    assert tree.status_code() == 0
+    assert torch.equal(bits(out), bits(ref)), "fused output != front -> verify -> norm"
+    for s in range(cfg.n_seq):
+        assert torch.equal(bits(S2[s]), bits(S0[s])), f"sequence {s}: the verify changed a state"
+        assert torch.equal(bits(tails[s]), bits(tails0[s])), f"sequence {s}: the verify changed a tail"
