@@ -146,6 +146,14 @@ __device__ __forceinline__ f2_t f2_dup(float x) {
   asm("mov.b64 %0, {%1, %1};" : "=l"(d) : "f"(x));
   return d;
 }
+__device__ __forceinline__ f2_t f2_pack(float lo, float hi) {
+  f2_t d;
+  asm("mov.b64 %0, {%1, %2};" : "=l"(d) : "f"(lo), "f"(hi));
+  return d;
+}
+__device__ __forceinline__ void f2_unpack(f2_t a, float& lo, float& hi) {
+  asm("mov.b64 {%0, %1}, %2;" : "=f"(lo), "=f"(hi) : "l"(a));
+}
 __device__ __forceinline__ float f2_hsum(f2_t a) {
   float lo, hi;
   asm("mov.b64 {%0, %1}, %2;" : "=f"(lo), "=f"(hi) : "l"(a));

@@ -101,22 +101,14 @@ __global__ void __launch_bounds__(128) gdn_out_norm_kernel(const void* o_, const
   const T* o = static_cast<const T*>(o_) + static_cast<size_t>(warp) * DV;
   const T* z = static_cast<const T*>(z_) + static_cast<size_t>(warp) * DV;
   T* out = static_cast<T*>(out_) + static_cast<size_t>(warp) * DV;
-  float ov[CPL];
-  float ss = 0.f;
+  float ov[CPL], zv[CPL], wn[CPL];
 #pragma unroll
   for (int e = 0; e < CPL; e++) {
     ov[e] = to_f32(o[lane + 32 * e]);
-    ss = __fmaf_rn(ov[e], ov[e], ss);
+    zv[e] = to_f32(z[lane + 32 * e]);
+    wn[e] = w_norm[lane + 32 * e];
   }
-#pragma unroll
-  for (int sh = 16; sh >= 1; sh >>= 1) ss = __fadd_rn(ss, __shfl_xor_sync(0xffffffffu, ss, sh));
-  const float inv = __fdiv_rn(1.f, __fsqrt_rn(__fadd_rn(__fdiv_rn(ss, static_cast<float>(DV)), kNormEps)));
-#pragma unroll
-  for (int e = 0; e < CPL; e++) {
-    const int c = lane + 32 * e;
-    const float y = __fmul_rn(__fmul_rn(__fmul_rn(ov[e], inv), w_norm[c]), silu_f(to_f32(z[c])));
-    out[c] = from_f32<T>(y);
-  }
+  gated_norm_vals<T, CPL>(ov, zv, wn, out, lane);
 }
 
 struct ConvCommitParams {

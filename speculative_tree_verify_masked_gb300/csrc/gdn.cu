@@ -54,6 +54,13 @@ struct GdnVerifyParams {
   const float* wconv;
   const void* tail[TV_MAX_SEQ];
   int C, W;
+  int front_off;  // byte offset of the front-end staging in shared memory
+  // gated norm inside the kernel (norm_in): the CTA's outputs staged at
+  // obuf_off, each (node, value head)'s then gathered in the head's CTA that
+  // normalizes it, out = norm(o) * w_norm * SiLU(z)
+  const void* z;
+  const float* w_norm;
+  int norm_in, obuf_off;
 };
 
 // Slots for states that must outlive a subtree: at most floor(log2(n / 5)) + 1
@@ -80,6 +87,7 @@ struct GdnShape {
 // against 17.7 us), 4 otherwise (more sequences: 18.5 against 18.9 us on the
 // four-sequence workload).
 constexpr int kGdnRpg = 2;
+constexpr size_t kGdnSmemMax = 232448;  // dynamic shared memory a CTA may opt into
 
 // Shared memory: slots [n_slots][R][DK] f32 | keys, queries [n_max][DK] KQ |
 // (alpha, beta, k.q, -) [n_max] | v [n_max][R] f32 | visits [n_max] | segments [n_max].
@@ -92,6 +100,179 @@ inline size_t gdn_verify_smem(int n_max, int n_slots) {
   b += 2 * ((n * Sh::DK * sizeof(KQ) + 15) / 16 * 16);
   b += n * 16 + n * Sh::R * 4 + 2 * n * 4;
   return b;
+}
+
+// Front-end staging of the fused verify (bytes, each part 16-byte aligned):
+// raw rows [W-1+n_max][CH] T (the tail rows, then the nodes'; channels: the
+// key head's query and key, then the CTA's value rows) | convolution weights
+// [CH][W] f32 | window rows [n_max][8] as byte offsets into the raw rows u32 |
+// (16-bit types) pre-norm queries
+// and keys [n_max][2 DK] f32.  fp32 layers keep those in the key and query
+// buffers themselves.  It lies in the slots when they are large enough
+// (nothing uses them before the first visit), else after the other tables.
+struct FrontLayout {
+  size_t xs, ws, win, vals, bytes;
+};
+__host__ __device__ inline FrontLayout front_layout(int n_max, int W, int DK, int R, int tsize) {
+  const size_t CH = 2 * static_cast<size_t>(DK) + R;
+  auto a16 = [](size_t b) { return (b + 15) / 16 * 16; };
+  FrontLayout f;
+  f.xs = 0;
+  f.ws = a16(static_cast<size_t>(W - 1 + n_max) * CH * tsize);
+  f.win = f.ws + a16(CH * W * 4);
+  f.vals = f.win + a16(static_cast<size_t>(n_max) * 32);
+  f.bytes = f.vals + (tsize == 2 ? static_cast<size_t>(n_max) * 2 * DK * 4 : 0);
+  return f;
+}
+
+// Shared-memory accesses by 32-bit shared-window address.
+__device__ __forceinline__ uint32_t sh_u32(uint32_t a) {
+  uint32_t v;
+  asm volatile("ld.shared.b32 %0, [%1];" : "=r"(v) : "r"(a));
+  return v;
+}
+__device__ __forceinline__ float sh_f32(uint32_t a) { return __uint_as_float(sh_u32(a)); }
+__device__ __forceinline__ uint4 sh_v4(uint32_t a) {
+  uint4 v;
+  asm volatile("ld.shared.v4.b32 {%0, %1, %2, %3}, [%4];" : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w) : "r"(a));
+  return v;
+}
+__device__ __forceinline__ f2_t sh_f2(uint32_t a) {
+  f2_t v;
+  asm volatile("ld.shared.b64 %0, [%1];" : "=l"(v) : "r"(a));
+  return v;
+}
+__device__ __forceinline__ void sh_st_f2(uint32_t a, float x, float y) {
+  asm volatile("st.shared.v2.f32 [%0], {%1, %2};" ::"r"(a), "f"(x), "f"(y) : "memory");
+}
+
+// Thread-block cluster: rank, size, barrier, peer shared-memory loads.
+__device__ __forceinline__ uint32_t cluster_rank() {
+  uint32_t r;
+  asm volatile("mov.u32 %0, %%cluster_ctarank;" : "=r"(r));
+  return r;
+}
+__device__ __forceinline__ uint32_t cluster_size() {
+  uint32_t r;
+  asm volatile("mov.u32 %0, %%cluster_nctarank;" : "=r"(r));
+  return r;
+}
+__device__ __forceinline__ void cluster_sync_all() {
+  asm volatile("barrier.cluster.arrive.release;\n\tbarrier.cluster.wait.acquire;" ::: "memory");
+}
+__device__ __forceinline__ uint4 peer_v4(uint32_t local_addr, uint32_t rank) {
+  uint32_t a;
+  asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(a) : "r"(local_addr), "r"(rank));
+  uint4 v;
+  asm volatile("ld.shared::cluster.v4.b32 {%0, %1, %2, %3}, [%4];" : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w) : "r"(a)
+               : "memory");
+  return v;
+}
+
+__device__ __forceinline__ void peer_st_v4(uint32_t local_addr, uint32_t rank, uint4 v) {
+  uint32_t a;
+  asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(a) : "r"(local_addr), "r"(rank));
+  asm volatile("st.shared::cluster.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(a), "r"(v.x), "r"(v.y), "r"(v.z), "r"(v.w)
+               : "memory");
+}
+// One element of type T at a shared-window address of CTA `rank` of the
+// cluster (this CTA's own when rank is its own), widened to fp32.
+template <typename T>
+__device__ __forceinline__ float cluster_ld(uint32_t local_addr, uint32_t rank, uint32_t self) {
+  uint32_t a = local_addr, v;
+  if (rank != self) asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(a) : "r"(local_addr), "r"(rank));
+  if constexpr (sizeof(T) == 2) {
+    unsigned short h;
+    asm volatile("ld.shared::cluster.b16 %0, [%1];" : "=h"(h) : "r"(a) : "memory");
+    v = static_cast<uint32_t>(h) << 16;
+  } else {
+    asm volatile("ld.shared::cluster.b32 %0, [%1];" : "=r"(v) : "r"(a) : "memory");
+  }
+  return __uint_as_float(v);
+}
+
+// Convolution and SiLU of the fused verify's staged channel pairs [p0, p1)
+// for a window of WW taps, at nodes nstart, nstart + nstride, ... (count of
+// them): thread unit u takes channels ch, ch + 1 (packed pairs, the weights
+// in registers) of the unit's nodes ph, ph + NS, ...; four nodes' chains at
+// a time, their loads ahead of their stores.  Each value is formed as
+// conv_silu forms it (front_gdn.cuh): taps in order from +0, then SiLU.
+// Values go to vb (rounded to T), pre-norm queries and keys to vals (16-bit
+// KQ) or to qb / kb themselves (fp32).  All addresses are shared-window
+// offsets: xs raw rows [.][CH] T, ws weights [CH][WW], wof [n][8] byte
+// offsets of each node's window rows within xs.
+template <int WW, typename T, typename KQ, int DK, int R, int NT>
+__device__ __forceinline__ void front_conv(int tid, int p0, int p1, int nstart, int nstride, int count, uint32_t xs,
+                                           uint32_t ws, uint32_t wof, uint32_t vals, uint32_t vb, uint32_t qb,
+                                           uint32_t kb) {
+  constexpr int NB = 4, TS = static_cast<int>(sizeof(T));
+  const int np = p1 - p0, NS = (count + NB - 1) / NB;
+  for (int u = tid; u < np * NS; u += NT) {
+    const int ch = 2 * (p0 + u % np), ph = u / np;
+    f2_t wr[WW];
+#pragma unroll
+    for (int jj = 0; jj < WW; jj++) wr[jj] = f2_pack(sh_f32(ws + (ch * WW + jj) * 4), sh_f32(ws + ((ch + 1) * WW + jj) * 4));
+    const uint32_t xb = xs + ch * TS;
+    const bool is_v = ch >= 2 * DK;
+    uint32_t db, dstride;
+    if (is_v) {
+      db = vb + (ch - 2 * DK) * 4;
+      dstride = R * 4;
+    } else if (sizeof(KQ) == 2) {
+      db = vals + ch * 4;
+      dstride = 2 * DK * 4;
+    } else {
+      db = (ch < DK ? qb : kb) + (ch % DK) * 4;
+      dstride = DK * 4;
+    }
+    {
+      const int k0 = ph;
+      // the window offsets of the four nodes, then all their taps' loads,
+      // then the chains
+      uint4 o[NB][WW > 4 ? 2 : 1];
+#pragma unroll
+      for (int b = 0; b < NB; b++) {
+        const int node = nstart + nstride * min(k0 + b * NS, count - 1);  // past the end: a repeat, not stored
+        o[b][0] = sh_v4(wof + node * 32);
+        if constexpr (WW > 4) o[b][1] = sh_v4(wof + node * 32 + 16);
+      }
+      f2_t x2[NB][WW];
+#pragma unroll
+      for (int b = 0; b < NB; b++)
+#pragma unroll
+        for (int jj = 0; jj < WW; jj++) {
+          const uint4 q4 = o[b][jj / 4];
+          const uint32_t off = (jj & 3) == 0 ? q4.x : (jj & 3) == 1 ? q4.y : (jj & 3) == 2 ? q4.z : q4.w;
+          if constexpr (TS == 2) {
+            const uint32_t w2 = sh_u32(xb + off);
+            x2[b][jj] = f2_pack(bf16_lo(w2), bf16_hi(w2));
+          } else {
+            x2[b][jj] = sh_f2(xb + off);
+          }
+        }
+      f2_t acc[NB];
+#pragma unroll
+      for (int b = 0; b < NB; b++) {
+        acc[b] = 0ull;
+#pragma unroll
+        for (int jj = 0; jj < WW; jj++) acc[b] = f2_fma(wr[jj], x2[b][jj], acc[b]);
+      }
+#pragma unroll
+      for (int b = 0; b < NB; b++) {
+        if (k0 + b * NS < count) {
+          const int node = nstart + nstride * (k0 + b * NS);
+          float a0, a1;
+          f2_unpack(acc[b], a0, a1);
+          float y0 = silu_f(a0), y1 = silu_f(a1);
+          if (is_v) {
+            y0 = to_f32(from_f32<T>(y0));
+            y1 = to_f32(from_f32<T>(y1));
+          }
+          sh_st_f2(db + node * dstride, y0, y1);
+        }
+      }
+    }
+  }
 }
 
 __device__ __forceinline__ void cp_async16_g(void* dst, const void* src) {
@@ -146,11 +327,35 @@ __global__ void __launch_bounds__(32 * WARPS) gdn_verify_kernel(const GdnVerifyP
   pdl_trigger();
   MetaView mv = meta_view(const_cast<void*>(p.meta), p.n_total);
   const SeqInfo info = mv.seq[s];
-  if (status_bad(p.status)) return;
+  // The fused form may run in clusters of the CTAs that share a key head
+  // (they split its queries and keys by node, then exchange them): a CTA
+  // that leaves early still takes the cluster's two barriers, so none waits
+  // on it.  The status word can change under the launch, so CTAs of one
+  // cluster can take different paths here (each CTA decides as one: its
+  // threads vote).
+  uint32_t crank = 0, csize = 1;
+  if constexpr (FRONT) {
+    crank = cluster_rank();
+    csize = cluster_size();
+  }
+  auto leave = [&]() {
+    if (FRONT && csize > 1) {
+      cluster_sync_all();                  // the exchange of queries and keys
+      if (p.norm_in) cluster_sync_all();  // the outputs gathered
+    }
+  };
+  if (FRONT ? __syncthreads_or(status_bad(p.status)) != 0 : status_bad(p.status)) {
+    leave();
+    return;
+  }
   const int n = info.n, off = info.off, n_seg = info.n_seg;
-  if (n <= 0 || n > p.n_max || n_seg < 1 || n_seg > n) return;
+  if (n <= 0 || n > p.n_max || n_seg < 1 || n_seg > n) {
+    leave();
+    return;
+  }
   if (info.max_slot > p.n_slots) {
     if (tid == 0) set_status(p.status, TV_ERR_TREE);
+    leave();
     return;
   }
   const int g = h / (p.Hv / p.Hk);
@@ -166,51 +371,139 @@ __global__ void __launch_bounds__(32 * WARPS) gdn_verify_kernel(const GdnVerifyP
   int* sgt = sch + p.n_max;                                                           // [n_max] segments
 
   if constexpr (FRONT) {
-    // The front end, as tv_gdn_front forms it (front_gdn.cuh): this key
-    // head's query and key of every node (one warp per node and vector:
-    // convolution along the node's ancestor path into the committed tail,
-    // SiLU, division by the head's L2 norm, rounding to the layer type), the
-    // values of this CTA's rows (convolution, SiLU, rounding) and the gates.
-    const T* x = static_cast<const T*>(p.x);
-    const T* tail = static_cast<const T*>(p.tail[s]);
-    const int warp = tid >> 5, lane = tid & 31;
-    constexpr int CPL = DK / 32;
-    auto window = [&](int node, int (&src)[kMaxConvWidth]) {
-      const int row = off + node;
-      conv_window(src, p.W, mv.depth[row], off, mv.anc_at + static_cast<size_t>(row) * TV_MAX_PATH, row);
-    };
-    for (int w = warp; w < 2 * n; w += WARPS) {
-      const int node = w >> 1, is_k = w & 1;
-      int src[kMaxConvWidth];
-      window(node, src);
-      const int c0 = (is_k ? p.Hk + g : g) * DK;
-      float val[CPL];
-#pragma unroll
-      for (int e = 0; e < CPL; e++) val[e] = conv_silu(x, tail, p.wconv, p.C, p.W, src, c0 + lane + 32 * e);
-      const float sc = warp_l2_scale<CPL>(val);
-      KQ* dst = (is_k ? kb : qb) + static_cast<size_t>(node) * DK;
-#pragma unroll
-      for (int e = 0; e < CPL; e++) dst[lane + 32 * e] = from_f32<KQ>(__fmul_rn(val[e], sc));
-    }
-    for (int idx = tid; idx < n * R; idx += NT) {
-      const int node = idx / R, rr = rb * R + idx % R;
-      float vv = 0.f;
-      if (rr < p.dv) {
-        int src[kMaxConvWidth];
-        window(node, src);
-        vv = to_f32(from_f32<T>(conv_silu(x, tail, p.wconv, p.C, p.W, src, 2 * p.Hk * DK + h * p.dv + rr)));
+    // The front end, as tv_gdn_front forms it (front_gdn.cuh), in one memory
+    // round trip: the raw rows this CTA reads (the sequence's tail and its
+    // nodes, at the key head's query and key channels and the CTA's value
+    // rows), the convolution weights of those channels and each node's
+    // window rows go to shared memory; then every channel of every node is
+    // convolved (taps in order) and passed through SiLU, values rounded to
+    // the layer type; then each query and key is divided by its L2 norm
+    // (lane sums in channel order, then the butterfly) and rounded.
+    constexpr int CH = 2 * DK + R, EPC = 16 / static_cast<int>(sizeof(T)), CPL = DK / 32;
+    const int W = p.W, W1 = p.W - 1;
+    const int vch = min(R, p.dv - rb * R);  // value channels this CTA holds
+    const FrontLayout fl = front_layout(p.n_max, W, DK, R, static_cast<int>(sizeof(T)));
+    uint8_t* fb = reinterpret_cast<uint8_t*>(smem4) + p.front_off;
+    T* xs = reinterpret_cast<T*>(fb + fl.xs);
+    float* ws = reinterpret_cast<float*>(fb + fl.ws);
+    uint32_t* wof = reinterpret_cast<uint32_t*>(fb + fl.win);
+    float* vals = reinterpret_cast<float*>(fb + fl.vals);
+    {
+      const T* x = static_cast<const T*>(p.x);
+      const T* tail = static_cast<const T*>(p.tail[s]);
+      const int cq = DK / EPC, cpr = 2 * cq + vch / EPC;  // chunks of a row
+      const size_t v0 = static_cast<size_t>(2) * p.Hk * DK + static_cast<size_t>(h) * p.dv + rb * R;
+      for (int idx = tid; idx < (W1 + n) * cpr; idx += NT) {
+        const int r = idx / cpr, c = idx % cpr;
+        const T* row = r < W1 ? tail + static_cast<size_t>(r) * p.C : x + static_cast<size_t>(off + r - W1) * p.C;
+        const size_t src = c < cq ? static_cast<size_t>(g) * DK + c * EPC
+                                  : (c < 2 * cq ? static_cast<size_t>(p.Hk + g) * DK + (c - cq) * EPC
+                                                : v0 + (c - 2 * cq) * EPC);
+        cp_async16_g(xs + static_cast<size_t>(r) * CH + c * EPC, row + src);
       }
-      vb[idx] = vv;
+      const int wq = DK * W / 4, wv = vch * W / 4;  // 16-byte chunks of weights
+      for (int idx = tid; idx < 2 * wq + wv; idx += NT) {
+        const size_t src = idx < wq ? static_cast<size_t>(g) * DK * W + idx * 4
+                                    : (idx < 2 * wq ? static_cast<size_t>(p.Hk + g) * DK * W + (idx - wq) * 4
+                                                    : v0 * W + (idx - 2 * wq) * 4);
+        cp_async16_g(ws + idx * 4, p.wconv + src);
+      }
+      asm volatile("cp.async.commit_group;" ::: "memory");
+      for (int idx = tid; idx < n; idx += NT) {
+        const int row = off + idx;
+        const int depth = mv.depth[row];
+        // the node's ancestors (one byte per depth), one 16-byte load beside the depth's
+        const ulonglong2 anc = *reinterpret_cast<const ulonglong2*>(mv.anc_at + static_cast<size_t>(row) * TV_MAX_PATH);
+        for (int jj = 0; jj < W; jj++) {
+          const int m = depth + jj - W1;  // window element jj: ancestor at depth m, or tail row m + W - 1
+          const int am = static_cast<int8_t>(((m < 8 ? anc.x : anc.y) >> (8 * (m & 7))) & 0xFF);
+          wof[idx * 8 + jj] = static_cast<uint32_t>((m < 0 ? m + W1 : W1 + am) * CH * static_cast<int>(sizeof(T)));
+        }
+        const size_t ah = static_cast<size_t>(row) * p.Hv + h;
+        float a, b;
+        front_gates(p.a_raw[ah], p.b_raw[ah], a, b);
+        nc[idx] = make_float4(a, b, 0.f, 0.f);
+        sch[idx] = mv.sched[row];
+        sgt[idx] = mv.seg[row];
+      }
+      if (vch < R)
+        for (int idx = tid; idx < n * R; idx += NT)
+          if (idx % R >= vch) vb[idx] = 0.f;
+      asm volatile("cp.async.wait_all;" ::: "memory");
+      __syncthreads();
     }
-    for (int idx = tid; idx < n; idx += NT) {
-      const size_t ah = static_cast<size_t>(off + idx) * p.Hv + h;
-      float a, b;
-      front_gates(p.a_raw[ah], p.b_raw[ah], a, b);
-      nc[idx] = make_float4(a, b, 0.f, 0.f);
-      sch[idx] = mv.sched[off + idx];
-      sgt[idx] = mv.seg[off + idx];
+    {
+      const uint32_t xs_s = static_cast<uint32_t>(__cvta_generic_to_shared(xs));
+      const uint32_t ws_s = static_cast<uint32_t>(__cvta_generic_to_shared(ws));
+      const uint32_t wo_s = static_cast<uint32_t>(__cvta_generic_to_shared(wof));
+      const uint32_t va_s = static_cast<uint32_t>(__cvta_generic_to_shared(vals));
+      const uint32_t vb_s = static_cast<uint32_t>(__cvta_generic_to_shared(vb));
+      const uint32_t qb_s = static_cast<uint32_t>(__cvta_generic_to_shared(qb));
+      const uint32_t kb_s = static_cast<uint32_t>(__cvta_generic_to_shared(kb));
+      // this CTA's share of the queries and keys (nodes crank, crank + csize,
+      // ...), then the values of its rows at every node
+      const int own = (n - static_cast<int>(crank) + static_cast<int>(csize) - 1) / static_cast<int>(csize);
+#define TV_FRONT_CONV(WW)                                                                                   \
+  front_conv<WW, T, KQ, DK, R, NT>(tid, 0, DK, crank, csize, own, xs_s, ws_s, wo_s, va_s, vb_s, qb_s, kb_s); \
+  front_conv<WW, T, KQ, DK, R, NT>(tid, DK, DK + vch / 2, 0, 1, n, xs_s, ws_s, wo_s, va_s, vb_s, qb_s, kb_s)
+      switch (W) {
+        case 1: TV_FRONT_CONV(1); break;
+        case 2: TV_FRONT_CONV(2); break;
+        case 3: TV_FRONT_CONV(3); break;
+        case 4: TV_FRONT_CONV(4); break;
+        case 5: TV_FRONT_CONV(5); break;
+        case 6: TV_FRONT_CONV(6); break;
+        case 7: TV_FRONT_CONV(7); break;
+        default: TV_FRONT_CONV(8); break;
+      }
+#undef TV_FRONT_CONV
     }
     __syncthreads();
+    const int warp = tid >> 5, lane = tid & 31;
+    // two heads a warp at a time (task w: the CTA's node w / 2, query or key)
+    const int own = (n - static_cast<int>(crank) + static_cast<int>(csize) - 1) / static_cast<int>(csize);
+    for (int w0 = warp; w0 < 2 * own; w0 += 2 * WARPS) {
+      const int tk[2] = {w0, w0 + WARPS < 2 * own ? w0 + WARPS : w0};
+      float val[2][CPL], sc[2];
+#pragma unroll
+      for (int i = 0; i < 2; i++) {
+        const int node = static_cast<int>(crank + csize * (tk[i] >> 1)), is_k = tk[i] & 1;
+        const float* src = sizeof(KQ) == 2 ? vals + node * 2 * DK + is_k * DK
+                                           : reinterpret_cast<const float*>((is_k ? kb : qb) + static_cast<size_t>(node) * DK);
+#pragma unroll
+        for (int e = 0; e < CPL; e++) val[i][e] = src[lane + 32 * e];
+      }
+      warp_l2_scales<CPL, 2>(val, sc);
+#pragma unroll
+      for (int i = 0; i < 2; i++) {
+        if (i == 1 && tk[1] == tk[0]) break;
+        const int node = static_cast<int>(crank + csize * (tk[i] >> 1)), is_k = tk[i] & 1;
+        KQ* dst = (is_k ? kb : qb) + static_cast<size_t>(node) * DK;
+#pragma unroll
+        for (int e = 0; e < CPL; e++) dst[lane + 32 * e] = from_f32<KQ>(__fmul_rn(val[i][e], sc[i]));
+      }
+    }
+    __syncthreads();
+    if (csize > 1) {
+      // push this CTA's share (its nodes' key and query rows) into every
+      // other CTA of the cluster, same offsets; the barrier then makes all
+      // shares visible everywhere (and no CTA leaves with writes pending)
+      constexpr int CPV = DK * static_cast<int>(sizeof(KQ)) / 16;  // 16-byte chunks of a row
+      const uint32_t kb_s = static_cast<uint32_t>(__cvta_generic_to_shared(kb));
+      const uint32_t qb_s = static_cast<uint32_t>(__cvta_generic_to_shared(qb));
+      const int per = own * 2 * CPV;
+      for (int idx = tid; idx < per * static_cast<int>(csize - 1); idx += NT) {
+        const int pi = idx / per, rem = idx % per;
+        const uint32_t peer = (crank + 1 + static_cast<uint32_t>(pi)) % csize;
+        const int node = static_cast<int>(crank) + static_cast<int>(csize) * (rem / (2 * CPV));
+        const int r2 = rem % (2 * CPV);
+        const uint32_t a = (r2 < CPV ? kb_s : qb_s) + node * DK * static_cast<int>(sizeof(KQ)) + (r2 % CPV) * 16;
+        uint4 v;
+        asm volatile("ld.shared.v4.b32 {%0, %1, %2, %3}, [%4];" : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w) : "r"(a));
+        peer_st_v4(a, peer, v);
+      }
+      cluster_sync_all();
+    }
   } else {
   // Stage the tree's keys and queries of this key head (cp.async), the
   // values of this CTA's rows, alpha, beta and the steps.  Every global load
@@ -291,7 +584,16 @@ __global__ void __launch_bounds__(32 * WARPS) gdn_verify_kernel(const GdnVerifyP
   // Outputs go out as explicit global stores: the compiler then knows they
   // cannot alias the shared-memory tables and may issue the next visit's
   // loads ahead of them.
+  // fused form with the norm: this CTA's output rows of every node go to
+  // stage [n_max][R] (shared memory), gathered after the visits
+  const int dvp = rb_per_head * R;
+  T* stage = FRONT ? reinterpret_cast<T*>(reinterpret_cast<uint8_t*>(smem4) + p.obuf_off) : nullptr;
   auto put = [&](int node, const float (&o)[RPG]) {
+    if (FRONT && p.norm_in) {
+#pragma unroll
+      for (int i = 0; i < RPG; i++) stage[node * R + RPG * gi + i] = from_f32<T>(o[i]);
+      return;
+    }
     T* dst = out + static_cast<size_t>(node) * out_stride;
     if (vec_store) {
       uint32_t w[RPG / 2 > 0 ? RPG / 2 : 1];
@@ -381,6 +683,73 @@ __global__ void __launch_bounds__(32 * WARPS) gdn_verify_kernel(const GdnVerifyP
       for (int i = 0; i < RPG; i++) store_row<LPR>(sl + i * DK, st[i], j);
     }
   }
+  if constexpr (FRONT) {
+    if (p.norm_in) {
+      // gated norm of (node, head h) for this CTA's nodes rb, rb + rbph, ...,
+      // two a warp at a time; z and w_norm load before the barrier that
+      // completes the gathered outputs
+      constexpr int CPL = DK / 32;  // the front end's dv = dk
+      const int warp = tid >> 5, lane = tid & 31;
+      const T* z = static_cast<const T*>(p.z);
+      T* o_out = static_cast<T*>(p.out);
+      // gather: node k's rows go to the head's CTA k mod rb_per_head, which
+      // holds the node's dv outputs at obuf[k / rb_per_head][.] (this CTA's
+      // at rb R ..): 16-byte chunks, stored into peers directly
+      const int stage_b = p.n_max * R * static_cast<int>(sizeof(T));
+      const uint32_t st_s = static_cast<uint32_t>(__cvta_generic_to_shared(stage));
+      const uint32_t ob_s = st_s + stage_b;
+      const T* obuf = stage + p.n_max * R;
+      {
+        __syncthreads();
+        constexpr int CPN = R * static_cast<int>(sizeof(T)) / 16;  // chunks of a node's rows
+        for (int idx = tid; idx < n * CPN; idx += NT) {
+          const int node = idx / CPN, c = idx % CPN, owner = node % rb_per_head;
+          uint4 v;
+          asm volatile("ld.shared.v4.b32 {%0, %1, %2, %3}, [%4];" : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w)
+                       : "r"(st_s + node * R * static_cast<int>(sizeof(T)) + c * 16));
+          const uint32_t a = ob_s + ((node / rb_per_head) * dvp + rb * R) * static_cast<int>(sizeof(T)) + c * 16;
+          if (owner == rb) {
+            asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(a), "r"(v.x), "r"(v.y), "r"(v.z), "r"(v.w)
+                         : "memory");
+          } else {
+            peer_st_v4(a, static_cast<uint32_t>(h * rb_per_head + owner) % csize, v);
+          }
+        }
+      }
+      auto row = [&](int k) { return (static_cast<size_t>(off + rb + k * rb_per_head) * p.Hv + h) * p.dv; };
+      auto zload = [&](int k, float (&zz)[CPL]) {
+        if (rb + k * rb_per_head < n) {
+#pragma unroll
+          for (int e = 0; e < CPL; e++) zz[e] = to_f32(z[row(k) + lane + 32 * e]);
+        }
+      };
+      float wn[CPL], za[CPL], zb[CPL];
+#pragma unroll
+      for (int e = 0; e < CPL; e++) wn[e] = p.w_norm[lane + 32 * e];
+      zload(warp, za);
+      zload(warp + WARPS, zb);
+      if (csize > 1) cluster_sync_all(); else __syncthreads();
+      for (int k = warp; rb + k * rb_per_head < n; k += 2 * WARPS) {
+        const int k2 = k + WARPS;
+        const bool has2 = rb + k2 * rb_per_head < n;
+        float oa[CPL], ob[CPL], na[CPL], nb[CPL];
+#pragma unroll
+        for (int e = 0; e < CPL; e++) {
+          oa[e] = to_f32(obuf[k * dvp + lane + 32 * e]);
+          ob[e] = has2 ? to_f32(obuf[k2 * dvp + lane + 32 * e]) : 0.f;
+        }
+        zload(k + 2 * WARPS, na);
+        zload(k2 + 2 * WARPS, nb);
+        gated_norm_vals<T, CPL>(oa, za, wn, o_out + row(k), lane);
+        if (has2) gated_norm_vals<T, CPL>(ob, zb, wn, o_out + row(k2), lane);
+#pragma unroll
+        for (int e = 0; e < CPL; e++) {
+          za[e] = na[e];
+          zb[e] = nb[e];
+        }
+      }
+    }
+  }
 }
 
 struct GdnDecodeParams {
@@ -445,26 +814,102 @@ static bool gdn_shape_ok(const tv_gdn_layer* l) {
          (l->dk == 64 || l->dk == 128) && l->dv >= 1 && l->dv <= 256 && l->S;
 }
 
+// Whether clusters of G CTAs of this kernel and shared memory can be placed
+// at all (answers cached per kernel, size and shared memory).
+static bool cluster_fits(const void* kern, int G, dim3 grid, dim3 block, size_t smem) {
+  struct Entry {
+    const void* k;
+    int G;
+    size_t smem;
+    bool ok;
+  };
+  static Entry cache[64];
+  static int n_cache = 0;
+  for (int i = 0; i < n_cache; i++)
+    if (cache[i].k == kern && cache[i].G == G && cache[i].smem == smem) return cache[i].ok;
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = grid;
+  cfg.blockDim = block;
+  cfg.dynamicSmemBytes = smem;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeClusterDimension;
+  attr[0].val.clusterDim.x = G;
+  attr[0].val.clusterDim.y = 1;
+  attr[0].val.clusterDim.z = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  int n_clusters = 0;
+  const bool ok = cudaOccupancyMaxActiveClusters(&n_clusters, kern, &cfg) == cudaSuccess && n_clusters > 0;
+  cudaGetLastError();
+  if (n_cache < 64) cache[n_cache++] = {kern, G, smem, ok};
+  return ok;
+}
+
+// Shared memory of the fused verify (front-end staging inside the slots when
+// it fits, else after the tables; the norm's output rows last) and the
+// offsets it places.
+template <typename T, typename Sh>
+static size_t fused_smem(const GdnVerifyParams& p, bool norm_in, int* front_off, int* obuf_off) {
+  size_t smem = gdn_verify_smem<T, Sh>(p.n_max, p.n_slots);
+  *front_off = 0;
+  const size_t fb = front_layout(p.n_max, p.W, Sh::DK, Sh::R, static_cast<int>(sizeof(T))).bytes;
+  if (fb > static_cast<size_t>(p.n_slots) * Sh::R * Sh::DK * 4) {
+    *front_off = static_cast<int>((smem + 15) / 16 * 16);
+    smem = *front_off + fb;
+  }
+  *obuf_off = static_cast<int>((smem + 15) / 16 * 16);
+  const int rbph = (p.dv + Sh::R - 1) / Sh::R;  // stage [n_max][R], gathered [ceil(n_max / rbph)][rbph R]
+  if (norm_in)
+    smem = *obuf_off + (static_cast<size_t>(p.n_max) + static_cast<size_t>((p.n_max + rbph - 1) / rbph) * rbph) *
+                           Sh::R * sizeof(T);
+  return smem;
+}
+
+// Launches the verify kernel; for the fused form, returns whether the gated
+// norm ran inside it (else the caller runs tv_gdn_out_norm over out).
 template <typename T, int LPR, int WARPS, bool FRONT>
-static void launch_verify_w(const GdnVerifyParams& p, int n_seq, cudaStream_t st, bool ov) {
+static bool launch_verify_w(const GdnVerifyParams& p, int n_seq, cudaStream_t st, bool ov) {
   using Sh = GdnShape<LPR, kGdnRpg, WARPS>;
   constexpr int R = Sh::R;
   auto kern = gdn_verify_kernel<T, LPR, kGdnRpg, WARPS, FRONT>;
   static bool attrs = false;  // one-time, sized for the largest tree
   if (!attrs) {
-    const int smem_max = static_cast<int>(gdn_verify_smem<T, Sh>(TV_MAX_NODES, slots_for(TV_MAX_NODES)));
-    cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem_max);
+    const size_t smem_max = FRONT ? kGdnSmemMax : gdn_verify_smem<T, Sh>(TV_MAX_NODES, slots_for(TV_MAX_NODES));
+    cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(smem_max));
+    if (FRONT) cudaFuncSetAttribute(kern, cudaFuncAttributeNonPortableClusterSizeAllowed, 1);
     attrs = true;
   }
   const dim3 grid(p.Hv * ((p.dv + R - 1) / R), n_seq);
-  launch_k(ov, kern, grid, dim3(32 * WARPS), gdn_verify_smem<T, Sh>(p.n_max, p.n_slots), st, p);
+  if (!FRONT) {
+    launch_k(ov, kern, grid, dim3(32 * WARPS), gdn_verify_smem<T, Sh>(p.n_max, p.n_slots), st, p);
+    return false;
+  }
+  // clusters of the CTAs that share a key head (heads per key head x row
+  // blocks per head, at most 16): they split its queries and keys by node,
+  // and gather each head's outputs for the norm
+  const int rbph = (p.dv + R - 1) / R;
+  int G = (p.Hv / p.Hk) * rbph;
+  if (G > 16) G = 1;
+  GdnVerifyParams q = p;
+  const bool norm_fits = fused_smem<T, Sh>(p, true, &q.front_off, &q.obuf_off) <= kGdnSmemMax;
+  size_t smem = fused_smem<T, Sh>(p, norm_fits, &q.front_off, &q.obuf_off);
+  if (G > 1 && !cluster_fits(reinterpret_cast<const void*>(kern), G, grid, dim3(32 * WARPS), smem)) G = 1;
+  q.norm_in = norm_fits && (G > 1 || rbph == 1) ? 1 : 0;
+  smem = fused_smem<T, Sh>(p, q.norm_in != 0, &q.front_off, &q.obuf_off);
+  if (G > 1) launch_k_cluster(ov, G, kern, grid, dim3(32 * WARPS), smem, st, q);
+  else launch_k(ov, kern, grid, dim3(32 * WARPS), smem, st, q);
+  return q.norm_in != 0;
 }
 template <typename T, int LPR, bool FRONT>
-static void launch_verify(const GdnVerifyParams& p, int n_seq, cudaStream_t st, bool ov) {
+static bool launch_verify(const GdnVerifyParams& p, int n_seq, cudaStream_t st, bool ov) {
   constexpr int R4 = GdnShape<LPR, kGdnRpg, 4>::R;
   const long long ctas4 = static_cast<long long>(p.Hv) * ((p.dv + R4 - 1) / R4) * n_seq;
-  if (ctas4 <= 2LL * num_sms()) launch_verify_w<T, LPR, 8, FRONT>(p, n_seq, st, ov);
-  else launch_verify_w<T, LPR, 4, FRONT>(p, n_seq, st, ov);
+  bool four = ctas4 > 2LL * num_sms();
+  if (FRONT && four) {  // the fused form's tables must fit CTAs of four warps
+    int fo, oo;
+    four = fused_smem<T, GdnShape<LPR, kGdnRpg, 4>>(p, false, &fo, &oo) <= kGdnSmemMax;
+  }
+  return four ? launch_verify_w<T, LPR, 4, FRONT>(p, n_seq, st, ov) : launch_verify_w<T, LPR, 8, FRONT>(p, n_seq, st, ov);
 }
 
 template <typename T, int LPR>
@@ -539,9 +984,11 @@ extern "C" tv_status tv_gdn_tree_verify(const tv_gdn_layer* l, const tv_tree* t,
 
 // The fused form: the front end computed inside the verify kernel from the
 // raw projections (no q, k, v, alpha or beta in memory), then the gated RMS
-// norm of the outputs in place.  The norm needs all dv rows of a (node,
-// value head), which two CTAs of the verify kernel share, so it is a second
-// kernel over `out`.
+// norm of the outputs.  The norm of a (node, value head) needs all dv rows,
+// which the head's CTAs share: they run as one cluster (with the other heads
+// of the key head) and gather the rows through distributed shared memory.
+// Where no such cluster can be placed (more than 16 CTAs to a key head) the
+// norm runs as a second kernel over `out`.
 extern "C" tv_status tv_gdn_tree_verify_fused(const tv_gdn_layer* l, const tv_gdn_front_layer* f, const tv_tree* t,
                                               const void* x, const float* a_raw, const float* b_raw, const void* z,
                                               const float* w_norm, void* out, float scale, tv_stream stream) {
@@ -552,12 +999,13 @@ extern "C" tv_status tv_gdn_tree_verify_fused(const tv_gdn_layer* l, const tv_gd
   if (f->dtype != l->dtype || f->Hk != l->Hk || f->Hv != l->Hv || f->dk != l->dk || f->dv != l->dv)
     return TV_ERR_SHAPE;
   if (!x || !a_raw || !b_raw || !z || !w_norm || !out) return TV_ERR_ARG;
-  if (!aligned16(out)) return TV_ERR_ALIGN;
+  if (!aligned16(out) || !aligned16(x) || !aligned16(f->wconv)) return TV_ERR_ALIGN;
   GdnVerifyParams p{};
   for (int s = 0; s < t->n_seq; s++) {
     if (!l->S[s]) return TV_ERR_ARG;
     if (!aligned16(l->S[s])) return TV_ERR_ALIGN;
     if (f->width > 1 && !f->tail[s]) return TV_ERR_ARG;
+    if (f->width > 1 && !aligned16(f->tail[s])) return TV_ERR_ALIGN;
     p.S[s] = l->S[s];
     p.tail[s] = f->tail[s];
   }
@@ -569,16 +1017,18 @@ extern "C" tv_status tv_gdn_tree_verify_fused(const tv_gdn_layer* l, const tv_gd
   p.C = 2 * l->Hk * l->dk + l->Hv * l->dv;
   p.W = f->width;
   cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
+  p.z = z; p.w_norm = w_norm;
   const bool bf = l->dtype == TV_BF16;
   const bool ov = tree_overlap(t);
+  bool norm_in;
   if (l->dk == 128) {
     constexpr int LPR = lanes_per_row<128>();
-    if (bf) launch_verify<__nv_bfloat16, LPR, true>(p, t->n_seq, st, ov); else launch_verify<float, LPR, true>(p, t->n_seq, st, ov);
+    norm_in = bf ? launch_verify<__nv_bfloat16, LPR, true>(p, t->n_seq, st, ov) : launch_verify<float, LPR, true>(p, t->n_seq, st, ov);
   } else {
     constexpr int LPR = lanes_per_row<64>();
-    if (bf) launch_verify<__nv_bfloat16, LPR, true>(p, t->n_seq, st, ov); else launch_verify<float, LPR, true>(p, t->n_seq, st, ov);
+    norm_in = bf ? launch_verify<__nv_bfloat16, LPR, true>(p, t->n_seq, st, ov) : launch_verify<float, LPR, true>(p, t->n_seq, st, ov);
   }
   const tv_status ls = launch_status();
-  if (ls != TV_OK) return ls;
+  if (ls != TV_OK || norm_in) return ls;
   return tv_gdn_out_norm(f, t->n_total, out, z, w_norm, out, stream);
 }

@@ -31,6 +31,30 @@ inline void launch_k(bool overlap, void (*kernel)(KArgs...), dim3 grid, dim3 blo
   cudaLaunchKernelEx(&cfg, kernel, std::forward<Args>(args)...);
 }
 
+// launch_k with a thread-block cluster of cluster_x CTAs along x.
+template <typename... KArgs, typename... Args>
+inline void launch_k_cluster(bool overlap, int cluster_x, void (*kernel)(KArgs...), dim3 grid, dim3 block,
+                             size_t smem, cudaStream_t st, Args&&... args) {
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = grid;
+  cfg.blockDim = block;
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = st;
+  cudaLaunchAttribute attr[2];
+  attr[0].id = cudaLaunchAttributeClusterDimension;
+  attr[0].val.clusterDim.x = cluster_x;
+  attr[0].val.clusterDim.y = 1;
+  attr[0].val.clusterDim.z = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  if (overlap) {
+    attr[1].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[1].val.programmaticStreamSerializationAllowed = 1;
+    cfg.numAttrs = 2;
+  }
+  cudaLaunchKernelEx(&cfg, kernel, std::forward<Args>(args)...);
+}
+
 inline bool tree_overlap(const tv_tree* t) { return t && (t->flags & TV_TREE_OVERLAP) != 0; }
 
 // Status of the launches just enqueued.  Clears a sticky-free launch error
