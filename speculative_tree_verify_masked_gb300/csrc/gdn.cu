@@ -105,13 +105,11 @@ inline size_t gdn_verify_smem(int n_max, int n_slots) {
 // Front-end staging of the fused verify (bytes, each part 16-byte aligned):
 // raw rows [W-1+n_max][CH] T (the tail rows, then the nodes'; channels: the
 // key head's query and key, then the CTA's value rows) | convolution weights
-// [CH][W] f32 | window rows [n_max][8] as byte offsets into the raw rows u32 |
-// (16-bit types) pre-norm queries
-// and keys [n_max][2 DK] f32.  fp32 layers keep those in the key and query
-// buffers themselves.  It lies in the slots when they are large enough
-// (nothing uses them before the first visit), else after the other tables.
+// [CH][W] f32 | window rows [n_max][8] as byte offsets into the raw rows u32.
+// It lies in the slots when they are large enough (nothing uses them before
+// the first visit), else after the other tables.
 struct FrontLayout {
-  size_t xs, ws, win, vals, bytes;
+  size_t xs, ws, win, bytes;
 };
 __host__ __device__ inline FrontLayout front_layout(int n_max, int W, int DK, int R, int tsize) {
   const size_t CH = 2 * static_cast<size_t>(DK) + R;
@@ -120,8 +118,7 @@ __host__ __device__ inline FrontLayout front_layout(int n_max, int W, int DK, in
   f.xs = 0;
   f.ws = a16(static_cast<size_t>(W - 1 + n_max) * CH * tsize);
   f.win = f.ws + a16(CH * W * 4);
-  f.vals = f.win + a16(static_cast<size_t>(n_max) * 32);
-  f.bytes = f.vals + (tsize == 2 ? static_cast<size_t>(n_max) * 2 * DK * 4 : 0);
+  f.bytes = f.win + a16(static_cast<size_t>(n_max) * 32);
   return f;
 }
 
@@ -191,40 +188,27 @@ __device__ __forceinline__ float cluster_ld(uint32_t local_addr, uint32_t rank, 
   return __uint_as_float(v);
 }
 
-// Convolution and SiLU of the fused verify's staged channel pairs [p0, p1)
-// for a window of WW taps, at nodes nstart, nstart + nstride, ... (count of
-// them): thread unit u takes channels ch, ch + 1 (packed pairs, the weights
-// in registers) of the unit's nodes ph, ph + NS, ...; four nodes' chains at
-// a time, their loads ahead of their stores.  Each value is formed as
-// conv_silu forms it (front_gdn.cuh): taps in order from +0, then SiLU.
-// Values go to vb (rounded to T), pre-norm queries and keys to vals (16-bit
-// KQ) or to qb / kb themselves (fp32).  All addresses are shared-window
-// offsets: xs raw rows [.][CH] T, ws weights [CH][WW], wof [n][8] byte
-// offsets of each node's window rows within xs.
-template <int WW, typename T, typename KQ, int DK, int R, int NT>
-__device__ __forceinline__ void front_conv(int tid, int p0, int p1, int nstart, int nstride, int count, uint32_t xs,
-                                           uint32_t ws, uint32_t wof, uint32_t vals, uint32_t vb, uint32_t qb,
-                                           uint32_t kb) {
+// Values of the fused verify: convolution and SiLU of the staged value
+// channels (pairs [DK, DK + vch / 2) of the staged row) for a window of WW
+// taps at every node, rounded to T, into vb [n][R] f32.  Thread unit u takes
+// channels ch, ch + 1 (packed pairs, the weights in registers) of nodes ph,
+// ph + NS, ...; four nodes' chains at a time, their loads ahead of their
+// stores.  Each value is formed as conv_silu forms it (front_gdn.cuh): taps
+// in order from +0, then SiLU.  All addresses are shared-window offsets: xs
+// raw rows [.][CH] T, ws weights [CH][WW], wof [n][8] byte offsets of each
+// node's window rows within xs.
+template <int WW, typename T, int DK, int R, int NT>
+__device__ __forceinline__ void front_values(int tid, int vch, int count, uint32_t xs, uint32_t ws, uint32_t wof,
+                                             uint32_t vb) {
   constexpr int NB = 4, TS = static_cast<int>(sizeof(T));
-  const int np = p1 - p0, NS = (count + NB - 1) / NB;
+  const int np = vch / 2, NS = (count + NB - 1) / NB;
   for (int u = tid; u < np * NS; u += NT) {
-    const int ch = 2 * (p0 + u % np), ph = u / np;
+    const int ch = 2 * (DK + u % np), ph = u / np;
     f2_t wr[WW];
 #pragma unroll
     for (int jj = 0; jj < WW; jj++) wr[jj] = f2_pack(sh_f32(ws + (ch * WW + jj) * 4), sh_f32(ws + ((ch + 1) * WW + jj) * 4));
     const uint32_t xb = xs + ch * TS;
-    const bool is_v = ch >= 2 * DK;
-    uint32_t db, dstride;
-    if (is_v) {
-      db = vb + (ch - 2 * DK) * 4;
-      dstride = R * 4;
-    } else if (sizeof(KQ) == 2) {
-      db = vals + ch * 4;
-      dstride = 2 * DK * 4;
-    } else {
-      db = (ch < DK ? qb : kb) + (ch % DK) * 4;
-      dstride = DK * 4;
-    }
+    const uint32_t db = vb + (ch - 2 * DK) * 4;
     {
       const int k0 = ph;
       // the window offsets of the four nodes, then all their taps' loads,
@@ -232,7 +216,7 @@ __device__ __forceinline__ void front_conv(int tid, int p0, int p1, int nstart, 
       uint4 o[NB][WW > 4 ? 2 : 1];
 #pragma unroll
       for (int b = 0; b < NB; b++) {
-        const int node = nstart + nstride * min(k0 + b * NS, count - 1);  // past the end: a repeat, not stored
+        const int node = min(k0 + b * NS, count - 1);  // past the end: a repeat, not stored
         o[b][0] = sh_v4(wof + node * 32);
         if constexpr (WW > 4) o[b][1] = sh_v4(wof + node * 32 + 16);
       }
@@ -260,16 +244,61 @@ __device__ __forceinline__ void front_conv(int tid, int p0, int p1, int nstart, 
 #pragma unroll
       for (int b = 0; b < NB; b++) {
         if (k0 + b * NS < count) {
-          const int node = nstart + nstride * (k0 + b * NS);
+          const int node = k0 + b * NS;
           float a0, a1;
           f2_unpack(acc[b], a0, a1);
-          float y0 = silu_f(a0), y1 = silu_f(a1);
-          if (is_v) {
-            y0 = to_f32(from_f32<T>(y0));
-            y1 = to_f32(from_f32<T>(y1));
-          }
-          sh_st_f2(db + node * dstride, y0, y1);
+          sh_st_f2(db + node * R * 4, to_f32(from_f32<T>(silu_f(a0))), to_f32(from_f32<T>(silu_f(a1))));
         }
+      }
+    }
+  }
+}
+
+// Queries and keys of the fused verify's staged rows for a window of WW
+// taps: a warp per (node, vector) of this CTA's share (nodes crank, crank +
+// csize, ...; vector 0 the query, 1 the key), lane channels lane + 32e as
+// tv_gdn_front holds them: convolution (taps in order), SiLU, division by
+// the L2 norm (warp_l2_scale), rounding; the row then goes to every other
+// CTA of the cluster at the same offset.  With an even warp count a warp
+// keeps to one vector, so its weights stay in registers.
+template <int WW, typename T, typename KQ, int DK, int R, int WARPS>
+__device__ __forceinline__ void front_qk(int warp, int lane, uint32_t crank, uint32_t csize, int own, const T* xs,
+                                        const float* ws, const uint32_t* wof, KQ* qb, KQ* kb) {
+  constexpr int CPL = DK / 32, CPV = DK * static_cast<int>(sizeof(KQ)) / 16;
+  static_assert(WARPS % 2 == 0, "a warp keeps to one vector");
+  const int is_k = warp & 1;
+  float wr[CPL][WW];
+#pragma unroll
+  for (int e = 0; e < CPL; e++)
+#pragma unroll
+    for (int jj = 0; jj < WW; jj++) wr[e][jj] = ws[(is_k * DK + lane + 32 * e) * WW + jj];
+  for (int t = warp; t < 2 * own; t += WARPS) {
+    const int node = static_cast<int>(crank + csize * (t >> 1));
+    int off[WW];
+#pragma unroll
+    for (int jj = 0; jj < WW; jj++) off[jj] = static_cast<int>(wof[node * 8 + jj] / sizeof(T));
+    float val[CPL];
+#pragma unroll
+    for (int e = 0; e < CPL; e++) {
+      const int c = is_k * DK + lane + 32 * e;
+      float acc = 0.f;
+#pragma unroll
+      for (int jj = 0; jj < WW; jj++) acc = __fmaf_rn(wr[e][jj], to_f32(xs[off[jj] + c]), acc);
+      val[e] = silu_f(acc);
+    }
+    const float sc = warp_l2_scale<CPL>(val);
+    KQ* dst = (is_k ? kb : qb) + static_cast<size_t>(node) * DK;
+#pragma unroll
+    for (int e = 0; e < CPL; e++) dst[lane + 32 * e] = from_f32<KQ>(__fmul_rn(val[e], sc));
+    if (csize > 1) {
+      __syncwarp();
+      const uint32_t a0 = static_cast<uint32_t>(__cvta_generic_to_shared(dst));
+      for (int i = lane; i < CPV * static_cast<int>(csize - 1); i += 32) {
+        const uint32_t a = a0 + (i % CPV) * 16;
+        const uint32_t peer = (crank + 1 + static_cast<uint32_t>(i / CPV)) % csize;
+        uint4 v;
+        asm volatile("ld.shared.v4.b32 {%0, %1, %2, %3}, [%4];" : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w) : "r"(a));
+        peer_st_v4(a, peer, v);
       }
     }
   }
@@ -305,6 +334,7 @@ __global__ void __launch_bounds__(32 * WARPS) gdn_verify_kernel(const GdnVerifyP
   const int rb = blockIdx.x % rb_per_head;
   const int tid = threadIdx.x, j = tid % LPR;
   const int gi = tid / LPR;                 // lane group within the CTA
+  extern __shared__ float4 smem4[];
   const int row0 = rb * R + RPG * gi;       // the group's rows: row0 .. row0 + RPG - 1
 
   // this group's state rows first (they do not depend on the tree, and no
@@ -323,6 +353,21 @@ __global__ void __launch_bounds__(32 * WARPS) gdn_verify_kernel(const GdnVerifyP
       }
     }
   }
+  if constexpr (FRONT) {
+    // the convolution weights of the CTA's channels (constant: no earlier
+    // kernel writes them) start on their way before the wait
+    const int g0 = h / (p.Hv / p.Hk), vch0 = min(R, p.dv - rb * R);
+    float* ws = reinterpret_cast<float*>(reinterpret_cast<uint8_t*>(smem4) + p.front_off +
+                                         front_layout(p.n_max, p.W, DK, R, static_cast<int>(sizeof(T))).ws);
+    const size_t v0 = static_cast<size_t>(2) * p.Hk * DK + static_cast<size_t>(h) * p.dv + rb * R;
+    const int wq = DK * p.W / 4, wv = vch0 * p.W / 4;  // 16-byte chunks
+    for (int idx = tid; idx < 2 * wq + wv; idx += 32 * WARPS) {
+      const size_t src = idx < wq ? static_cast<size_t>(g0) * DK * p.W + idx * 4
+                                  : (idx < 2 * wq ? static_cast<size_t>(p.Hk + g0) * DK * p.W + (idx - wq) * 4
+                                                  : v0 * p.W + (idx - 2 * wq) * 4);
+      cp_async16_g(ws + idx * 4, p.wconv + src);
+    }
+  }
   pdl_wait();  // tree tables, status and node inputs come from earlier kernels
   pdl_trigger();
   MetaView mv = meta_view(const_cast<void*>(p.meta), p.n_total);
@@ -339,6 +384,7 @@ __global__ void __launch_bounds__(32 * WARPS) gdn_verify_kernel(const GdnVerifyP
     csize = cluster_size();
   }
   auto leave = [&]() {
+    if (FRONT) asm volatile("cp.async.wait_all;" ::: "memory");  // the weights' copies land before the CTA leaves
     if (FRONT && csize > 1) {
       cluster_sync_all();                  // the exchange of queries and keys
       if (p.norm_in) cluster_sync_all();  // the outputs gathered
@@ -360,7 +406,6 @@ __global__ void __launch_bounds__(32 * WARPS) gdn_verify_kernel(const GdnVerifyP
   }
   const int g = h / (p.Hv / p.Hk);
 
-  extern __shared__ float4 smem4[];
   float* slots = reinterpret_cast<float*>(smem4);  // [n_slots][R][DK]
   KQ* kb = reinterpret_cast<KQ*>(slots + static_cast<size_t>(p.n_slots) * R * DK);
   const size_t kq_bytes = (static_cast<size_t>(p.n_max) * DK * sizeof(KQ) + 15) / 16 * 16;
@@ -374,12 +419,13 @@ __global__ void __launch_bounds__(32 * WARPS) gdn_verify_kernel(const GdnVerifyP
     // The front end, as tv_gdn_front forms it (front_gdn.cuh), in one memory
     // round trip: the raw rows this CTA reads (the sequence's tail and its
     // nodes, at the key head's query and key channels and the CTA's value
-    // rows), the convolution weights of those channels and each node's
-    // window rows go to shared memory; then every channel of every node is
-    // convolved (taps in order) and passed through SiLU, values rounded to
-    // the layer type; then each query and key is divided by its L2 norm
-    // (lane sums in channel order, then the butterfly) and rounded.
-    constexpr int CH = 2 * DK + R, EPC = 16 / static_cast<int>(sizeof(T)), CPL = DK / 32;
+    // rows), the convolution weights of those channels (copied before the
+    // wait), each node's window rows and, with the norm inside, z and w_norm
+    // go to shared memory; then the values of the CTA's rows at every node
+    // (convolution, SiLU, rounding), and the queries and keys of the CTA's
+    // share of the nodes (convolution, SiLU, division by the L2 norm,
+    // rounding), sent to the cluster's other CTAs.
+    constexpr int CH = 2 * DK + R, EPC = 16 / static_cast<int>(sizeof(T));
     const int W = p.W, W1 = p.W - 1;
     const int vch = min(R, p.dv - rb * R);  // value channels this CTA holds
     const FrontLayout fl = front_layout(p.n_max, W, DK, R, static_cast<int>(sizeof(T)));
@@ -387,44 +433,75 @@ __global__ void __launch_bounds__(32 * WARPS) gdn_verify_kernel(const GdnVerifyP
     T* xs = reinterpret_cast<T*>(fb + fl.xs);
     float* ws = reinterpret_cast<float*>(fb + fl.ws);
     uint32_t* wof = reinterpret_cast<uint32_t*>(fb + fl.win);
-    float* vals = reinterpret_cast<float*>(fb + fl.vals);
     {
+      // the loads of this thread's node (one node a thread: n <= 64 < NT)
+      // go first, so their round trip overlaps the copies' issue
+      static_assert(TV_MAX_NODES <= NT, "one node per thread");
+      const bool has_node = tid < n;
+      int depth = 0, e_s = 0, e_g = 0;
+      ulonglong2 anc = make_ulonglong2(0ull, 0ull);  // the node's ancestors, one byte per depth
+      float a_in = 0.f, b_in = 0.f;
+      if (has_node) {
+        const int row = off + tid;
+        depth = mv.depth[row];
+        anc = *reinterpret_cast<const ulonglong2*>(mv.anc_at + static_cast<size_t>(row) * TV_MAX_PATH);
+        a_in = p.a_raw[static_cast<size_t>(row) * p.Hv + h];
+        b_in = p.b_raw[static_cast<size_t>(row) * p.Hv + h];
+        e_s = mv.sched[row];
+        e_g = mv.seg[row];
+      }
       const T* x = static_cast<const T*>(p.x);
       const T* tail = static_cast<const T*>(p.tail[s]);
       const int cq = DK / EPC, cpr = 2 * cq + vch / EPC;  // chunks of a row
       const size_t v0 = static_cast<size_t>(2) * p.Hk * DK + static_cast<size_t>(h) * p.dv + rb * R;
-      for (int idx = tid; idx < (W1 + n) * cpr; idx += NT) {
-        const int r = idx / cpr, c = idx % cpr;
-        const T* row = r < W1 ? tail + static_cast<size_t>(r) * p.C : x + static_cast<size_t>(off + r - W1) * p.C;
-        const size_t src = c < cq ? static_cast<size_t>(g) * DK + c * EPC
-                                  : (c < 2 * cq ? static_cast<size_t>(p.Hk + g) * DK + (c - cq) * EPC
-                                                : v0 + (c - 2 * cq) * EPC);
-        cp_async16_g(xs + static_cast<size_t>(r) * CH + c * EPC, row + src);
+      // a warp a row, lanes over the row's chunks (each lane's source
+      // channels fixed across rows)
+      constexpr int CU = ((2 * DK + R) * static_cast<int>(sizeof(T)) / 16 + 31) / 32;
+      const int lane0 = tid & 31, warp0 = tid >> 5;
+      size_t chan[CU];
+#pragma unroll
+      for (int u = 0; u < CU; u++) {
+        const int c = lane0 + 32 * u;
+        chan[u] = c < cq ? static_cast<size_t>(g) * DK + c * EPC
+                         : (c < 2 * cq ? static_cast<size_t>(p.Hk + g) * DK + (c - cq) * EPC : v0 + (c - 2 * cq) * EPC);
       }
-      const int wq = DK * W / 4, wv = vch * W / 4;  // 16-byte chunks of weights
-      for (int idx = tid; idx < 2 * wq + wv; idx += NT) {
-        const size_t src = idx < wq ? static_cast<size_t>(g) * DK * W + idx * 4
-                                    : (idx < 2 * wq ? static_cast<size_t>(p.Hk + g) * DK * W + (idx - wq) * 4
-                                                    : v0 * W + (idx - 2 * wq) * 4);
-        cp_async16_g(ws + idx * 4, p.wconv + src);
+      for (int r = warp0; r < W1 + n; r += WARPS) {
+        const T* row = r < W1 ? tail + static_cast<size_t>(r) * p.C : x + static_cast<size_t>(off + r - W1) * p.C;
+        T* dst = xs + static_cast<size_t>(r) * CH;
+#pragma unroll
+        for (int u = 0; u < CU; u++)
+          if (lane0 + 32 * u < cpr) cp_async16_g(dst + (lane0 + 32 * u) * EPC, row + chan[u]);
+      }
+      if (p.norm_in) {
+        // z of the nodes this CTA normalizes (rb, rb + rbph, ...) and w_norm
+        T* zs = reinterpret_cast<T*>(reinterpret_cast<uint8_t*>(smem4) + p.obuf_off) +
+                (static_cast<size_t>(p.n_max) * R + static_cast<size_t>((p.n_max + rb_per_head - 1) / rb_per_head) *
+                                                        rb_per_head * R);
+        float* wns = reinterpret_cast<float*>(zs + static_cast<size_t>((p.n_max + rb_per_head - 1) / rb_per_head) *
+                                                       rb_per_head * R);
+        const int nz = (n - rb + rb_per_head - 1) / rb_per_head, cz = p.dv / EPC;  // rows, chunks of a row
+        const int dvp = rb_per_head * R;
+        const T* z = static_cast<const T*>(p.z);
+        for (int idx = tid; idx < nz * cz; idx += NT) {
+          const int k = idx / cz, c = idx % cz;
+          cp_async16_g(zs + static_cast<size_t>(k) * dvp + c * EPC,
+                       z + (static_cast<size_t>(off + rb + k * rb_per_head) * p.Hv + h) * p.dv + c * EPC);
+        }
+        for (int idx = tid; idx < p.dv / 4; idx += NT) cp_async16_g(wns + idx * 4, p.w_norm + idx * 4);
       }
       asm volatile("cp.async.commit_group;" ::: "memory");
-      for (int idx = tid; idx < n; idx += NT) {
-        const int row = off + idx;
-        const int depth = mv.depth[row];
-        // the node's ancestors (one byte per depth), one 16-byte load beside the depth's
-        const ulonglong2 anc = *reinterpret_cast<const ulonglong2*>(mv.anc_at + static_cast<size_t>(row) * TV_MAX_PATH);
+      if (has_node) {
+        const int idx = tid;
         for (int jj = 0; jj < W; jj++) {
           const int m = depth + jj - W1;  // window element jj: ancestor at depth m, or tail row m + W - 1
           const int am = static_cast<int8_t>(((m < 8 ? anc.x : anc.y) >> (8 * (m & 7))) & 0xFF);
           wof[idx * 8 + jj] = static_cast<uint32_t>((m < 0 ? m + W1 : W1 + am) * CH * static_cast<int>(sizeof(T)));
         }
-        const size_t ah = static_cast<size_t>(row) * p.Hv + h;
         float a, b;
-        front_gates(p.a_raw[ah], p.b_raw[ah], a, b);
+        front_gates(a_in, b_in, a, b);
         nc[idx] = make_float4(a, b, 0.f, 0.f);
-        sch[idx] = mv.sched[row];
-        sgt[idx] = mv.seg[row];
+        sch[idx] = e_s;
+        sgt[idx] = e_g;
       }
       if (vch < R)
         for (int idx = tid; idx < n * R; idx += NT)
@@ -436,16 +513,15 @@ __global__ void __launch_bounds__(32 * WARPS) gdn_verify_kernel(const GdnVerifyP
       const uint32_t xs_s = static_cast<uint32_t>(__cvta_generic_to_shared(xs));
       const uint32_t ws_s = static_cast<uint32_t>(__cvta_generic_to_shared(ws));
       const uint32_t wo_s = static_cast<uint32_t>(__cvta_generic_to_shared(wof));
-      const uint32_t va_s = static_cast<uint32_t>(__cvta_generic_to_shared(vals));
       const uint32_t vb_s = static_cast<uint32_t>(__cvta_generic_to_shared(vb));
-      const uint32_t qb_s = static_cast<uint32_t>(__cvta_generic_to_shared(qb));
-      const uint32_t kb_s = static_cast<uint32_t>(__cvta_generic_to_shared(kb));
-      // this CTA's share of the queries and keys (nodes crank, crank + csize,
-      // ...), then the values of its rows at every node
+      // the values of this CTA's rows at every node (threads over channel
+      // pairs), then this CTA's share of the queries and keys (warps over
+      // nodes crank, crank + csize, ...), each row sent to the cluster
       const int own = (n - static_cast<int>(crank) + static_cast<int>(csize) - 1) / static_cast<int>(csize);
+      const int warp = tid >> 5, lane = tid & 31;
 #define TV_FRONT_CONV(WW)                                                                                   \
-  front_conv<WW, T, KQ, DK, R, NT>(tid, 0, DK, crank, csize, own, xs_s, ws_s, wo_s, va_s, vb_s, qb_s, kb_s); \
-  front_conv<WW, T, KQ, DK, R, NT>(tid, DK, DK + vch / 2, 0, 1, n, xs_s, ws_s, wo_s, va_s, vb_s, qb_s, kb_s)
+  front_values<WW, T, DK, R, NT>(tid, vch, n, xs_s, ws_s, wo_s, vb_s);                                      \
+  front_qk<WW, T, KQ, DK, R, WARPS>(warp, lane, crank, csize, own, xs, ws, wof, qb, kb)
       switch (W) {
         case 1: TV_FRONT_CONV(1); break;
         case 2: TV_FRONT_CONV(2); break;
@@ -458,52 +534,9 @@ __global__ void __launch_bounds__(32 * WARPS) gdn_verify_kernel(const GdnVerifyP
       }
 #undef TV_FRONT_CONV
     }
-    __syncthreads();
-    const int warp = tid >> 5, lane = tid & 31;
-    // two heads a warp at a time (task w: the CTA's node w / 2, query or key)
-    const int own = (n - static_cast<int>(crank) + static_cast<int>(csize) - 1) / static_cast<int>(csize);
-    for (int w0 = warp; w0 < 2 * own; w0 += 2 * WARPS) {
-      const int tk[2] = {w0, w0 + WARPS < 2 * own ? w0 + WARPS : w0};
-      float val[2][CPL], sc[2];
-#pragma unroll
-      for (int i = 0; i < 2; i++) {
-        const int node = static_cast<int>(crank + csize * (tk[i] >> 1)), is_k = tk[i] & 1;
-        const float* src = sizeof(KQ) == 2 ? vals + node * 2 * DK + is_k * DK
-                                           : reinterpret_cast<const float*>((is_k ? kb : qb) + static_cast<size_t>(node) * DK);
-#pragma unroll
-        for (int e = 0; e < CPL; e++) val[i][e] = src[lane + 32 * e];
-      }
-      warp_l2_scales<CPL, 2>(val, sc);
-#pragma unroll
-      for (int i = 0; i < 2; i++) {
-        if (i == 1 && tk[1] == tk[0]) break;
-        const int node = static_cast<int>(crank + csize * (tk[i] >> 1)), is_k = tk[i] & 1;
-        KQ* dst = (is_k ? kb : qb) + static_cast<size_t>(node) * DK;
-#pragma unroll
-        for (int e = 0; e < CPL; e++) dst[lane + 32 * e] = from_f32<KQ>(__fmul_rn(val[i][e], sc[i]));
-      }
-    }
-    __syncthreads();
-    if (csize > 1) {
-      // push this CTA's share (its nodes' key and query rows) into every
-      // other CTA of the cluster, same offsets; the barrier then makes all
-      // shares visible everywhere (and no CTA leaves with writes pending)
-      constexpr int CPV = DK * static_cast<int>(sizeof(KQ)) / 16;  // 16-byte chunks of a row
-      const uint32_t kb_s = static_cast<uint32_t>(__cvta_generic_to_shared(kb));
-      const uint32_t qb_s = static_cast<uint32_t>(__cvta_generic_to_shared(qb));
-      const int per = own * 2 * CPV;
-      for (int idx = tid; idx < per * static_cast<int>(csize - 1); idx += NT) {
-        const int pi = idx / per, rem = idx % per;
-        const uint32_t peer = (crank + 1 + static_cast<uint32_t>(pi)) % csize;
-        const int node = static_cast<int>(crank) + static_cast<int>(csize) * (rem / (2 * CPV));
-        const int r2 = rem % (2 * CPV);
-        const uint32_t a = (r2 < CPV ? kb_s : qb_s) + node * DK * static_cast<int>(sizeof(KQ)) + (r2 % CPV) * 16;
-        uint4 v;
-        asm volatile("ld.shared.v4.b32 {%0, %1, %2, %3}, [%4];" : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w) : "r"(a));
-        peer_st_v4(a, peer, v);
-      }
-      cluster_sync_all();
-    }
+    // every CTA's rows in place everywhere (the cluster's barrier), or this
+    // CTA's own
+    if (csize > 1) cluster_sync_all(); else __syncthreads();
   } else {
   // Stage the tree's keys and queries of this key head (cp.async), the
   // values of this CTA's rows, alpha, beta and the steps.  Every global load
@@ -686,11 +719,9 @@ __global__ void __launch_bounds__(32 * WARPS) gdn_verify_kernel(const GdnVerifyP
   if constexpr (FRONT) {
     if (p.norm_in) {
       // gated norm of (node, head h) for this CTA's nodes rb, rb + rbph, ...,
-      // two a warp at a time; z and w_norm load before the barrier that
-      // completes the gathered outputs
+      // two a warp at a time (z and w_norm staged with the front end)
       constexpr int CPL = DK / 32;  // the front end's dv = dk
       const int warp = tid >> 5, lane = tid & 31;
-      const T* z = static_cast<const T*>(p.z);
       T* o_out = static_cast<T*>(p.out);
       // gather: node k's rows go to the head's CTA k mod rb_per_head, which
       // holds the node's dv outputs at obuf[k / rb_per_head][.] (this CTA's
@@ -717,36 +748,26 @@ __global__ void __launch_bounds__(32 * WARPS) gdn_verify_kernel(const GdnVerifyP
         }
       }
       auto row = [&](int k) { return (static_cast<size_t>(off + rb + k * rb_per_head) * p.Hv + h) * p.dv; };
-      auto zload = [&](int k, float (&zz)[CPL]) {
-        if (rb + k * rb_per_head < n) {
+      const int nrows = (p.n_max + rb_per_head - 1) / rb_per_head;
+      const T* zs = obuf + static_cast<size_t>(nrows) * dvp;  // staged z rows, then w_norm
+      const float* wns = reinterpret_cast<const float*>(zs + static_cast<size_t>(nrows) * dvp);
+      float wn[CPL];
 #pragma unroll
-          for (int e = 0; e < CPL; e++) zz[e] = to_f32(z[row(k) + lane + 32 * e]);
-        }
-      };
-      float wn[CPL], za[CPL], zb[CPL];
-#pragma unroll
-      for (int e = 0; e < CPL; e++) wn[e] = p.w_norm[lane + 32 * e];
-      zload(warp, za);
-      zload(warp + WARPS, zb);
+      for (int e = 0; e < CPL; e++) wn[e] = wns[lane + 32 * e];
       if (csize > 1) cluster_sync_all(); else __syncthreads();
       for (int k = warp; rb + k * rb_per_head < n; k += 2 * WARPS) {
         const int k2 = k + WARPS;
         const bool has2 = rb + k2 * rb_per_head < n;
-        float oa[CPL], ob[CPL], na[CPL], nb[CPL];
+        float oa[CPL], ob[CPL], za[CPL], zb[CPL];
 #pragma unroll
         for (int e = 0; e < CPL; e++) {
           oa[e] = to_f32(obuf[k * dvp + lane + 32 * e]);
+          za[e] = to_f32(zs[k * dvp + lane + 32 * e]);
           ob[e] = has2 ? to_f32(obuf[k2 * dvp + lane + 32 * e]) : 0.f;
+          zb[e] = has2 ? to_f32(zs[k2 * dvp + lane + 32 * e]) : 0.f;
         }
-        zload(k + 2 * WARPS, na);
-        zload(k2 + 2 * WARPS, nb);
         gated_norm_vals<T, CPL>(oa, za, wn, o_out + row(k), lane);
         if (has2) gated_norm_vals<T, CPL>(ob, zb, wn, o_out + row(k2), lane);
-#pragma unroll
-        for (int e = 0; e < CPL; e++) {
-          za[e] = na[e];
-          zb[e] = nb[e];
-        }
       }
     }
   }
@@ -858,10 +879,13 @@ static size_t fused_smem(const GdnVerifyParams& p, bool norm_in, int* front_off,
     smem = *front_off + fb;
   }
   *obuf_off = static_cast<int>((smem + 15) / 16 * 16);
-  const int rbph = (p.dv + Sh::R - 1) / Sh::R;  // stage [n_max][R], gathered [ceil(n_max / rbph)][rbph R]
+  const int rbph = (p.dv + Sh::R - 1) / Sh::R;
+  // stage [n_max][R], gathered outputs and staged z [ceil(n_max / rbph)][rbph R] each, w_norm [rbph R] f32
   if (norm_in)
-    smem = *obuf_off + (static_cast<size_t>(p.n_max) + static_cast<size_t>((p.n_max + rbph - 1) / rbph) * rbph) *
-                           Sh::R * sizeof(T);
+    smem = *obuf_off +
+           (static_cast<size_t>(p.n_max) + 2 * static_cast<size_t>((p.n_max + rbph - 1) / rbph) * rbph) * Sh::R *
+               sizeof(T) +
+           static_cast<size_t>(rbph) * Sh::R * 4;
   return smem;
 }
 
@@ -999,7 +1023,8 @@ extern "C" tv_status tv_gdn_tree_verify_fused(const tv_gdn_layer* l, const tv_gd
   if (f->dtype != l->dtype || f->Hk != l->Hk || f->Hv != l->Hv || f->dk != l->dk || f->dv != l->dv)
     return TV_ERR_SHAPE;
   if (!x || !a_raw || !b_raw || !z || !w_norm || !out) return TV_ERR_ARG;
-  if (!aligned16(out) || !aligned16(x) || !aligned16(f->wconv)) return TV_ERR_ALIGN;
+  if (!aligned16(out) || !aligned16(x) || !aligned16(f->wconv) || !aligned16(z) || !aligned16(w_norm))
+    return TV_ERR_ALIGN;
   GdnVerifyParams p{};
   for (int s = 0; s < t->n_seq; s++) {
     if (!l->S[s]) return TV_ERR_ARG;
