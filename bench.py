@@ -331,6 +331,79 @@ def oracle_worker(args):
 # ---------------------------------------------------------------------------
 # our arm
 # ---------------------------------------------------------------------------
+def gdn_front_timing(r, n_rep: int = 10):
+    """Per GDN layer of the round: the front end fused into the verify
+    (tv_gdn_tree_verify_fused: raw projections in, gated-norm outputs out)
+    against the three calls it replaces (tv_gdn_front -> tv_gdn_tree_verify ->
+    tv_gdn_out_norm), each over all the round's GDN layers (their own states,
+    synthetic raw inputs of the layer's shape, convolution width 4) captured
+    in one CUDA graph on the round's tree and replayed; CUDA events, us per
+    layer (median over replays).  The outputs of both are checked equal."""
+    from speculative_tree_verify_masked_gb300 import binding as B
+
+    cfg = r.cfg
+    s = cfg.shapes
+    W = 4
+    C = 2 * s.Hk * s.dk + s.Hv * s.dv
+    n = sum(r.n_nodes)
+    dt = s.kv_dtype
+    dev = r.device
+    g = torch.Generator(device=dev).manual_seed(4242)
+    rn = lambda *shape, std=1.0, d=torch.float32: (torch.randn(*shape, generator=g, device=dev) * std).to(d)
+    e = lambda *shape, d=dt: torch.empty(*shape, dtype=d, device=dev)
+    layers = []
+    for li, gl in r.gdn.items():
+        tails = [rn(W - 1, C, d=dt) for _ in range(cfg.n_seq)]
+        layers.append(dict(gl=gl["layer"], fl=B.GdnFrontLayer(s.Hk, s.Hv, s.dk, s.dv, rn(C, W, std=0.5), tails, dt),
+                           tails=tails, x=rn(n, C, d=dt), a=rn(n, s.Hv), b=rn(n, s.Hv), z=rn(n, s.Hv, s.dv, d=dt),
+                           wn=1.0 + rn(s.dv, std=0.1), q=e(n, s.Hk, s.dk), k=e(n, s.Hk, s.dk), v=e(n, s.Hv, s.dv),
+                           al=e(n, s.Hv, d=torch.float32), be=e(n, s.Hv, d=torch.float32), o=e(n, s.Hv, s.dv),
+                           out3=e(n, s.Hv, s.dv), out1=e(n, s.Hv, s.dv)))
+    B.tv_tree_prepare(r.tree)
+
+    def three():
+        for L in layers:
+            B.tv_gdn_front(L["fl"], r.tree, cfg.n_seq, L["x"], L["a"], L["b"], L["q"], L["k"], L["v"], L["al"], L["be"])
+            B.tv_gdn_tree_verify(L["gl"], r.tree, L["q"], L["k"], L["v"], L["al"], L["be"], L["o"], r.gdn_scale)
+            B.tv_gdn_out_norm(L["fl"], n, L["o"], L["z"], L["wn"], L["out3"])
+
+    def fused():
+        for L in layers:
+            B.tv_gdn_tree_verify_fused(L["gl"], L["fl"], r.tree, L["x"], L["a"], L["b"], L["z"], L["wn"], L["out1"],
+                                       r.gdn_scale)
+
+    res = {}
+    for name, fn in (("three_calls", three), ("fused", fused)):
+        side = torch.cuda.Stream()
+        side.wait_stream(torch.cuda.current_stream())
+        with torch.cuda.stream(side):
+            fn()
+        torch.cuda.current_stream().wait_stream(side)
+        torch.cuda.synchronize()
+        graph = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(graph):
+            fn()
+        for _ in range(3):
+            graph.replay()
+        ts = []
+        for _ in range(n_rep):
+            a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            a.record()
+            graph.replay()
+            b.record()
+            torch.cuda.synchronize()
+            ts.append(a.elapsed_time(b) * 1e3 / len(layers))
+        res[name] = round(statistics.median(ts), 2)
+        del graph
+    assert r.status() == 0
+    same = all(torch.equal(L["out1"].view(torch.int16), L["out3"].view(torch.int16)) for L in layers)
+    assert same, "fused GDN front end differs from the three calls"
+    return {"fused_us_per_layer": res["fused"], "three_calls_us_per_layer": res["three_calls"],
+            "layers": len(layers), "conv_width": W, "bit_equal": same,
+            "how": "each form over all GDN layers of the round in one CUDA graph (programmatic launch as in the "
+                   "round), CUDA events around replays, median of " + str(n_rep)}
+
+
 def max_over_ranks(x: float, world: int, device) -> float:
     """The largest of every rank's value: a replicated job is as slow as its
     slowest replica.  One rank: the value itself."""
@@ -412,6 +485,10 @@ def run_ours(args, rank, world, local_rank):
         del marked
     attn_timing = ("CUDA events around each layer's verify call, captured in a graph of the same round and "
                    "replayed after the timed region (median over replays of the mean over layers)")
+
+    # --- the GDN front end fused into the verify, against the three calls ---
+    gdn_front = gdn_front_timing(r) if (r.gdn and cfg.shapes.kv_dtype == torch.bfloat16 and not args.no_front) \
+        else None
 
     # --- eager rounds (launch overhead included), for context ---------------
     stream = torch.cuda.current_stream()
@@ -521,6 +598,7 @@ def run_ours(args, rank, world, local_rank):
                      "how": "CUDA events around each layer's verify call in a marked copy of the round's graph "
                             "(median over replays of the mean over layers of that kind; the marks cut the "
                             "programmatic launch overlap between neighbouring layers)"},
+        "gdn_front_fused": gdn_front,
         "roofline": roof, "roofline_round": roof_round, "cpu_baseline": cpu, "e2e": e2e, "clocks": clk,
         "gpu_launches": launches_per_round * args.steps,
     }
@@ -584,6 +662,7 @@ def main():
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-clocks", action="store_true")
+    ap.add_argument("--no-front", action="store_true", help="skip the fused GDN front-end timing")
     ap.add_argument("--kv-pool", action="store_true", help="attention caches from the KV pool (tv_kvpool_*)")
     ap.add_argument("--kv-window", type=int, default=None,
                     help="cache rows per sequence (default: the context plus 64)")
