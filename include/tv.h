@@ -333,18 +333,25 @@ tv_status tv_gdn_front(const tv_gdn_front_layer* layer, const tv_tree* tree, int
 tv_status tv_gdn_out_norm(const tv_gdn_front_layer* layer, int32_t rows, const void* o, const void* z,
                           const float* w_norm, void* out, tv_stream stream);
 
-/* tv_gdn_front, tv_gdn_tree_verify and tv_gdn_out_norm in two launches: the
+/* tv_gdn_front, tv_gdn_tree_verify and tv_gdn_out_norm in one launch: the
  * verify kernel forms each node's query, key, value and gates from the raw
  * projections inside its staging (no q, k, v, alpha or beta in memory), runs
- * the recurrence, writes o to out; a second kernel applies the gated norm to
- * out in place (the norm of a (node, value head) needs all dv rows, which
- * two verify CTAs share).  The result equals the three calls bit for bit.
- *  layer  tv_gdn_tree_verify's layer (states updated the same way: none)
- *  front  the front-end layer: same dtype, Hk, Hv, dk, dv
+ * the recurrence and applies the gated norm to its outputs.  The CTAs that
+ * share a key head run as one thread-block cluster: they split the key head's
+ * queries and keys by node and exchange them, and gather each (node, value
+ * head)'s dv outputs for the norm, through distributed shared memory.  Where
+ * no such cluster fits (more than 16 CTAs to a key head, or the shared memory
+ * of the gather) the norm runs as a second kernel over out.  The result
+ * equals the three calls bit for bit.
+ *  layer  tv_gdn_tree_verify's layer (states read only, as there)
+ *  front  the front-end layer: same dtype, Hk, Hv, dk, dv; wconv and each
+ *         tail 16-byte aligned
  *  x [n_total][C], a_raw, b_raw [n_total][Hv], z [n_total][Hv][dv], w_norm [dv]
+ *         (x, z, w_norm 16-byte aligned)
  *  out    [n_total][Hv][dv], 16-byte aligned
  * Errors as tv_gdn_tree_verify's and tv_gdn_front's; TV_ERR_SHAPE when the two
- * layers disagree.  The tails are read only. */
+ * layers disagree, TV_ERR_ALIGN for a misaligned buffer.  The tails are read
+ * only. */
 tv_status tv_gdn_tree_verify_fused(const tv_gdn_layer* layer, const tv_gdn_front_layer* front, const tv_tree* tree,
                                    const void* x, const float* a_raw, const float* b_raw, const void* z,
                                    const float* w_norm, void* out, float scale, tv_stream stream);
