@@ -19,6 +19,7 @@ from speculative_tree_verify_masked_gb300 import synth
 pytestmark = pytest.mark.gpu
 
 W = 4
+TV_ERR_TREE = 5
 
 
 def check_gated_norm(got, ref, gate, stages, what):
@@ -160,16 +161,18 @@ def test_gdn_front_verify_rows_equal_decode_rows(cfg_id):
         assert np.array_equal(f64(tail2), G.commit_tail(f64(c.tail0), f64(c.x), path))
 
 
-@pytest.mark.parametrize("cfg_id,width", [(0, 1), (0, 4), (1, 8), (2, 4), (3, 4), (4, 4)])
-def test_gdn_fused_equals_front_verify_norm(cfg_id, width):
+@pytest.mark.parametrize("cfg_id,width,dt", [(0, 1, None), (0, 4, None), (1, 8, None), (2, 4, None), (3, 4, None),
+                                             (4, 4, None), (1, 4, torch.float32), (4, 2, torch.float32)])
+def test_gdn_fused_equals_front_verify_norm(cfg_id, width, dt):
     """tv_gdn_tree_verify_fused gives the bits of tv_gdn_front ->
     tv_gdn_tree_verify -> tv_gdn_out_norm on every sequence of the workload's
     trees (one 8/16/64/32-node tree, four 16-node trees), for convolution
-    widths 1 (no tail), 4 and 8 (windows reaching past the root into each
-    sequence's own tail); states and tails stay as they were."""
+    widths 1 (no tail), 2, 4 and 8 (windows reaching past the root into each
+    sequence's own tail), bf16 and fp32 layers (fp32 on the 27B shapes runs
+    the key-head clusters too); states and tails stay as they were."""
     cfg = synth.workload(cfg_id)
     sh = cfg.shapes
-    dt = sh.kv_dtype
+    dt = dt or sh.kv_dtype
     parents = [synth.tree_and_tokens(cfg, s)[0] for s in range(cfg.n_seq)]
     n = sum(len(p) for p in parents)
     C = 2 * sh.Hk * sh.dk + sh.Hv * sh.dv
@@ -203,3 +206,31 @@ def test_gdn_fused_equals_front_verify_norm(cfg_id, width):
     for s in range(cfg.n_seq):
         assert torch.equal(bits(S2[s]), bits(S0[s])), f"sequence {s}: the verify changed a state"
         assert torch.equal(bits(tails[s]), bits(tails0[s])), f"sequence {s}: the verify changed a tail"
+
+
+def test_gdn_fused_after_a_malformed_tree_does_nothing():
+    """A launch whose status word already holds an error (here a malformed
+    tree in the second of four sequences) leaves the fused call a no-op:
+    every CTA, clusters included, takes the early path through the cluster's
+    barriers and returns; the output keeps its fill and the call returns."""
+    cfg = synth.workload(4)
+    sh = cfg.shapes
+    dt = sh.kv_dtype
+    parents = [synth.tree_and_tokens(cfg, s)[0] for s in range(cfg.n_seq)]
+    parents[1] = list(parents[1])
+    parents[1][3] = 7  # a parent after its child
+    n = sum(len(p) for p in parents)
+    C = 2 * sh.Hk * sh.dk + sh.Hv * sh.dv
+    g = torch.Generator(device="cuda").manual_seed(1300)
+    rn = lambda *shape, std=1.0, d=torch.float32: (torch.randn(*shape, generator=g, device="cuda") * std).to(d)
+    tails = [rn(3, C, d=dt) for _ in parents]
+    fl = B.GdnFrontLayer(sh.Hk, sh.Hv, sh.dk, sh.dv, rn(C, 4, std=0.5), tails, dt)
+    S = [rn(sh.Hv, sh.dv, sh.dk, std=0.1) for _ in parents]
+    tree = B.Tree(parents)
+    B.tv_tree_prepare(tree)
+    out = torch.full((n, sh.Hv, sh.dv), 7.0, dtype=dt, device="cuda")
+    B.tv_gdn_tree_verify_fused(B.GdnLayer(S, sh.Hk, dt), fl, tree, rn(n, C, d=dt), rn(n, sh.Hv), rn(n, sh.Hv),
+                               rn(n, sh.Hv, sh.dv, d=dt), 1.0 + rn(sh.dv, std=0.1), out, sh.dk ** -0.5)
+    torch.cuda.synchronize()
+    assert tree.status_code() == TV_ERR_TREE
+    assert bool((out == 7.0).all()), "an output was written after the error"
