@@ -172,11 +172,31 @@ def test_gdn_fused_equals_front_verify_norm(cfg_id, width, dt):
     the key-head clusters too); states and tails stay as they were."""
     cfg = synth.workload(cfg_id)
     sh = cfg.shapes
-    dt = dt or sh.kv_dtype
     parents = [synth.tree_and_tokens(cfg, s)[0] for s in range(cfg.n_seq)]
+    fused_vs_three(parents, sh.Hk, sh.Hv, sh.dk, dt or sh.kv_dtype, width, 1200 + 10 * cfg_id + width)
+
+
+@pytest.mark.parametrize("Hk,Hv,dk,n_seq,width", [(4, 8, 64, 2, 4), (2, 8, 128, 1, 3), (8, 8, 128, 3, 5),
+                                                  (2, 2, 64, 2, 8)])
+def test_gdn_fused_other_head_shapes(Hk, Hv, dk, n_seq, width):
+    """The fused call on head shapes beside the workloads': dk = dv = 64
+    (a whole head in one CTA), four value heads to a key head (clusters of
+    eight), one value head to a key head (clusters of two), merged trees of
+    20-40 nodes, bf16."""
+    rng = np.random.default_rng(Hk * 100 + Hv + dk + width)
+    parents = [synth.merged_tree(int(rng.integers(20, 41)), 10, rng) for _ in range(n_seq)]
+    fused_vs_three(parents, Hk, Hv, dk, torch.bfloat16, width, 1400 + Hk + Hv + dk + width)
+
+
+def fused_vs_three(parents, Hk, Hv, dk, dt, width, seed):
+    """tv_gdn_tree_verify_fused against tv_gdn_front -> tv_gdn_tree_verify ->
+    tv_gdn_out_norm on the same inputs: bitwise equal outputs, states and
+    tails untouched, status clean."""
+    sh = type("Shapes", (), dict(Hk=Hk, Hv=Hv, dk=dk, dv=dk))
+    n_seq = len(parents)
     n = sum(len(p) for p in parents)
     C = 2 * sh.Hk * sh.dk + sh.Hv * sh.dv
-    g = torch.Generator(device="cuda").manual_seed(1200 + 10 * cfg_id + width)
+    g = torch.Generator(device="cuda").manual_seed(seed)
     rn = lambda *shape, std=1.0, d=torch.float32: (torch.randn(*shape, generator=g, device="cuda") * std).to(d)
     x = rn(n, C, d=dt)
     a_raw, b_raw = rn(n, sh.Hv), rn(n, sh.Hv)
@@ -193,7 +213,7 @@ def test_gdn_fused_equals_front_verify_norm(cfg_id, width, dt):
     alpha, beta = e(n, sh.Hv, d=torch.float32), e(n, sh.Hv, d=torch.float32)
     o, ref = e(n, sh.Hv, sh.dv), e(n, sh.Hv, sh.dv)
     S1 = [s.clone() for s in S0]
-    B.tv_gdn_front(fl, tree, cfg.n_seq, x, a_raw, b_raw, q, k, v, alpha, beta)
+    B.tv_gdn_front(fl, tree, n_seq, x, a_raw, b_raw, q, k, v, alpha, beta)
     B.tv_gdn_tree_verify(B.GdnLayer(S1, sh.Hk, dt), tree, q, k, v, alpha, beta, o, scale)
     B.tv_gdn_out_norm(fl, n, o, z, w_norm, ref)
     S2 = [s.clone() for s in S0]
@@ -203,7 +223,7 @@ def test_gdn_fused_equals_front_verify_norm(cfg_id, width, dt):
     torch.cuda.synchronize()
     assert tree.status_code() == 0
     assert torch.equal(bits(out), bits(ref)), "fused output != front -> verify -> norm"
-    for s in range(cfg.n_seq):
+    for s in range(n_seq):
         assert torch.equal(bits(S2[s]), bits(S0[s])), f"sequence {s}: the verify changed a state"
         assert torch.equal(bits(tails[s]), bits(tails0[s])), f"sequence {s}: the verify changed a tail"
 
