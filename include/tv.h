@@ -119,8 +119,11 @@ typedef struct {
  * predecessor has returned (the attention split and tail kernels, GDN
  * verify), or at exit, so everything older than the predecessor has
  * completed.  Before
- * waiting, a kernel reads only the recurrent states (GDN verify; GDN commit,
- * whose predecessor is always a kernel of the same commit call), the lengths
+ * waiting, a kernel reads only the recurrent states (GDN verify, which also
+ * reads its sequence's node range from the tree tables to prefetch its node
+ * inputs into L2, a cache hint clamped to the buffers; the fused GDN verify
+ * copies its convolution weights; GDN commit, whose predecessor is always a
+ * kernel of the same commit call), the lengths
  * and node_off (attention; the split kernel also prefetches K/V tiles and
  * its first query rows into L2, which is only a cache hint), and the tree tables, the query rows, the
  * tree's K/V rows and the cache rows of its own segment (the attention tail,

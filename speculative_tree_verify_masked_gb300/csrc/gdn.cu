@@ -353,6 +353,29 @@ __global__ void __launch_bounds__(32 * WARPS) gdn_verify_kernel(const GdnVerifyP
       }
     }
   }
+  if constexpr (!FRONT) {
+    // this CTA's node inputs into L2 while the previous kernel finishes (the
+    // key head's key and query rows, the head's value rows of this CTA): the
+    // node range comes from the tree tables, written at the start of the
+    // round, and is clamped to the buffers, so a stale read only warms
+    // other rows of the same inputs
+    const SeqInfo si = meta_view(const_cast<void*>(p.meta), p.n_total).seq[s];
+    const int n0 = min(max(si.n, 0), min(p.n_max, p.n_total)), off0 = min(max(si.off, 0), p.n_total - n0);
+    const int g0 = h / (p.Hv / p.Hk);
+    constexpr int KL = DK * static_cast<int>(sizeof(T)) / 128;  // 128-byte lines of a key row
+    for (int idx = tid; idx < n0 * (2 * KL + 1); idx += 32 * WARPS) {
+      const int node = off0 + idx / (2 * KL + 1), part = idx % (2 * KL + 1);
+      const char* a;
+      if (part < 2 * KL) {
+        const T* base = static_cast<const T*>(part < KL ? p.k : p.q);
+        a = reinterpret_cast<const char*>(base + (static_cast<size_t>(node) * p.Hk + g0) * DK) + (part % KL) * 128;
+      } else {
+        a = reinterpret_cast<const char*>(static_cast<const T*>(p.v) +
+                                          (static_cast<size_t>(node) * p.Hv + h) * p.dv + rb * R);
+      }
+      asm volatile("prefetch.global.L2 [%0];" ::"l"(a));
+    }
+  }
   if constexpr (FRONT) {
     // the convolution weights of the CTA's channels (constant: no earlier
     // kernel writes them) start on their way before the wait
