@@ -123,7 +123,8 @@ typedef struct {
  * reads its sequence's node range from the tree tables to prefetch its node
  * inputs into L2, a cache hint clamped to the buffers; the fused GDN verify
  * copies its convolution weights; GDN commit, whose predecessor is always a
- * kernel of the same commit call), the lengths
+ * kernel of the same commit call, and which prefetches every node's key and
+ * value rows into L2 from the tree tables' node range), the lengths
  * and node_off (attention; the split kernel also prefetches K/V tiles and
  * its first query rows into L2, which is only a cache hint), and the tree tables, the query rows, the
  * tree's K/V rows and the cache rows of its own segment (the attention tail,

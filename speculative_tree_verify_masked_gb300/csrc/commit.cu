@@ -115,6 +115,25 @@ __global__ void __launch_bounds__(128) gdn_commit_kernel(const GdnCommitParams p
 #pragma unroll
     for (int e = 0; e < kPairs; e++) st1[e] = 0ull;
   }
+  {
+    // the keys and values of every node of the sequence into L2 while the
+    // accept kernel finishes (the accepted path is only known after the
+    // wait): node range from the tree tables, clamped to the buffers (a
+    // cache hint)
+    const SeqInfo si = meta_view(const_cast<void*>(p.meta), p.n_total).seq[s];
+    const int n0 = min(max(si.n, 0), min(TV_MAX_NODES, p.n_total)), off0 = min(max(si.off, 0), p.n_total - n0);
+    const int g0 = h / (p.Hv / p.Hk);
+    constexpr int KL = DK * static_cast<int>(sizeof(T)) / 128;  // 128-byte lines of a key row
+    for (int idx = threadIdx.x; idx < n0 * (KL + 1); idx += 128) {
+      const int node = off0 + idx / (KL + 1), part = idx % (KL + 1);
+      const char* ad = part < KL ? reinterpret_cast<const char*>(static_cast<const T*>(lay.k) +
+                                                                 (static_cast<size_t>(node) * p.Hk + g0) * DK) +
+                                       part * 128
+                                 : reinterpret_cast<const char*>(static_cast<const T*>(lay.v) +
+                                                                 (static_cast<size_t>(node) * p.Hv + h) * p.dv + rb * R);
+      asm volatile("prefetch.global.L2 [%0];" ::"l"(ad));
+    }
+  }
   pdl_wait();
   if (status_bad(p.status)) return;
   const int g = h / (p.Hv / p.Hk);
