@@ -161,19 +161,23 @@ def test_gdn_front_verify_rows_equal_decode_rows(cfg_id):
         assert np.array_equal(f64(tail2), G.commit_tail(f64(c.tail0), f64(c.x), path))
 
 
-@pytest.mark.parametrize("cfg_id,width,dt", [(0, 1, None), (0, 4, None), (1, 8, None), (2, 4, None), (3, 4, None),
-                                             (4, 4, None), (1, 4, torch.float32), (4, 2, torch.float32)])
-def test_gdn_fused_equals_front_verify_norm(cfg_id, width, dt):
+@pytest.mark.parametrize("cfg_id,width,dt,overlap", [(0, 1, None, False), (0, 4, None, False), (1, 8, None, False),
+                                                     (2, 4, None, False), (3, 4, None, False), (4, 4, None, False),
+                                                     (1, 4, torch.float32, False), (4, 2, torch.float32, False),
+                                                     (3, 4, None, True), (4, 4, None, True)])
+def test_gdn_fused_equals_front_verify_norm(cfg_id, width, dt, overlap):
     """tv_gdn_tree_verify_fused gives the bits of tv_gdn_front ->
     tv_gdn_tree_verify -> tv_gdn_out_norm on every sequence of the workload's
     trees (one 8/16/64/32-node tree, four 16-node trees), for convolution
     widths 1 (no tail), 2, 4 and 8 (windows reaching past the root into each
     sequence's own tail), bf16 and fp32 layers (fp32 on the 27B shapes runs
-    the key-head clusters too); states and tails stay as they were."""
+    the key-head clusters too), plain and overlapped launches (programmatic
+    dependent launch, as a round runs them); states and tails stay as they
+    were."""
     cfg = synth.workload(cfg_id)
     sh = cfg.shapes
     parents = [synth.tree_and_tokens(cfg, s)[0] for s in range(cfg.n_seq)]
-    fused_vs_three(parents, sh.Hk, sh.Hv, sh.dk, dt or sh.kv_dtype, width, 1200 + 10 * cfg_id + width)
+    fused_vs_three(parents, sh.Hk, sh.Hv, sh.dk, dt or sh.kv_dtype, width, 1200 + 10 * cfg_id + width, overlap)
 
 
 @pytest.mark.parametrize("Hk,Hv,dk,n_seq,width", [(4, 8, 64, 2, 4), (2, 8, 128, 1, 3), (8, 8, 128, 3, 5),
@@ -188,7 +192,7 @@ def test_gdn_fused_other_head_shapes(Hk, Hv, dk, n_seq, width):
     fused_vs_three(parents, Hk, Hv, dk, torch.bfloat16, width, 1400 + Hk + Hv + dk + width)
 
 
-def fused_vs_three(parents, Hk, Hv, dk, dt, width, seed):
+def fused_vs_three(parents, Hk, Hv, dk, dt, width, seed, overlap=False):
     """tv_gdn_tree_verify_fused against tv_gdn_front -> tv_gdn_tree_verify ->
     tv_gdn_out_norm on the same inputs: bitwise equal outputs, states and
     tails untouched, status clean."""
@@ -205,7 +209,7 @@ def fused_vs_three(parents, Hk, Hv, dk, dt, width, seed):
     tails = [rn(max(width - 1, 1), C, d=dt) for _ in parents]
     S0 = [rn(sh.Hv, sh.dv, sh.dk, std=0.1) for _ in parents]
     scale = sh.dk ** -0.5
-    tree = B.Tree(parents)
+    tree = B.Tree(parents, overlap=overlap)
     B.tv_tree_prepare(tree)
     fl = B.GdnFrontLayer(sh.Hk, sh.Hv, sh.dk, sh.dv, wconv, tails, dt)
     e = lambda *shape, d=dt: torch.empty(*shape, dtype=d, device="cuda")
