@@ -396,9 +396,10 @@ __global__ void __launch_bounds__(32 * WARPS) gdn_verify_kernel(const GdnVerifyP
   MetaView mv = meta_view(const_cast<void*>(p.meta), p.n_total);
   const SeqInfo info = mv.seq[s];
   // The fused form may run in clusters of the CTAs that share a key head
-  // (they split its queries and keys by node, then exchange them): a CTA
-  // that leaves early still takes the cluster's two barriers, so none waits
-  // on it.  The status word can change under the launch, so CTAs of one
+  // (they split its queries and keys by node, then exchange them, and gather
+  // each head's outputs for the norm): a CTA that leaves early still takes
+  // the cluster's barriers (the exchange's and, with the norm inside, the
+  // gather's), so none waits on it.  The status word can change under the launch, so CTAs of one
   // cluster can take different paths here (each CTA decides as one: its
   // threads vote).
   uint32_t crank = 0, csize = 1;
