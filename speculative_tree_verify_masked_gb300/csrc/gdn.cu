@@ -26,6 +26,16 @@
 // query serving both rows) and CTAs of four or eight warps that share one
 // staged copy of the tree's inputs; leaves skip the update (nothing reads
 // their state).
+//
+// Fused form (tv_gdn_tree_verify_fused; "Adding a model", the Gated
+// DeltaNet layer with its gated norm; "The model layer", the convolution
+// tails).  The same kernel with the front end in its staging and the gated
+// norm after its visits: each node's query, key, value and gates are formed
+// from the raw projections in shared memory (front_gdn.cuh's operations in
+// tv_gdn_front's order), and the CTAs that share a key head run as one
+// thread-block cluster, splitting the key head's queries and keys by node
+// and gathering each (node, value head)'s outputs through distributed shared
+// memory for the norm.  The result is the three separate calls' bit for bit.
 #include "common.cuh"
 #include "front_gdn.cuh"
 #include "gdn_step.cuh"
