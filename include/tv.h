@@ -360,6 +360,20 @@ tv_status tv_gdn_tree_verify_fused(const tv_gdn_layer* layer, const tv_gdn_front
                                    const void* x, const float* a_raw, const float* b_raw, const void* z,
                                    const float* w_norm, void* out, float scale, tv_stream stream);
 
+/* The decode counterpart of tv_gdn_tree_verify_fused: tv_gdn_front (one token
+ * a sequence), the GDN half of tv_decode_step and tv_gdn_out_norm in one
+ * launch, one CTA per (value head, sequence).  The states advance in place
+ * as tv_decode_step advances them; the result and the states equal the three
+ * calls' bit for bit, so a row verified by tv_gdn_tree_verify_fused equals
+ * the same token decoded here.
+ *  x [n_seq][C], a_raw, b_raw [n_seq][Hv], z [n_seq][Hv][dv], w_norm [dv];
+ *  out [n_seq][Hv][dv]; errors go to *status (16-byte aligned), and a call
+ *  given a status word that holds an error does nothing.
+ * The tails are read only: run tv_gdn_conv_commit (tree NULL) afterwards. */
+tv_status tv_gdn_decode_fused(const tv_gdn_layer* layer, const tv_gdn_front_layer* front, int32_t n_seq,
+                              const void* x, const float* a_raw, const float* b_raw, const void* z,
+                              const float* w_norm, void* out, float scale, int32_t* status, tv_stream stream);
+
 /* Commit of the convolution tails: each sequence's tail becomes the last W-1
  * of (tail, x[path[0..a-1]]) for the accepted path of tv_accept_path (tree),
  * or of (tail, x[s]) for a decoded token (tree NULL, n_seq tokens).  Run it

@@ -114,6 +114,8 @@ def lib():
         L.tv_gdn_out_norm.argtypes = [F, c_int32, vp, vp, vp, vp, vp]
         L.tv_gdn_tree_verify_fused.restype = c_int32
         L.tv_gdn_tree_verify_fused.argtypes = [G, F, T, vp, vp, vp, vp, vp, vp, c_float, vp]
+        L.tv_gdn_decode_fused.restype = c_int32
+        L.tv_gdn_decode_fused.argtypes = [G, F, c_int32, vp, vp, vp, vp, vp, vp, c_float, vp, vp]
         L.tv_gdn_conv_commit.restype = c_int32
         L.tv_gdn_conv_commit.argtypes = [F, T, c_int32, vp, vp, vp, vp, vp]
         L.tv_kvpool_page_bytes.restype = c_size_t
@@ -144,7 +146,7 @@ EXPORTED = ["tv_status_string", "tv_version", "tv_tree_meta_bytes", "tv_tree_pre
             "tv_kvpool_create", "tv_kvpool_reserve", "tv_kvpool_commit_rows", "tv_kvpool_release_rows",
             "tv_kvpool_committed_bytes", "tv_kvpool_reserved_bytes", "tv_kvpool_destroy", "tv_attn_rope",
             "tv_attn_tree_verify_gated", "tv_attn_decode_gated", "tv_gdn_front", "tv_gdn_out_norm",
-            "tv_gdn_conv_commit", "tv_gdn_tree_verify_fused", "tv_wait_selftest"]
+            "tv_gdn_conv_commit", "tv_gdn_tree_verify_fused", "tv_gdn_decode_fused", "tv_wait_selftest"]
 
 
 def _check(code: int, where: str):
@@ -339,6 +341,13 @@ def tv_gdn_tree_verify_fused(layer: GdnLayer, front: GdnFrontLayer, tree: Tree, 
     _check(lib().tv_gdn_tree_verify_fused(ctypes.byref(layer.c), ctypes.byref(front.c), ctypes.byref(tree.c), _ptr(x),
                                           _ptr(a_raw), _ptr(b_raw), _ptr(z), _ptr(w_norm), _ptr(out), scale,
                                           _stream(stream)), "tv_gdn_tree_verify_fused")
+
+
+def tv_gdn_decode_fused(layer: GdnLayer, front: GdnFrontLayer, n_seq, x, a_raw, b_raw, z, w_norm, out, scale, status,
+                        stream=None):
+    _check(lib().tv_gdn_decode_fused(ctypes.byref(layer.c), ctypes.byref(front.c), n_seq, _ptr(x), _ptr(a_raw),
+                                     _ptr(b_raw), _ptr(z), _ptr(w_norm), _ptr(out), scale, _ptr(status),
+                                     _stream(stream)), "tv_gdn_decode_fused")
 
 
 def tv_accept_path(tree: Tree, tok, greedy, path, acc_len, bonus, stream=None):

@@ -864,6 +864,90 @@ __global__ void __launch_bounds__(128) gdn_decode_kernel(const GdnDecodeParams p
   }
 }
 
+// Fused decode: tv_gdn_front (one token a sequence), the decode step of
+// tv_decode_step and tv_gdn_out_norm in one kernel, one CTA of 256 threads
+// per (value head, sequence) owning all dv rows (RPG = dv / (256 / LPR) rows
+// a lane group, one after another), so the gated norm needs no other CTA.
+// Every value is formed as the three calls form it: the front end with
+// front_gdn.cuh's operations (queries and keys rounded to the layer type and
+// widened, as the decode kernel stages them), each row's step with
+// gdn_row_step, the norm with gated_norm_vals.
+struct GdnDecodeFusedParams {
+  float* S[TV_MAX_SEQ];
+  const void* tail[TV_MAX_SEQ];
+  const void* x;
+  const float* a_raw;
+  const float* b_raw;
+  const float* wconv;
+  const void* z;
+  const float* w_norm;
+  void* out;
+  int32_t* status;
+  int Hk, Hv, dv, C, W;
+  float scale;
+};
+
+template <typename T, int LPR>
+__global__ void __launch_bounds__(256) gdn_decode_fused_kernel(const GdnDecodeFusedParams p) {
+  constexpr int DK = 2 * kPairs * LPR, NT = 256, NG = NT / LPR, CPL = DK / 32;
+  const int h = blockIdx.x, s = blockIdx.y;
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  if (__syncthreads_or(status_bad(p.status))) return;
+  const int g = h / (p.Hv / p.Hk);
+  __shared__ __align__(16) float kb[DK];
+  __shared__ __align__(16) float qb[DK];
+  __shared__ float vbuf[DK];  // dv = dk
+  __shared__ T obuf[DK];
+  __shared__ float gates[2];
+  const T* x = static_cast<const T*>(p.x);
+  const T* tail = static_cast<const T*>(p.tail[s]);
+  int src[kMaxConvWidth];
+  conv_window(src, p.W, 0, s, nullptr, s);  // a decoded token: the tail, then itself
+  if (warp < 2) {
+    // warp 0 the query, warp 1 the key: convolution, SiLU, L2 norm, rounding
+    const int c0 = (warp == 0 ? g : p.Hk + g) * DK;
+    float val[CPL];
+#pragma unroll
+    for (int e = 0; e < CPL; e++) val[e] = conv_silu(x, tail, p.wconv, p.C, p.W, src, c0 + lane + 32 * e);
+    const float sc = warp_l2_scale<CPL>(val);
+    float* dst = warp == 0 ? qb : kb;
+#pragma unroll
+    for (int e = 0; e < CPL; e++) dst[lane + 32 * e] = to_f32(from_f32<T>(__fmul_rn(val[e], sc)));
+  }
+  for (int c = tid; c < p.dv; c += NT)
+    vbuf[c] = to_f32(from_f32<T>(conv_silu(x, tail, p.wconv, p.C, p.W, src, 2 * p.Hk * DK + h * p.dv + c)));
+  if (tid == 0) front_gates(p.a_raw[static_cast<size_t>(s) * p.Hv + h], p.b_raw[static_cast<size_t>(s) * p.Hv + h],
+                            gates[0], gates[1]);
+  __syncthreads();
+  const int gi = tid / LPR, j = tid % LPR;
+  f2_t kk[kPairs], qq[kPairs];
+  load_row<LPR>(kk, kb, j);
+  load_row<LPR>(qq, qb, j);
+  const float kq = kq_group<LPR>(kk, qq);
+  const float alpha = gates[0], beta = gates[1];
+  for (int row = gi; row < p.dv; row += NG) {
+    float* Srow = p.S[s] + (static_cast<size_t>(h) * p.dv + row) * DK;
+    f2_t st[kPairs];
+    load_row<LPR>(st, Srow, j);
+    const float o = gdn_row_step<LPR, true>(st, kk, qq, kq, vbuf[row], alpha, beta, p.scale, true);
+    store_row<LPR>(Srow, st, j);
+    if (j == 0) obuf[row] = from_f32<T>(o);
+  }
+  __syncthreads();
+  if (warp == 0) {
+    const size_t base = (static_cast<size_t>(s) * p.Hv + h) * p.dv;
+    const T* z = static_cast<const T*>(p.z) + base;
+    float ov[CPL], zv[CPL], wn[CPL];
+#pragma unroll
+    for (int e = 0; e < CPL; e++) {
+      ov[e] = to_f32(obuf[lane + 32 * e]);
+      zv[e] = to_f32(z[lane + 32 * e]);
+      wn[e] = p.w_norm[lane + 32 * e];
+    }
+    gated_norm_vals<T, CPL>(ov, zv, wn, static_cast<T*>(p.out) + base, lane);
+  }
+}
+
 static bool gdn_shape_ok(const tv_gdn_layer* l) {
   return l && (l->dtype == TV_F32 || l->dtype == TV_BF16) && l->Hk >= 1 && l->Hv >= l->Hk && l->Hv % l->Hk == 0 &&
          (l->dk == 64 || l->dk == 128) && l->dv >= 1 && l->dv <= 256 && l->S;
@@ -1090,4 +1174,43 @@ extern "C" tv_status tv_gdn_tree_verify_fused(const tv_gdn_layer* l, const tv_gd
   const tv_status ls = launch_status();
   if (ls != TV_OK || norm_in) return ls;
   return tv_gdn_out_norm(f, t->n_total, out, z, w_norm, out, stream);
+}
+
+extern "C" tv_status tv_gdn_decode_fused(const tv_gdn_layer* l, const tv_gdn_front_layer* f, int32_t n_seq,
+                                         const void* x, const float* a_raw, const float* b_raw, const void* z,
+                                         const float* w_norm, void* out, float scale, int32_t* status,
+                                         tv_stream stream) {
+  if (!l || !l->S || !f) return TV_ERR_ARG;
+  if (l->dtype != TV_F32 && l->dtype != TV_BF16) return TV_ERR_DTYPE;
+  if (!gdn_shape_ok(l) || !front_layer_ok(f)) return TV_ERR_SHAPE;
+  if (f->dtype != l->dtype || f->Hk != l->Hk || f->Hv != l->Hv || f->dk != l->dk || f->dv != l->dv)
+    return TV_ERR_SHAPE;
+  if (n_seq < 1 || n_seq > TV_MAX_SEQ || !x || !a_raw || !b_raw || !z || !w_norm || !out || !status)
+    return TV_ERR_ARG;
+  if (!aligned16(status)) return TV_ERR_ALIGN;
+  GdnDecodeFusedParams p{};
+  for (int s = 0; s < n_seq; s++) {
+    if (!l->S[s]) return TV_ERR_ARG;
+    if (!aligned16(l->S[s])) return TV_ERR_ALIGN;
+    if (f->width > 1 && !f->tail[s]) return TV_ERR_ARG;
+    p.S[s] = l->S[s];
+    p.tail[s] = f->tail[s];
+  }
+  p.x = x; p.a_raw = a_raw; p.b_raw = b_raw; p.wconv = f->wconv; p.z = z; p.w_norm = w_norm; p.out = out;
+  p.status = status;
+  p.Hk = l->Hk; p.Hv = l->Hv; p.dv = l->dv; p.C = 2 * l->Hk * l->dk + l->Hv * l->dv; p.W = f->width;
+  p.scale = scale;
+  cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
+  const dim3 grid(l->Hv, n_seq);
+  const bool bf = l->dtype == TV_BF16;
+  if (l->dk == 128) {
+    constexpr int LPR = lanes_per_row<128>();
+    if (bf) gdn_decode_fused_kernel<__nv_bfloat16, LPR><<<grid, 256, 0, st>>>(p);
+    else gdn_decode_fused_kernel<float, LPR><<<grid, 256, 0, st>>>(p);
+  } else {
+    constexpr int LPR = lanes_per_row<64>();
+    if (bf) gdn_decode_fused_kernel<__nv_bfloat16, LPR><<<grid, 256, 0, st>>>(p);
+    else gdn_decode_fused_kernel<float, LPR><<<grid, 256, 0, st>>>(p);
+  }
+  return launch_status();
 }

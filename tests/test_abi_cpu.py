@@ -174,8 +174,9 @@ def test_gdn_front_host_argument_errors(L):
 
 
 def test_gdn_fused_host_argument_errors(L):
-    """tv_gdn_tree_verify_fused rejects a missing or mismatched front-end
-    layer, a missing input and a misaligned output before any launch."""
+    """tv_gdn_tree_verify_fused and tv_gdn_decode_fused reject a missing or
+    mismatched front-end layer, a missing input, a misaligned output or
+    status word and a sequence count out of range before any launch."""
     vp = ctypes.c_void_p
     tails = (vp * 1)(vp(0x1000))
     states = (vp * 1)(vp(0x3000))
@@ -198,6 +199,15 @@ def test_gdn_fused_host_argument_errors(L):
     assert fused(ctypes.byref(no_tail)) == 1                                       # W > 1 needs each tail
     assert fused(ctypes.byref(f), x=None) == 1
     assert fused(ctypes.byref(f), out=vp(24)) == 4                                 # misaligned output
+    # the decode form: a status word is required and aligned, n_seq in range
+    dec = lambda n, st: L.tv_gdn_decode_fused(ctypes.byref(g), ctypes.byref(f), n, vp(16), vp(16), vp(16), vp(16),
+                                              vp(16), vp(16), 0.1, st, None)
+    assert dec(1, None) == 1
+    assert dec(0, vp(16)) == 1
+    assert dec(9, vp(16)) == 1
+    assert dec(1, vp(20)) == 4
+    assert L.tv_gdn_decode_fused(ctypes.byref(g), ctypes.byref(other), 1, vp(16), vp(16), vp(16), vp(16), vp(16),
+                                 vp(16), 0.1, vp(16), None) == 2
 
 
 def test_static_scratch_rejects_oversized_request_on_host(L):

@@ -258,3 +258,52 @@ def test_gdn_fused_after_a_malformed_tree_does_nothing():
     torch.cuda.synchronize()
     assert tree.status_code() == TV_ERR_TREE
     assert bool((out == 7.0).all()), "an output was written after the error"
+
+
+@pytest.mark.parametrize("cfg_id", [0, 2, 3])
+def test_gdn_fused_verify_rows_equal_fused_decode_rows(cfg_id):
+    """The fused forms keep the row-invariance rule ("Adding a model", step
+    4): each node verified by tv_gdn_tree_verify_fused equals the same token
+    decoded by tv_gdn_decode_fused after its ancestors (tails committed token
+    by token), bit for bit; and tv_gdn_decode_fused equals tv_gdn_front ->
+    tv_decode_step -> tv_gdn_out_norm, outputs and states."""
+    c = Case(cfg_id, 1500 + cfg_id)
+    tree = B.Tree([c.parent])
+    B.tv_tree_prepare(tree)
+    tail = c.tail0.clone()
+    fl = c.layer(tail)
+    S = c.S0.clone()
+    ver = torch.empty(c.n, c.Hv, c.dv, dtype=c.dt, device="cuda")
+    B.tv_gdn_tree_verify_fused(B.GdnLayer([S], c.Hk, c.dt), fl, tree, c.x, c.a_raw, c.b_raw, c.z, c.w_norm, ver,
+                               c.scale)
+    torch.cuda.synchronize()
+    assert tree.status_code() == 0
+    leaves = [i for i in range(c.n) if i not in c.parent]
+    rng = np.random.default_rng(cfg_id + 7)
+    ends = [max(range(c.n), key=lambda i: len(O.root_path(c.parent, i)))] + \
+        list(rng.choice(leaves, size=min(2, len(leaves)), replace=False))
+    status = torch.zeros(4, dtype=torch.int32, device="cuda")
+    for end in ends:
+        path = O.root_path(c.parent, int(end))
+        t1, t2 = c.tail0.clone(), c.tail0.clone()
+        f1, f2 = c.layer(t1), c.layer(t2)
+        S1, S2 = c.S0.clone(), c.S0.clone()
+        g1, g2 = B.GdnLayer([S1], c.Hk, c.dt), B.GdnLayer([S2], c.Hk, c.dt)
+        for j in path:
+            xj, aj, bj, zj = (c.x[j:j + 1].clone(), c.a_raw[j:j + 1].clone(), c.b_raw[j:j + 1].clone(),
+                              c.z[j:j + 1].clone())
+            fused = torch.empty(1, c.Hv, c.dv, dtype=c.dt, device="cuda")
+            B.tv_gdn_decode_fused(g1, f1, 1, xj, aj, bj, zj, c.w_norm, fused, c.scale, status)
+            B.tv_gdn_conv_commit(f1, None, 1, xj, status=status)
+            d = c.empty(1)
+            B.tv_gdn_front(f2, None, 1, xj, aj, bj, d["q"], d["k"], d["v"], d["alpha"], d["beta"], status)
+            B.tv_decode_step(None, None, g2, 1, None, 0, d["q"], d["k"], d["v"], d["alpha"], d["beta"], d["o"],
+                             c.scale, None, status)
+            B.tv_gdn_out_norm(f2, 1, d["o"], zj, c.w_norm, d["out"])
+            B.tv_gdn_conv_commit(f2, None, 1, xj, status=status)
+            torch.cuda.synchronize()
+            assert int(status[0]) == 0
+            assert torch.equal(bits(fused), bits(d["out"])), f"node {j}: fused decode != three calls"
+            assert torch.equal(bits(fused[0]), bits(ver[j])), f"node {j}: fused decode != fused verify row"
+        assert torch.equal(bits(S1), bits(S2)), f"path {path}: fused decode state != decode state"
+        assert torch.equal(bits(t1), bits(t2))
