@@ -889,11 +889,18 @@ struct GdnDecodeFusedParams {
 
 template <typename T, int LPR>
 __global__ void __launch_bounds__(256) gdn_decode_fused_kernel(const GdnDecodeFusedParams p) {
-  constexpr int DK = 2 * kPairs * LPR, NT = 256, NG = NT / LPR, CPL = DK / 32;
+  constexpr int DK = 2 * kPairs * LPR, NT = 256, NG = NT / LPR, CPL = DK / 32, RPG = DK / NG;
   const int h = blockIdx.x, s = blockIdx.y;
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  const int gi = tid / LPR, j = tid % LPR;
   if (__syncthreads_or(status_bad(p.status))) return;
   const int g = h / (p.Hv / p.Hk);
+  // this lane group's state rows (gi, gi + NG, ...) first: their loads run
+  // under the front end
+  f2_t st[RPG][kPairs];
+#pragma unroll
+  for (int i = 0; i < RPG; i++)
+    load_row<LPR>(st[i], p.S[s] + (static_cast<size_t>(h) * p.dv + gi + i * NG) * DK, j);
   __shared__ __align__(16) float kb[DK];
   __shared__ __align__(16) float qb[DK];
   __shared__ float vbuf[DK];  // dv = dk
@@ -919,18 +926,16 @@ __global__ void __launch_bounds__(256) gdn_decode_fused_kernel(const GdnDecodeFu
   if (tid == 0) front_gates(p.a_raw[static_cast<size_t>(s) * p.Hv + h], p.b_raw[static_cast<size_t>(s) * p.Hv + h],
                             gates[0], gates[1]);
   __syncthreads();
-  const int gi = tid / LPR, j = tid % LPR;
   f2_t kk[kPairs], qq[kPairs];
   load_row<LPR>(kk, kb, j);
   load_row<LPR>(qq, qb, j);
   const float kq = kq_group<LPR>(kk, qq);
   const float alpha = gates[0], beta = gates[1];
-  for (int row = gi; row < p.dv; row += NG) {
-    float* Srow = p.S[s] + (static_cast<size_t>(h) * p.dv + row) * DK;
-    f2_t st[kPairs];
-    load_row<LPR>(st, Srow, j);
-    const float o = gdn_row_step<LPR, true>(st, kk, qq, kq, vbuf[row], alpha, beta, p.scale, true);
-    store_row<LPR>(Srow, st, j);
+#pragma unroll
+  for (int i = 0; i < RPG; i++) {
+    const int row = gi + i * NG;
+    const float o = gdn_row_step<LPR, true>(st[i], kk, qq, kq, vbuf[row], alpha, beta, p.scale, true);
+    store_row<LPR>(p.S[s] + (static_cast<size_t>(h) * p.dv + row) * DK, st[i], j);
     if (j == 0) obuf[row] = from_f32<T>(o);
   }
   __syncthreads();
