@@ -515,9 +515,22 @@ def run_ours(args, rank, world, local_rank):
         host_in.copy_(io_in)
         host_out = torch.empty(io_out.shape, dtype=torch.uint8, pin_memory=True)
 
+        # the trees, tokens and the first tenth of the layers' inputs go in
+        # on the round's stream; the rest on a copy stream, which the round
+        # waits for just before the first layer that reads it
+        cut, li_cut = r.input_split(0.1)
+        side = torch.cuda.Stream()
+        arrived = torch.cuda.Event()
+
         def e2e_step():
-            io_in.copy_(host_in, non_blocking=True)
-            r.run()
+            io_in[:cut].copy_(host_in[:cut], non_blocking=True)
+            side.wait_stream(stream)
+            with torch.cuda.stream(side):
+                io_in[cut:].copy_(host_in[cut:], non_blocking=True)
+                arrived.record(side)
+            r.run(layer_waits={li_cut: arrived} if li_cut is not None else None)
+            if li_cut is None:
+                stream.wait_event(arrived)
             host_out.copy_(io_out, non_blocking=True)
             stream.synchronize()
 
@@ -535,10 +548,12 @@ def run_ours(args, rank, world, local_rank):
         assert r.status() == 0
         e2e = {"value": round(job_throughput(nodes_per_round, world, e2e_ms), 1), "unit": UNIT,
                "h2d_bytes_per_step": int(io_in.numel()), "d2h_bytes_per_step": int(io_out.numel()),
-               "h2d_copies_per_step": 1, "d2h_copies_per_step": 1, "ms_per_step": round(e2e_ms, 4),
+               "h2d_copies_per_step": 2, "d2h_copies_per_step": 1, "ms_per_step": round(e2e_ms, 4),
                "steps": n_e2e,
                "path": "eager C-ABI calls (ctypes); the round's host inputs (trees, tokens, every layer's node "
-                       "inputs) in from one pinned buffer, the accepted paths, lengths and bonus tokens out"}
+                       "inputs) in from one pinned buffer in two copies (the first tenth on the round's "
+                       "stream, the rest on a copy stream the round waits for before the first layer that "
+                       "reads it), the accepted paths, lengths and bonus tokens out"}
 
     # --- CPU baseline: the oracle on its stated sample (rank 0, N = 1) -------
     cpu = None

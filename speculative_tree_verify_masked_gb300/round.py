@@ -153,7 +153,7 @@ class VerifyRound:
             else:
                 (self.attn.get(owner) or self.gdn[owner])[name] = t
 
-        def pack(keys):
+        def pack(keys, record=False):
             offs, total = [], 0
             for key in keys:
                 t = get(key)
@@ -166,14 +166,27 @@ class VerifyRound:
                 v = buf[o:o + nb].view(t.dtype).view(t.shape)
                 v.copy_(t)
                 put(key, v)
+            if record:
+                self.io_in_offsets = dict(zip(keys, offs))
             return buf
 
-        self.io_in = pack(ins)
+        self.io_in = pack(ins, record=True)
         self.io_out = pack([("r", "path"), ("r", "acc_len"), ("r", "bonus")])
         self.tree.c.node_off = self.tree.node_off.data_ptr()
         self.tree.c.parent = self.tree.parent.data_ptr()
         self._build_commit_args()
         return self.io_in, self.io_out
+
+    def input_split(self, frac: float):
+        """(byte offset, layer): the packed inputs from the first layer whose
+        inputs start at or past frac of the buffer, and that layer; the bytes
+        before it hold the trees, tokens and the earlier layers' inputs."""
+        total = self.io_in.numel()
+        for li in self.layers:
+            first = min(o for (owner, _), o in self.io_in_offsets.items() if owner == li)
+            if first >= frac * total:
+                return first, li
+        return total, None
 
     def _alloc_ws(self):
         ws_bytes = 0
@@ -218,9 +231,15 @@ class VerifyRound:
             B.tv_gdn_tree_verify(g["layer"], self.tree, g["q"], g["k"], g["v"], g["alpha"], g["beta"], g["out"],
                                  self.gdn_scale, stream)
 
-    def verify(self, stream=None):
+    def verify(self, stream=None, layer_waits=None):
+        """Prepare, then every layer's verify.  layer_waits maps a layer to a
+        CUDA event the stream waits for before that layer (inputs that arrive
+        by a copy on another stream)."""
         self.prepare(stream)
         for li in self.layers:
+            if layer_waits and li in layer_waits:
+                s = stream if isinstance(stream, torch.cuda.Stream) else torch.cuda.current_stream()
+                s.wait_event(layer_waits[li])
             marks = self._marks is not None
             if marks:
                 # external events become timing-capable record nodes of the graph
@@ -238,13 +257,13 @@ class VerifyRound:
     def commit(self, stream=None):
         B.tv_commit_path(self.tree, self.path, self.acc_len, self.commit_args, self.len, stream)
 
-    def run(self, stream=None, reset_len: bool = True):
+    def run(self, stream=None, reset_len: bool = True, layer_waits=None):
         """One round.  With reset_len the context length is first restored so
         repeated rounds do the same work (the caches' rows past it and the
         states are overwritten by each commit)."""
         if reset_len:
             self.len.copy_(self.len0)
-        self.verify(stream)
+        self.verify(stream, layer_waits)
         self.accept(stream)
         self.commit(stream)
 
