@@ -703,7 +703,7 @@ __global__ void __launch_bounds__(32 * WARPS) gdn_verify_kernel(const GdnVerifyP
     // entry, key, query, gates and value are loaded during this one (the
     // index clamped at the last visit, so the loads need no branch).
     const int last = first + cnt - 1;
-#pragma unroll 2
+#pragma unroll 4
     for (int v = first; v <= last; v++) {
       const int node = e & 0xFF;
       const bool hc = (e >> 24) & 1;
